@@ -1,0 +1,300 @@
+"""Pins for the fp64 CPU oracle, checked against things other than itself.
+
+Each test ties one part of the oracle to a closed form, a worked example
+derived by hand from the pages (tests/golden/hand_cases.json), a mathematical
+invariant, a library routine on a special case, or brute force on tiny inputs.
+Sources: the RAPID explainer page ("2) 推理时知识迁移" mixture equation,
+"3) 候选验证机制（伪代码）" loop), the speculative-decoding explainer page
+("修改的拒绝采样", "加速效果分析") and the EAGLE explainer page
+("1. 为什么无损": resample from max(0, p - q)).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+import torch
+
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
+
+
+# --------------------------------------------------------------------------- softmax
+def test_softmax_closed_form(oracle_mod):
+    p = oracle_mod.softmax([0.0, math.log(2.0), math.log(3.0)])
+    np.testing.assert_allclose(p, [1 / 6, 2 / 6, 3 / 6], rtol=0, atol=1e-15)
+
+
+def test_softmax_large_logits_need_the_max_shift(oracle_mod):
+    # exp(1000) overflows: only a max-shifted softmax gets [0.5, 0.5]
+    np.testing.assert_array_equal(oracle_mod.softmax([1000.0, 1000.0]), [0.5, 0.5])
+    np.testing.assert_allclose(oracle_mod.softmax([-1000.0, -1000.0 + math.log(3.0)]),
+                               [0.25, 0.75], atol=1e-15)
+
+
+def test_softmax_single_entry_and_library(oracle_mod):
+    np.testing.assert_array_equal(oracle_mod.softmax([3.5]), [1.0])
+    rng = np.random.default_rng(1)
+    for V in (2, 7, 1000, 50_000):
+        z = rng.normal(0, 4, V)
+        np.testing.assert_allclose(oracle_mod.softmax(z), scipy.special.softmax(z),
+                                   rtol=1e-12, atol=1e-300)
+
+
+# --------------------------------------------------------------------------- mixtures
+def test_mix_prob_special_values(oracle_mod):
+    pt = np.array([0.5, 0.3, 0.2])
+    pq = np.array([0.2, 0.2, 0.6])
+    np.testing.assert_array_equal(oracle_mod.mix_prob(pt, pq, 0.0), pt)
+    np.testing.assert_array_equal(oracle_mod.mix_prob(pt, pq, 1.0), pq)
+    # lambda = 1/4 by hand: 0.75*pt + 0.25*pq
+    np.testing.assert_allclose(oracle_mod.mix_prob(pt, pq, 0.25), [0.425, 0.275, 0.3],
+                               atol=1e-15)
+
+
+def test_mix_logit_closed_forms(oracle_mod):
+    # V = 2: p~_0 = sigmoid(w_0 - w_1) with w = (1-l) z_t + l z_q
+    zt = np.array([0.7, -1.1])
+    zq = np.array([-0.4, 2.0])
+    for lam in (0.0, 0.2, 0.5, 1.0):
+        d = (1 - lam) * (zt[0] - zt[1]) + lam * (zq[0] - zq[1])
+        got = oracle_mod.mix_logit(zt, zq, lam)
+        np.testing.assert_allclose(got, [scipy.special.expit(d), scipy.special.expit(-d)],
+                                   atol=1e-15)
+    # lambda = 1/2: the logit mixture is the normalised geometric mean sqrt(p_t q)
+    rng = np.random.default_rng(2)
+    zt = rng.normal(0, 2, 64)
+    zq = rng.normal(0, 2, 64)
+    g = np.sqrt(scipy.special.softmax(zt) * scipy.special.softmax(zq))
+    np.testing.assert_allclose(oracle_mod.mix_logit(zt, zq, 0.5), g / g.sum(), rtol=1e-12)
+
+
+def test_rows_sum_to_one(oracle_mod):
+    w = workloads.WORKLOADS[3].scaled(B=2, V=4099)
+    x = workloads.make_inputs(w)
+    for mode in (oracle_mod.PROB_MIX, oracle_mod.LOGIT_MIX):
+        for b in range(2):
+            pt, q = oracle_mod.rows(x["target_logits"][b], x["draft_logits"][b],
+                                    float(x["lam"][b]), mode)
+            np.testing.assert_allclose(pt.sum(axis=1), 1.0, atol=1e-12)
+            np.testing.assert_allclose(q.sum(axis=1), 1.0, atol=1e-12)
+            assert (pt >= 0).all() and (q >= 0).all()
+
+
+def test_lambda_zero_is_plain_target(oracle_mod):
+    w = workloads.WORKLOADS[1].scaled(V=257)
+    x = workloads.make_inputs(w)
+    for mode in (oracle_mod.PROB_MIX, oracle_mod.LOGIT_MIX):
+        pt, q = oracle_mod.rows(x["target_logits"][0], x["draft_logits"][0], 0.0, mode)
+        for i in range(w.K + 1):
+            ref = scipy.special.softmax(x["target_logits"][0, i].double().numpy())
+            np.testing.assert_allclose(pt[i], ref, rtol=1e-12)
+        for i in range(w.K):
+            ref = scipy.special.softmax(x["draft_logits"][0, i].double().numpy())
+            np.testing.assert_allclose(q[i], ref, rtol=1e-12)
+
+
+# --------------------------------------------------------------------------- inverse CDF
+def test_inverse_cdf_hand_cases(oracle_mod):
+    w = [1.0, 2.0, 3.0, 0.0]       # CDF boundaries 1/6, 1/2, 1
+    assert oracle_mod.sample_inverse_cdf(w, 0.0)[0] == 0
+    assert oracle_mod.sample_inverse_cdf(w, 0.1)[0] == 0
+    assert oracle_mod.sample_inverse_cdf(w, 0.2)[0] == 1
+    assert oracle_mod.sample_inverse_cdf(w, 0.49)[0] == 1
+    assert oracle_mod.sample_inverse_cdf(w, 0.51)[0] == 2
+    assert oracle_mod.sample_inverse_cdf(w, 0.999999)[0] == 2
+    assert oracle_mod.sample_inverse_cdf([0.0, 0.0], 0.5)[0] == -1
+    # u = 1 leaves no prefix strictly above u*W: the last positive weight is taken
+    idx, fb, _ = oracle_mod.sample_inverse_cdf([0.5, 0.25, 0.0], 1.0)
+    assert idx == 1 and fb
+    # the margin is the distance of u to the nearest boundary C_k / W
+    _, _, m = oracle_mod.sample_inverse_cdf(w, 0.49)
+    assert m == pytest.approx(0.01, abs=1e-12)
+
+
+def test_inverse_cdf_maps_uniform_grid_to_the_distribution(oracle_mod):
+    # Midpoints of N equal cells: each index is hit N*w_v/W times up to one
+    # cell per boundary.  Zero-weight indices are never hit.
+    rng = np.random.default_rng(3)
+    w = rng.random(13) * (rng.random(13) > 0.3)
+    N = 20000
+    counts = np.zeros(13)
+    for k in range(N):
+        counts[oracle_mod.sample_inverse_cdf(w, (k + 0.5) / N)[0]] += 1
+    assert (counts[w == 0] == 0).all()
+    np.testing.assert_allclose(counts / N, w / w.sum(), atol=1.0 / N + 1e-12)
+
+
+# --------------------------------------------------------------------------- worked examples
+def _golden_cases():
+    with open(GOLDEN) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c["name"])
+def test_hand_worked_examples(oracle_mod, case):
+    pt = np.array(case["p_t"], np.float64)
+    q = np.array(case["q"], np.float64)
+    K = q.shape[0]
+    zt = np.log(pt).astype(np.float32)[None]
+    zq = np.log(q).astype(np.float32)[None]
+    mode = oracle_mod.PROB_MIX if case["mode"] == "prob" else oracle_mod.LOGIT_MIX
+    r = oracle_mod.verify(zt, zq, np.array([case["tokens"]], np.int32),
+                          np.array([case["u_accept"]], np.float32),
+                          np.array([case["u_resample"]], np.float32),
+                          np.array([case["lam"]], np.float32), mode=mode)
+    assert r.tokens[0].tolist() == case["expect_tokens"]
+    assert int(r.n_accepted[0]) == case["expect_n"]
+    if "expect_ratio" in case:
+        np.testing.assert_allclose(r.ratio[0], case["expect_ratio"], rtol=2e-6)
+        np.testing.assert_allclose(r.alpha[0], case["expect_alpha"], rtol=2e-6)
+
+
+# --------------------------------------------------------------------------- exactness
+def _lattice(N, g):
+    i = np.arange(N, dtype=np.float64)
+    return ((i + 0.5) / N).astype(np.float32), (np.mod(i * g + 0.5, N) / N).astype(np.float32)
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+@pytest.mark.parametrize("lam", [0.0, 0.3, 0.8])
+def test_output_distribution_is_ptilde_by_quadrature(oracle_mod, mode, lam):
+    """Brute force over the draft token and a rank-1 lattice of uniform pairs.
+
+    The token emitted at position 0 must be distributed as p~_0 (accept with
+    min(1, p~/q), else resample max(0, p~ - q)), and the bonus token, given
+    that the draft passed, as the target softmax of row 1.
+    """
+    rng = np.random.default_rng(7 + mode)
+    V = 5
+    zt = rng.normal(0, 1.5, (1, 2, V)).astype(np.float32)
+    zq = rng.normal(0, 1.5, (1, 1, V)).astype(np.float32)
+    ptilde, q = oracle_mod.rows(zt[0], zq[0], lam, mode)
+    N = 1 << 15
+    ua, ur = _lattice(N, 20261)          # generator close to N / golden ratio, odd
+    dist0 = np.zeros(V)
+    bonus = np.zeros(V)
+    bonus_w = 0.0
+    for x in range(V):
+        r = oracle_mod.verify(np.broadcast_to(zt, (N, 2, V)), np.broadcast_to(zq, (N, 1, V)),
+                              np.full((N, 1), x, np.int32), ua[:, None], ur,
+                              np.full(N, lam, np.float32), mode=mode, diagnostics=False)
+        t0 = r.tokens[:, 0]
+        dist0 += q[0, x] * np.bincount(t0, minlength=V) / N
+        acc = r.n_accepted == 1
+        bonus += q[0, x] * np.bincount(r.tokens[acc, 1], minlength=V) / N
+        bonus_w += q[0, x] * acc.mean()
+    np.testing.assert_allclose(dist0, ptilde[0], atol=2e-3)
+    np.testing.assert_allclose(bonus / bonus_w, scipy.special.softmax(zt[0, 1].astype(np.float64)),
+                               atol=2e-3)
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+def test_chi_square_and_acceptance_rate_monte_carlo(oracle_mod, mode):
+    """Monte Carlo with the exactness workload's recipe at V = 8, K = 2."""
+    w = workloads.WORKLOADS[5].scaled(B=200_000, K=2, V=8)
+    x = workloads.make_inputs(w, lam=0.4)
+    r = oracle_mod.verify(x["target_logits"], x["draft_logits"], x["draft_tokens"],
+                          x["u_accept"], x["u_resample"], x["lam"], mode=mode)
+    ptilde, q = oracle_mod.rows(x["target_logits"][0], x["draft_logits"][0], float(x["lam"][0]),
+                                mode)
+    n = r.n_accepted
+    for j in range(w.K + 1):
+        reached = n >= j
+        obs = np.bincount(r.tokens[reached, j], minlength=w.V)
+        exp = ptilde[j] * reached.sum()
+        stat, pval = scipy.stats.chisquare(obs, exp)
+        assert pval > 1e-4, (j, stat, pval)
+    # P(accept at i | reached i) = sum_v min(p~, q) = 1 - TV(p~, q)
+    for i in range(w.K):
+        alpha = r.alpha[0, i]
+        assert alpha == pytest.approx(1 - 0.5 * np.abs(ptilde[i] - q[i]).sum(), abs=1e-12)
+        reached = n >= i
+        acc = (n[reached] > i).mean()
+        sigma = math.sqrt(alpha * (1 - alpha) / reached.sum())
+        assert abs(acc - alpha) < 5 * sigma, (i, acc, alpha, sigma)
+
+
+def test_expected_tokens_formula_truncated(oracle_mod):
+    """With the same alpha at every position, the mean number of emitted tokens
+    is 1 + a + ... + a^K = (1 - a^(K+1)) / (1 - a) (the explainer's
+    1/(1 - r) series, cut at the K drafted tokens)."""
+    K, V, B = 4, 16, 100_000
+    rng = np.random.default_rng(11)
+    zt1 = rng.normal(0, 1.5, V).astype(np.float32)
+    zq1 = rng.normal(0, 1.5, V).astype(np.float32)
+    zt = np.broadcast_to(zt1, (B, K + 1, V))
+    zq = np.broadcast_to(zq1, (B, K, V))
+    g = torch.Generator().manual_seed(5)
+    gum = -torch.log(-torch.log(torch.rand((B, K, V), generator=g).clamp_min(1e-30)))
+    tok = torch.argmax(torch.from_numpy(zq.copy()) + gum, dim=-1).to(torch.int32)
+    ua = torch.rand((B, K), generator=g)
+    ur = torch.rand((B,), generator=g)
+    r = oracle_mod.verify(zt, zq, tok, ua, ur, np.full(B, 0.3, np.float32))
+    a = r.alpha[0, 0]
+    assert np.allclose(r.alpha[0], a)
+    emitted = r.n_accepted + 1
+    mean = (1 - a ** (K + 1)) / (1 - a)
+    ex2 = sum((2 * k + 1) * a ** k for k in range(K + 1))  # E[m^2], m = tokens emitted
+    sd = math.sqrt((ex2 - mean * mean) / B)
+    assert abs(emitted.mean() - mean) < 5 * sd
+
+
+# --------------------------------------------------------------------------- special cases
+def test_identical_draft_and_target_accepts_everything(oracle_mod):
+    w = workloads.WORKLOADS[4].scaled(B=8, V=3001)
+    x = workloads.make_inputs(w)
+    h = w.B // 2
+    for mode in (0, 1):
+        for lam in (0.0, 0.2):
+            r = oracle_mod.verify(x["target_logits"][h:], x["draft_logits"][h:],
+                                  x["draft_tokens"][h:], x["u_accept"][h:],
+                                  x["u_resample"][h:], np.full(w.B - h, lam, np.float32),
+                                  mode=mode)
+            assert (r.n_accepted == w.K).all()
+            assert (r.flags & oracle_mod.FLAG_BONUS).all()
+
+
+def test_lambda_one_prob_mode_accepts_everything(oracle_mod):
+    w = workloads.WORKLOADS[3].scaled(B=4, V=2049)
+    x = workloads.make_inputs(w, lam=1.0)
+    r = oracle_mod.verify(x["target_logits"], x["draft_logits"], x["draft_tokens"],
+                          x["u_accept"], x["u_resample"], x["lam"], mode=0)
+    assert (r.n_accepted == w.K).all()
+
+
+def test_zero_uniform_accepts_unless_ptilde_is_zero(oracle_mod):
+    w = workloads.WORKLOADS[1].scaled(B=16, V=101)
+    x = workloads.make_inputs(w)
+    ua = torch.zeros_like(x["u_accept"])
+    r = oracle_mod.verify(x["target_logits"], x["draft_logits"], x["draft_tokens"], ua,
+                          x["u_resample"], x["lam"])
+    assert (r.n_accepted == w.K).all()
+    # p~(x) = 0 with q(x) > 0 (logits of -inf-like size) rejects even at u = 0
+    zt = np.array([[[-200.0, 0.0], [0.0, 0.0]]], np.float32)
+    zq = np.array([[[0.0, 0.0]]], np.float32)
+    r = oracle_mod.verify(zt, zq, np.array([[0]], np.int32), np.zeros((1, 1), np.float32),
+                          np.array([0.5], np.float32), np.array([0.0], np.float32))
+    # p~(x) = e^-200 / (1 + e^-200) > 0 in fp64, so this still accepts
+    assert r.n_accepted[0] == 1
+    # push the target probability of x to an exact zero
+    zt[0, 0, 0] = -1e30
+    r = oracle_mod.verify(zt, zq, np.array([[0]], np.int32), np.zeros((1, 1), np.float32),
+                          np.array([0.5], np.float32), np.array([0.0], np.float32))
+    assert r.n_accepted[0] == 0 and r.tokens[0].tolist() == [1, -1]
+
+
+def test_seq_range_and_threads_do_not_change_results(oracle_mod):
+    w = workloads.WORKLOADS[3].scaled(B=12, V=999)
+    x = workloads.make_inputs(w)
+    a = oracle_mod.verify(x["target_logits"], x["draft_logits"], x["draft_tokens"],
+                          x["u_accept"], x["u_resample"], x["lam"], threads=1)
+    b = oracle_mod.verify(x["target_logits"], x["draft_logits"], x["draft_tokens"],
+                          x["u_accept"], x["u_resample"], x["lam"], threads=5)
+    np.testing.assert_array_equal(a.tokens, b.tokens)
+    np.testing.assert_array_equal(a.n_accepted, b.n_accepted)
+    np.testing.assert_array_equal(a.ratio, b.ratio)
