@@ -1,0 +1,430 @@
+"""Benchmark of the verify/accept step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 4] [--mode prob|logit]
+    python bench.py --impl reference ...      # the fp64 CPU oracle, timed on the host cores
+
+A step is one specv_verify call over the whole batch of the chosen workload
+(default: B=256 sequences, K=8 drafts, V=128256, fp32 logits -- the batched
+128K-vocabulary workload).  The metric is verified draft rows per second,
+B*K per step; the roofline line reports the achieved HBM bandwidth of the
+verify kernel with the algorithmic bytes (2K+1)*B*V*sizeof(dtype) per launch.
+The inputs (2.2 GB) are larger than L2, so no flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs the same per-GPU batch on its own GPU
+(weak scaling, no collective in the data path); the reported value is the
+sum of all ranks' rows over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "verified draft rows/sec (B·K) and achieved HBM GB/s vs GB300 peak, 1 GPU"
+UNIT = "rows/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rows_kernel_batched_v128256_f32.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_specv_gb300", "csrc", f)
+                  for f in ("specv_rows.cu", "specv_device.cuh")]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="specv", choices=["specv", "reference"])
+    ap.add_argument("--config", type=int, default=4, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--mode", default="prob", choices=["prob", "logit"])
+    ap.add_argument("--B", type=int, default=None, help="override the batch size (profiling)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every step from the host instead of replaying a CUDA graph")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source for this workload; else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if line.startswith("bench-key ") and ":" in line:
+            k, v = line[len("bench-key "):].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    if vals.get("workload") != config_name:
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def cpu_baseline(w, mode, target_seconds, host_inputs=None):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload."""
+    import oracle
+    oracle.build()
+    if host_inputs is None:
+        nb = min(w.B, 16)
+        host_inputs = workloads.make_inputs(w.scaled(B=nb), "cpu")
+    xh = host_inputs
+    B = xh["target_logits"].shape[0]
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    passes = 0
+    seqs = 0
+    while True:
+        oracle.verify(xh["target_logits"], xh["draft_logits"], xh["draft_tokens"],
+                      xh["u_accept"], xh["u_resample"], xh["lam"], mode=mode,
+                      diagnostics=False, threads=threads)
+        passes += 1
+        seqs += B
+        el = time.perf_counter() - t0
+        if el >= target_seconds or passes >= 50:
+            break
+    rows = seqs * w.K
+    return {"value": rows / el, "unit": UNIT, "cores": min(threads, B), "kind": "oracle",
+            "sample": f"{passes} pass(es) over {B} sequences of {w.name} (K={w.K}, V={w.V}, "
+                      f"{w.dtype}); {el:.1f} s wall on {min(threads, B)} host threads"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS[args.config]
+    mode = 0 if args.mode == "prob" else 1
+    import oracle
+    oracle.build()
+    nb = min(w.B, 8)
+    xh = workloads.make_inputs(w.scaled(B=nb), "cpu")
+    threads = os.cpu_count() or 1
+
+    def step():
+        oracle.verify(xh["target_logits"], xh["draft_logits"], xh["draft_tokens"], xh["u_accept"],
+                      xh["u_resample"], xh["lam"], mode=mode, diagnostics=False, threads=threads)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    rows = nb * w.K * args.steps
+    value = rows / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "logits": w.dtype,
+                   "mode": args.mode, "sample_sequences_per_step": nb},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(threads, nb), "kind": "oracle",
+                         "sample": f"{nb} sequences of {w.name} per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import speculative_decoding_verification_specv_gb300 as specv
+    specv.load(build_if_missing=True)
+
+    w = workloads.WORKLOADS[args.config]
+    if args.B:
+        w = w.scaled(B=args.B, name=f"{w.name}-B{args.B}")
+    mode = 0 if args.mode == "prob" else 1
+    x = workloads.make_inputs(w, dev, seed_offset=rank)
+    stream = torch.cuda.current_stream(dev)
+    out_tok = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((w.B,), dtype=torch.int32, device=dev)
+    call_args = (x["target_logits"], x["draft_logits"], x["draft_tokens"], x["u_accept"],
+                 x["u_resample"], x["lam"])
+
+    def launch():
+        specv.verify(*call_args, mode=mode, out_tokens=out_tok, out_n_accepted=out_n,
+                     stream=torch.cuda.current_stream(dev))
+
+    # One step = one specv_verify call.  By default it is captured once in a
+    # CUDA graph (kernel, workspace alloc/memset/free nodes) and replayed, so
+    # the device time is not hidden behind host launch overhead.
+    graph = None
+    if not args.no_graph:
+        launch()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            launch()
+        torch.cuda.synchronize(dev)
+
+    def step():
+        if graph is not None:
+            graph.replay()
+        else:
+            launch()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # Working sets smaller than twice the L2 are re-read from L2 by the next
+    # step; for those the L2 is flushed (a 2x-L2 buffer is written) before
+    # every timed step, outside the per-step events.
+    try:
+        l2_bytes = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    except Exception:
+        l2_bytes = 126 * 2**20
+    flush_buf = None
+    if w.roofline_bytes < 2 * l2_bytes:
+        flush_buf = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        t_start.record(stream)
+        for i in range(K):
+            if flush_buf is not None:
+                flush_buf.fill_(float(i))
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    per_call_ms = [a.elapsed_time(b) for a, b in ev]
+    if flush_buf is not None:  # the timed region holds the flushes: count the steps only
+        total_ms = sum(per_call_ms)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    rows_per_step = w.B * w.K
+    value = rows_per_step * K * ws / (total_ms / 1e3)
+    mean_accepted = float(out_n.float().mean().item())
+
+    # end to end: pinned host inputs -> device, verify, result -> host, every step
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in x.items()}
+        for k, v in x.items():
+            host[k].copy_(v)
+        dev_in = {k: torch.empty_like(v) for k, v in x.items()}
+        host_tok = torch.empty((w.B, w.K + 1), dtype=torch.int32, pin_memory=True)
+        host_n = torch.empty((w.B,), dtype=torch.int32, pin_memory=True)
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = host_tok.numel() * 4 + host_n.numel() * 4
+
+        def e2e_step():
+            for k in dev_in:
+                dev_in[k].copy_(host[k], non_blocking=True)
+            specv.verify(dev_in["target_logits"], dev_in["draft_logits"], dev_in["draft_tokens"],
+                         dev_in["u_accept"], dev_in["u_resample"], dev_in["lam"], mode=mode,
+                         out_tokens=out_tok, out_n_accepted=out_n, stream=stream)
+            host_tok.copy_(out_tok, non_blocking=True)
+            host_n.copy_(out_n, non_blocking=True)
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e_steps = max(3, min(K, 10))
+        barrier()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e_ms = a.elapsed_time(b)
+        if ws > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": rows_per_step * e_steps * ws / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+               "ms_per_step": e_ms / e_steps}
+        del dev_in, host
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    plan = specv.plan(w.B, w.K, w.V, 1 if w.dtype == "bf16" else 0, mode)
+    kern_ms = statistics.mean(per_call_ms)
+    alg_bytes = w.roofline_bytes
+    achieved = alg_bytes / (kern_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    traffic = profiled_traffic(w.name)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                "kernel": "rows_kernel" if plan["kernel"] == "rows" else "tile_kernel",
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "launch_ms_mean": kern_ms, "launch_ms_min": min(per_call_ms),
+                "timing": ("CUDA events around each replay of a CUDA graph holding one "
+                           "specv_verify call" if graph is not None else
+                           "CUDA events around each specv_verify call") +
+                          " on its stream (the kernel plus a B*4-byte workspace memset)"}
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        cpu = cpu_baseline(w, mode, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "logits": w.dtype,
+                   "mode": args.mode, "lambda": list(w.lam), "structure": w.structure,
+                   "plan": plan, "graph_replay": graph is not None,
+                   "l2": "L2 flushed before every timed step (2x-L2 write, outside the step "
+                         "events)" if flush_buf is not None else
+                         "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{ws} (batch per GPU fixed)"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
+        "gpu_launches": K, "mean_accepted": mean_accepted,
+        "hbm_gbs_step": alg_bytes * ws / (total_ms / K / 1e3) / 1e9,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,143 @@
+/*
+ * specv.h -- C ABI of libspecv.so: the speculative-decoding verify/accept step
+ * with RAPID's inference-time knowledge transfer, on one GB300 (sm_103a).
+ *
+ * What the step computes (sources, by page title and section):
+ *   "RAPID：基于检索增强的推测解码长上下文推理"
+ *     - "2) 推理时知识迁移", displayed equation: the enhanced target
+ *       p~ = (1 - lambda) * p_t + lambda * p_q  (probability mixture);
+ *     - "3) 候选验证机制（伪代码）": softmax of the enhanced target row and
+ *       of the draft row, r ~ U(0,1), accept token i iff
+ *       r < min(1, p~(x_i) / q(x_i)), otherwise resample and stop.  The
+ *       pseudocode mixes logits before the softmax; that reading is the
+ *       logit mode, p~ = softmax((1 - lambda) * z_t + lambda * z_q).
+ *   "大模型推理的Speculative Decoding原理详解", "数学原理 / 修改的拒绝采样":
+ *       the first rejected position ends the step; the rest of the draft is
+ *       discarded.
+ *   "投机解码（EAGLE）：让小模型猜、大模型验，无损加速 LLM 生成",
+ *   "1. 为什么无损": the replacement token is drawn from
+ *       normalize(max(0, p~ - q)).
+ * Readings where the pages are silent: when all K drafts pass, one bonus
+ * token is drawn from p~ at position K+1, which is the target softmax of row
+ * K (no draft row exists there); one uniform per sequence serves the
+ * resample or the bonus draw; the inverse CDF takes the smallest index whose
+ * inclusive prefix sum exceeds u * (total mass); temperature 1, full
+ * vocabulary.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers to contiguous row-major memory
+ *     owned by the caller; the library never frees or retains them.  The
+ *     only memory the library allocates is a small scratch workspace
+ *     (per call, stream-ordered on `stream`, released on `stream`).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous: they return after the launch;
+ *     faults surface at the caller's next synchronisation.
+ *   - Host-side argument errors return a status and launch nothing.
+ *   - Device-side input errors (a draft token outside [0, V), or lambda
+ *     outside [0, 1] or NaN) set out_n_accepted[b] = -1 and fill
+ *     out_tokens[b][0..K] with -1.  No trap, no assert.
+ *   - NaN or +-inf logits: behaviour unspecified (no fault).
+ *   - Uniforms are taken as given; values in [0, 1) give the documented
+ *     distribution.
+ */
+#ifndef SPECV_H
+#define SPECV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPECV_F32 = 0,   /* IEEE fp32 logits */
+    SPECV_BF16 = 1   /* bfloat16 logits (widened to fp32 exactly on load) */
+} specv_dtype;
+
+typedef enum {
+    SPECV_PROB_MIX = 0,  /* p~ = (1-l) softmax(z_t) + l softmax(z_q)  (the displayed equation) */
+    SPECV_LOGIT_MIX = 1  /* p~ = softmax((1-l) z_t + l z_q)            (the pseudocode) */
+} specv_mode;
+
+typedef enum {
+    SPECV_OK = 0,
+    SPECV_ERR_INVALID_ARG = 1,  /* null pointer, size out of range, unknown enum */
+    SPECV_ERR_UNSUPPORTED = 2,  /* no usable sm_100-family device / launch shape */
+    SPECV_ERR_CUDA = 3,         /* a CUDA runtime call failed (see specv_last_cuda_error) */
+    SPECV_ERR_NO_MEMORY = 4     /* the scratch workspace could not be allocated */
+} specv_status;
+
+/*
+ * specv_verify -- one verify/accept step for B sequences of K drafted tokens.
+ *
+ *   target_logits  [B][K+1][V]  dtype  target scores of the K drafted
+ *                                      positions and of position K+1
+ *   draft_logits   [B][K][V]    dtype  draft scores of the K drafted positions
+ *   draft_tokens   [B][K]       int32  x_i, each in [0, V)
+ *   u_accept       [B][K]       fp32   r of the acceptance test, in [0, 1)
+ *   u_resample     [B]          fp32   uniform of the resample / bonus draw, in [0, 1)
+ *   lambda         [B]          fp32   mixing coefficient per sequence, in [0, 1]
+ *   B >= 1, 1 <= K <= 4096, 1 <= V < 2^31, and B*(K+1)*V < 2^62.
+ *   out_tokens     [B][K+1]     int32  x_0..x_{n-1}, then the resampled (n < K)
+ *                                      or bonus (n = K) token at index n, then -1
+ *   out_n_accepted [B]          int32  n = number of accepted drafts (0..K), -1 if invalid
+ *
+ * Each logit is read from HBM once for the statistics pass; the rejected
+ * row pair (or the bonus row) of each sequence is read a second time,
+ * usually from L2, by the sampler.
+ */
+specv_status specv_verify(const void *target_logits, const void *draft_logits,
+                          const int32_t *draft_tokens, const float *u_accept,
+                          const float *u_resample, const float *lambda, int64_t B, int32_t K,
+                          int32_t V, specv_dtype dtype, specv_mode mode, int32_t *out_tokens,
+                          int32_t *out_n_accepted, void *stream);
+
+/*
+ * specv_verify_debug -- specv_verify plus the intermediate probabilities, for
+ * tests.  Same kernels and the same arithmetic as specv_verify; the extra
+ * outputs (device pointers, each may be NULL) are:
+ *   out_ptilde_at_x [B][K]     fp32  p~(x_i) as the kernel computed it
+ *   out_q_at_x      [B][K]     fp32  q(x_i)
+ *   out_lse         [B][K+1][2] fp32 natural-log normalisers: [.][i][0] of the
+ *                                     p~ source row (target row in probability
+ *                                     mode and at i = K, mixed row in logit
+ *                                     mode), [.][i][1] of the draft row
+ *                                     (undefined at i = K)
+ * For a given input, out_tokens and out_n_accepted equal specv_verify's.
+ */
+specv_status specv_verify_debug(const void *target_logits, const void *draft_logits,
+                                const int32_t *draft_tokens, const float *u_accept,
+                                const float *u_resample, const float *lambda, int64_t B,
+                                int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,
+                                int32_t *out_tokens, int32_t *out_n_accepted,
+                                float *out_ptilde_at_x, float *out_q_at_x, float *out_lse,
+                                void *stream);
+
+/*
+ * specv_plan -- host-only query of the launch specv_verify would make for
+ * these sizes (no device work, no allocation).  Outputs may be NULL:
+ *   kernel:  0 = small-vocabulary tile kernel, 1 = cluster row kernel
+ *   cluster: CTAs per thread-block cluster splitting each row (1 for kernel 0)
+ *   ctas:    total CTAs launched
+ *   workspace_bytes: scratch bytes allocated per call
+ * Returns SPECV_ERR_INVALID_ARG for sizes specv_verify would reject.
+ */
+specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,
+                        int32_t *kernel, int32_t *cluster, int64_t *ctas,
+                        int64_t *workspace_bytes);
+
+/* Human-readable name of a status. Never NULL. */
+const char *specv_status_string(specv_status status);
+
+/* Text of the CUDA error behind the most recent SPECV_ERR_CUDA on this
+ * thread ("" if none).  Never NULL. */
+const char *specv_last_cuda_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t specv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECV_H */

@@ -1,0 +1,205 @@
+"""GB300-native speculative-decoding verify/accept with RAPID knowledge transfer.
+
+A thin ctypes binding over ``libspecv.so`` (C ABI in ``include/specv.h``).
+Every step of the verify path runs in the library's CUDA kernels; this module
+only checks tensor metadata, passes device pointers and the current CUDA
+stream, and turns status codes into exceptions.  PyTorch provides device
+memory and streams.  There is no CPU fallback: if the library is missing the
+calls raise.
+
+Sources (page title, section): "RAPID：基于检索增强的推测解码长上下文推理",
+"2) 推理时知识迁移" (p~ = (1-λ) p_t + λ p_q) and "3) 候选验证机制（伪代码）"
+(the per-step acceptance loop); "大模型推理的Speculative Decoding原理详解",
+"修改的拒绝采样"; "投机解码（EAGLE）…", "1. 为什么无损" (resample from
+max(0, p - q)).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = ["SpecvError", "PROB_MIX", "LOGIT_MIX", "F32", "BF16", "load", "lib_path", "verify",
+           "verify_debug", "plan", "status_string", "EXPORTED_SYMBOLS"]
+
+PROB_MIX = 0
+LOGIT_MIX = 1
+F32 = 0
+BF16 = 1
+
+EXPORTED_SYMBOLS = ("specv_verify", "specv_verify_debug", "specv_plan", "specv_status_string",
+                    "specv_last_cuda_error", "specv_version")
+
+_STATUS = {0: "SPECV_OK", 1: "SPECV_ERR_INVALID_ARG", 2: "SPECV_ERR_UNSUPPORTED",
+           3: "SPECV_ERR_CUDA", 4: "SPECV_ERR_NO_MEMORY"}
+
+
+class SpecvError(RuntimeError):
+    def __init__(self, status: int, what: str, detail: str = ""):
+        self.status = status
+        msg = f"{what}: {_STATUS.get(status, status)}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libspecv.so (optionally building it first).  Raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing:
+            _build.build()
+        if not os.path.exists(_build.LIB_PATH):
+            raise RuntimeError(
+                f"libspecv.so not found at {_build.LIB_PATH}; build it with "
+                "`python -m speculative_decoding_verification_specv_gb300.build`")
+        lib = ctypes.CDLL(_build.LIB_PATH)
+        vp, i32p, f32p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p
+        i64, i32 = ctypes.c_int64, ctypes.c_int32
+        common = [vp, vp, vp, vp, vp, vp, i64, i32, i32, ctypes.c_int, ctypes.c_int, vp, vp]
+        lib.specv_verify.argtypes = common + [vp]
+        lib.specv_verify.restype = ctypes.c_int
+        lib.specv_verify_debug.argtypes = common + [vp, vp, vp, vp]
+        lib.specv_verify_debug.restype = ctypes.c_int
+        lib.specv_plan.argtypes = [i64, i32, i32, ctypes.c_int, ctypes.c_int, i32p, i32p,
+                                   ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        lib.specv_plan.restype = ctypes.c_int
+        lib.specv_status_string.argtypes = [ctypes.c_int]
+        lib.specv_status_string.restype = ctypes.c_char_p
+        lib.specv_last_cuda_error.argtypes = []
+        lib.specv_last_cuda_error.restype = ctypes.c_char_p
+        lib.specv_version.argtypes = []
+        lib.specv_version.restype = ctypes.c_int32
+        _ = f32p
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().specv_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        detail = load().specv_last_cuda_error().decode() if status == 3 else ""
+        raise SpecvError(status, what, detail)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _require(t: torch.Tensor, name: str, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _args(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam, mode, out_tokens,
+          out_n_accepted):
+    zt, zq = target_logits, draft_logits
+    if zt.dim() != 3:
+        raise ValueError("target_logits must be [B][K+1][V]")
+    B, K1, V = zt.shape
+    K = K1 - 1
+    dev = zt.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors (the verify step runs only on the GPU)")
+    _require(zt, "target_logits", None, (B, K + 1, V), dev)
+    _require(zq, "draft_logits", zt.dtype, (B, K, V), dev)
+    _require(draft_tokens, "draft_tokens", torch.int32, (B, K), dev)
+    _require(u_accept, "u_accept", torch.float32, (B, K), dev)
+    _require(u_resample, "u_resample", torch.float32, (B,), dev)
+    _require(lam, "lam", torch.float32, (B,), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_n_accepted is None:
+        out_n_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _require(out_tokens, "out_tokens", torch.int32, (B, K + 1), dev)
+    _require(out_n_accepted, "out_n_accepted", torch.int32, (B,), dev)
+    if mode not in (PROB_MIX, LOGIT_MIX):
+        raise ValueError("mode must be PROB_MIX (0) or LOGIT_MIX (1)")
+    return B, K, V, dev, out_tokens, out_n_accepted
+
+
+def _stream_ptr(stream, dev):
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def verify(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam,
+           mode: int = PROB_MIX, out_tokens=None, out_n_accepted=None, stream=None):
+    """One verify/accept step on the GPU.  Returns (out_tokens [B][K+1], out_n [B]).
+
+    All tensors are CUDA, contiguous: target_logits [B][K+1][V] and
+    draft_logits [B][K][V] (float32 or bfloat16), draft_tokens int32 [B][K],
+    u_accept float32 [B][K], u_resample float32 [B], lam float32 [B].  Runs
+    asynchronously on ``stream`` (default: the current stream).
+    """
+    B, K, V, dev, out_tokens, out_n = _args(target_logits, draft_logits, draft_tokens, u_accept,
+                                            u_resample, lam, mode, out_tokens, out_n_accepted)
+    st = load().specv_verify(
+        target_logits.data_ptr(), draft_logits.data_ptr(), draft_tokens.data_ptr(),
+        u_accept.data_ptr(), u_resample.data_ptr(), lam.data_ptr(), B, K, V,
+        _dtype_code(target_logits), int(mode), out_tokens.data_ptr(), out_n.data_ptr(),
+        _stream_ptr(stream, dev))
+    _check(st, "specv_verify")
+    return out_tokens, out_n
+
+
+def verify_debug(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam,
+                 mode: int = PROB_MIX, stream=None):
+    """verify() plus p~(x_i), q(x_i) [B][K] and the row log-normalisers [B][K+1][2]."""
+    B, K, V, dev, out_tokens, out_n = _args(target_logits, draft_logits, draft_tokens, u_accept,
+                                            u_resample, lam, mode, None, None)
+    px = torch.full((B, K), float("nan"), dtype=torch.float32, device=dev)
+    qx = torch.full((B, K), float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full((B, K + 1, 2), float("nan"), dtype=torch.float32, device=dev)
+    st = load().specv_verify_debug(
+        target_logits.data_ptr(), draft_logits.data_ptr(), draft_tokens.data_ptr(),
+        u_accept.data_ptr(), u_resample.data_ptr(), lam.data_ptr(), B, K, V,
+        _dtype_code(target_logits), int(mode), out_tokens.data_ptr(), out_n.data_ptr(),
+        px.data_ptr(), qx.data_ptr(), lse.data_ptr(), _stream_ptr(stream, dev))
+    _check(st, "specv_verify_debug")
+    return dict(tokens=out_tokens, n_accepted=out_n, ptilde_x=px, q_x=qx, lse=lse)
+
+
+def plan(B: int, K: int, V: int, dtype: int = F32, mode: int = PROB_MIX) -> dict:
+    """The launch specv_verify would make (host-only query)."""
+    kern, clus = ctypes.c_int32(0), ctypes.c_int32(0)
+    ctas, ws = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = load().specv_plan(int(B), int(K), int(V), int(dtype), int(mode), ctypes.byref(kern),
+                           ctypes.byref(clus), ctypes.byref(ctas), ctypes.byref(ws))
+    _check(st, "specv_plan")
+    return dict(kernel="tile" if kern.value == 0 else "rows", cluster=clus.value,
+                ctas=ctas.value, workspace_bytes=ws.value)
+
+
+def raw_call(name: str, *args) -> int:
+    """Call an entry point of the C ABI with raw arguments (tests of the boundary)."""
+    return int(getattr(load(), name)(*args))

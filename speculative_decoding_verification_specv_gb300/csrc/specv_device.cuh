@@ -1,0 +1,185 @@
+// specv_device.cuh -- device helpers shared by the verify kernels (sm_103a).
+//
+// Row statistics are kept as (m, S): m = max_v z_v and S = sum_v exp(z_v - m),
+// both fp32.  A probability is exp(z - m) / S.  Ratios of probabilities are
+// formed from differences (z_x - m), which are exact or nearly so for the
+// likely tokens, so the acceptance ratio keeps fp32 accuracy even when the
+// logits are large.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace specv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+enum : int { kProbMix = 0, kLogitMix = 1 };
+
+// 2^x and log2(x) on the special-function unit (PTX ex2/lg2, flush-to-zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// exp(z - m) computed as 2^((z - m) * log2 e); the subtraction is done first
+// (exact for z near m) and rounded operations are spelled out so that every
+// call site rounds identically.
+__device__ __forceinline__ float exp_shifted(float z, float m) {
+  return ex2(__fmul_rn(__fsub_rn(z, m), kLog2e));
+}
+
+// Logit-mode mixture (1 - l) z_t + l z_q, written as z_t + l (z_q - z_t):
+// equal in exact arithmetic, and exactly z_t whenever z_q == z_t.
+__device__ __forceinline__ float mix_logit(float zt, float zq, float lam) {
+  return __fmaf_rn(lam, __fsub_rn(zq, zt), zt);
+}
+
+// bf16 bits -> fp32 (exact).
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+// Element access for the two logit types.  A 16-byte vector holds kPerVec
+// elements; get(v, e) widens element e to fp32 (exact for both types).
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+  static constexpr int kPerVec = 4;  // elements per 16-byte vector
+  static constexpr uint32_t kNegInfBits = 0xff800000u;
+  __device__ __forceinline__ static float load(const float *p) { return __ldg(p); }
+  __device__ __forceinline__ static uint32_t load_bits(const float *p) {
+    return __float_as_uint(__ldg(p));
+  }
+  __device__ __forceinline__ static float get(const uint4 &v, int e) {
+    const uint32_t w = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+    return __uint_as_float(w);
+  }
+  // element e of a vector assembled from scalar loads
+  __device__ __forceinline__ static void put_bits(uint4 &v, int e, uint32_t bits) {
+    if (e == 0) v.x = bits;
+    else if (e == 1) v.y = bits;
+    else if (e == 2) v.z = bits;
+    else v.w = bits;
+  }
+};
+template <>
+struct Elem<uint16_t> {  // bfloat16 storage
+  static constexpr int kPerVec = 8;
+  static constexpr uint32_t kNegInfBits = 0xff80u;
+  __device__ __forceinline__ static float load(const uint16_t *p) {
+    return bf16_bits_to_float(__ldg(p));
+  }
+  __device__ __forceinline__ static uint32_t load_bits(const uint16_t *p) { return __ldg(p); }
+  __device__ __forceinline__ static float get(const uint4 &v, int e) {
+    const uint32_t w = (e >> 1) == 0 ? v.x : (e >> 1) == 1 ? v.y : (e >> 1) == 2 ? v.z : v.w;
+    return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+  __device__ __forceinline__ static void put_bits(uint4 &v, int e, uint32_t bits) {
+    uint32_t &w = (e >> 1) == 0 ? v.x : (e >> 1) == 1 ? v.y : (e >> 1) == 2 ? v.z : v.w;
+    w = (e & 1) ? ((w & 0x0000ffffu) | (bits << 16)) : ((w & 0xffff0000u) | bits);
+  }
+};
+
+// 16-byte streaming load: read-only path, no L1 allocation (each byte is
+// used once by this CTA); L2 keeps its normal policy so that the sampler's
+// re-read of the rejected row can hit in L2.
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Merge two (m, S) partial statistics.  Empty partials are (-inf, 0).
+__device__ __forceinline__ void merge_stats(float &m, float &s, float m2, float s2) {
+  float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;  // both empty
+  float a = (m == mn) ? s : __fmul_rn(s, exp_shifted(m, mn));
+  float b = (m2 == mn) ? s2 : __fmul_rn(s2, exp_shifted(m2, mn));
+  m = mn;
+  s = __fadd_rn(a, b);
+}
+
+// Butterfly merge across a warp; every lane ends with the same result and the
+// combination order is fixed.
+__device__ __forceinline__ void warp_merge_stats(float &m, float &s) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+    merge_stats(m, s, m2, s2);
+  }
+}
+
+// Statistics of one position: A = source row of p~ (target row in
+// probability mode and at the bonus position, mixed row in logit mode),
+// B = draft row.
+struct PosStats {
+  float mA, sA, mB, sB;
+};
+
+// Acceptance ratio p~(x)/q(x) of one drafted position, and optionally p~(x)
+// and q(x) themselves.
+//   prob:  r = p_t(x)/q(x) = e^{(zt_x - mA) - (zq_x - mB)} * sB / sA and
+//          p~/q = 1 + (1 - l)(r - 1), which is exactly 1 when r == 1 or l == 1.
+//   logit: p~/q = e^{(w_x - mA) - (zq_x - mB)} * sB / sA, w_x = mix_logit(.).
+__device__ __forceinline__ float accept_ratio(int mode, const PosStats &st, float zt_x, float zq_x,
+                                              float lam, float *ptilde_x, float *q_x) {
+  float a_x = (mode == kProbMix) ? zt_x : mix_logit(zt_x, zq_x, lam);
+  float da = __fsub_rn(a_x, st.mA);
+  float db = __fsub_rn(zq_x, st.mB);
+  float d = __fsub_rn(da, db);
+  float e = (d == 0.0f) ? 1.0f : ex2(__fmul_rn(d, kLog2e));
+  float r = __fmul_rn(e, __fdiv_rn(st.sB, st.sA));
+  if (ptilde_x != nullptr) {
+    float q = __fdiv_rn(ex2(__fmul_rn(db, kLog2e)), st.sB);
+    float pa = __fdiv_rn(ex2(__fmul_rn(da, kLog2e)), st.sA);
+    *q_x = q;
+    *ptilde_x = (mode == kProbMix) ? __fmaf_rn(lam, q, __fmul_rn(__fsub_rn(1.0f, lam), pa)) : pa;
+  }
+  if (mode == kProbMix) r = __fmaf_rn(__fsub_rn(1.0f, lam), __fsub_rn(r, 1.0f), 1.0f);
+  return r;
+}
+
+// The acceptance test r < min(1, ratio) (strict, as printed in the pages' loop).
+__device__ __forceinline__ bool accept_test(float u, float ratio) {
+  return u < fminf(1.0f, ratio);
+}
+
+__device__ __forceinline__ bool lambda_valid(float lam) { return lam >= 0.0f && lam <= 1.0f; }
+
+// Weight of vocabulary entry v in the sampler.  What selects the weight:
+//   kWResidual : max(0, p~_v - q_v) up to the constant factor (1 - l) in
+//                probability mode (p~ - q = (1 - l)(p_t - q) there), exactly
+//                in logit mode;
+//   kWBonus    : p~_v at the bonus position = target softmax of row K;
+//   kWMixture  : p~_v itself (fallback when the residual has zero mass).
+enum : int { kWResidual = 0, kWBonus = 1, kWMixture = 2 };
+
+struct SampleParams {
+  float mA, invSA, mB, invSB, lam;
+};
+
+__device__ __forceinline__ float sample_weight(int mode, int kind, const SampleParams &p, float zt,
+                                               float zq) {
+  if (kind == kWBonus) return __fmul_rn(exp_shifted(zt, p.mA), p.invSA);
+  float a = (mode == kProbMix) ? zt : mix_logit(zt, zq, p.lam);
+  float pa = __fmul_rn(exp_shifted(a, p.mA), p.invSA);
+  float pq = __fmul_rn(exp_shifted(zq, p.mB), p.invSB);
+  if (kind == kWResidual) return fmaxf(0.0f, __fsub_rn(pa, pq));
+  // kWMixture
+  if (mode == kProbMix) return __fmaf_rn(p.lam, pq, __fmul_rn(__fsub_rn(1.0f, p.lam), pa));
+  return pa;
+}
+
+}  // namespace specv

@@ -1,0 +1,67 @@
+// specv_internal.h -- launch interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace specv {
+
+constexpr int kRowThreads = 256;   // threads per CTA of the cluster row kernel
+constexpr int kMaxCluster = 16;    // largest cluster (non-portable size, opt-in)
+constexpr int kTileThreads = 256;  // threads per CTA of the small-vocabulary kernel
+
+// Arguments of the cluster row kernel (one cluster per (sequence, position)).
+struct RowArgs {
+  const void *target;        // [B][K+1][V]
+  const void *draft;         // [B][K][V]
+  const int32_t *tokens;     // [B][K]
+  const float *u_accept;     // [B][K]
+  const float *u_resample;   // [B]
+  const float *lam;          // [B]
+  int64_t B;
+  int K;
+  int V;
+  int32_t *out_tokens;       // [B][K+1]
+  int32_t *out_n;            // [B]
+  float4 *ws_stats;          // scratch [B][K+1]: (mA, sA, mB, sB) per position
+  unsigned *ws_count;        // scratch [B]: positions published so far (zeroed per call)
+  float *dbg_ptilde;         // optional [B][K]
+  float *dbg_q;              // optional [B][K]
+  float *dbg_lse;            // optional [B][K+1][2]
+  int groups_per_slice;      // 16-byte groups of a row handled by one CTA
+  int num_groups;            // ceil(V / elements per 16 bytes)
+};
+
+// Arguments of the small-vocabulary tile kernel (a CTA holds whole sequences).
+struct TileArgs {
+  const void *target;
+  const void *draft;
+  const int32_t *tokens;
+  const float *u_accept;
+  const float *u_resample;
+  const float *lam;
+  int64_t B;
+  int K;
+  int V;
+  int32_t *out_tokens;
+  int32_t *out_n;
+  float *dbg_ptilde;
+  float *dbg_q;
+  float *dbg_lse;
+  int tile_seqs;             // sequences per tile
+  int64_t num_tiles;
+  int vec_copy;              // 1: tiles start on 16-byte boundaries and span whole vectors
+  int smem_target_bytes;     // bytes of the staged target block (16-byte padded)
+  int smem_draft_bytes;      // bytes of the staged draft block (16-byte padded)
+};
+
+cudaError_t rows_prepare();
+cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
+                        int64_t grid, cudaStream_t stream);
+
+cudaError_t tile_prepare(int max_smem_bytes);
+int tile_blocks_per_sm(int dtype_bf16, int mode, int smem_bytes);
+cudaError_t tile_launch(const TileArgs &a, int dtype_bf16, int mode, int64_t grid, int smem_bytes,
+                        cudaStream_t stream);
+
+}  // namespace specv

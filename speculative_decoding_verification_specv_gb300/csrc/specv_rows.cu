@@ -1,0 +1,522 @@
+// specv_rows.cu -- the cluster row kernel: the verify/accept step for
+// vocabularies too long for one CTA to hold a sequence.
+//
+// Work decomposition.  A "position" is (b, i), i in [0, K]: for i < K the pair
+// (target row i, draft row i), for i = K the target row K alone (the bonus
+// row).  Each position is one thread-block cluster of S CTAs; CTA `rank`
+// streams the rank-th slice of the vocabulary of its position's row(s).
+//
+// Phase 1 (every cluster): one pass over HBM.  Each thread keeps running
+// (max, sum-exp) statistics of its 16-byte groups (online softmax with a
+// per-batch max, so each element costs one exp); warp butterflies and a
+// fixed-order cross-warp merge give the CTA's partials; rank 0 merges the S
+// partials over DSMEM in rank order and publishes the position's statistics
+// to the scratch workspace.  The target and the draft row of a pair go
+// through the same instruction sequence, so identical rows give bitwise
+// identical statistics (and an acceptance ratio of exactly 1).
+//
+// Phase 2 (the last cluster of sequence b to publish, found with one atomic
+// counter per sequence): rank 0's first warp evaluates the acceptance test
+// of every drafted position (the pages' loop: accept x_i iff
+// u_i < min(1, p~(x_i)/q(x_i))), takes the first rejection n, and writes the
+// accepted prefix.  The whole cluster then draws the token at index n by
+// inverse CDF: over normalize(max(0, p~ - q)) of row n if n < K, over the
+// target softmax of row K if every draft passed.  Each CTA sums the weights
+// of its slice with a streaming reduction, the S slice masses are exchanged
+// over DSMEM, and the CTA whose slice holds u * (total mass) finds the token
+// with block scans over tiles of its slice in index order.  (If round-off
+// makes that scan end below the routed target, the slice's last entry of
+// positive weight is taken.)
+//
+// No thread ever waits on another cluster: the counter only decides which
+// cluster does phase 2, and the only barriers are hardware cluster barriers.
+#include <cooperative_groups.h>
+
+#include "specv_device.cuh"
+#include "specv_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace specv {
+
+namespace {
+
+constexpr int kNT = kRowThreads;  // threads per CTA
+constexpr int kNW = kNT / 32;
+constexpr int kUnroll = 4;        // 16-byte groups per thread per batch
+
+struct Broadcast {
+  int n;        // first rejected position (K if none), -1 if the sequence is invalid
+  int kind;     // sampler weight kind (kWResidual / kWBonus / kWMixture)
+  SampleParams sp;
+  float u;      // u_resample[b]
+};
+
+struct __align__(16) RowsShared {
+  float red[kNW][4];
+  float part[4];
+  int last;
+  Broadcast bc;
+  float masses[2][kMaxCluster];
+  float incl[kNT];
+  int found;
+  int lastpos[kNW];
+};
+
+// Load group g (VW consecutive elements) of a row as one 16-byte vector.  In
+// the aligned case every row starts on a 16-byte boundary and V is a multiple
+// of VW, so a group is one 16-byte load (streaming: no L1 allocation; cached:
+// through L1, for the search pass whose threads read consecutive groups).
+// Otherwise the vector is assembled from scalar loads and entries past V read
+// as -inf (they add nothing to a max or a sum).  Elements are widened to fp32
+// where they are used (Elem<T>::get), which keeps bf16 groups at 4 registers.
+template <typename T, bool ALIGNED, bool CACHED = false>
+__device__ __forceinline__ uint4 load_group(const T *row, int64_t g, int V) {
+  constexpr int VW = Elem<T>::kPerVec;
+  if constexpr (ALIGNED) {
+    if constexpr (CACHED)
+      return __ldg(reinterpret_cast<const uint4 *>(row + g * VW));
+    else
+      return ld_stream16(row + g * VW);
+  } else {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      const int64_t idx = g * VW + e;
+      Elem<T>::put_bits(v, e, idx < V ? Elem<T>::load_bits(row + idx) : Elem<T>::kNegInfBits);
+    }
+    return v;
+  }
+}
+
+// Sum of one float per thread in a fixed order (warp butterflies, then the
+// warps in index order); every thread returns the same total.
+__device__ __forceinline__ float block_sum(RowsShared &sh, float x) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, off));
+  if (lane == 0) sh.red[warp][0] = x;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kNW; ++w) t = __fadd_rn(t, sh.red[w][0]);
+  __syncthreads();
+  return t;
+}
+
+// Inclusive block scan of one float per thread; returns the exclusive value
+// (exactly the previous thread's inclusive value) and the block total.
+__device__ __forceinline__ void block_scan(RowsShared &sh, float x, float &excl, float &incl,
+                                           float &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float v = x;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    float y = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v = __fadd_rn(v, y);
+  }
+  if (lane == 31) sh.red[warp][0] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float ws = lane < kNW ? sh.red[lane][0] : 0.0f;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      float y = __shfl_up_sync(0xffffffffu, ws, off);
+      if (lane >= off) ws = __fadd_rn(ws, y);
+    }
+    if (lane < kNW) sh.red[lane][2] = ws;  // inclusive warp offsets
+  }
+  __syncthreads();
+  float woff = warp == 0 ? 0.0f : sh.red[warp - 1][2];
+  incl = warp == 0 ? v : __fadd_rn(woff, v);
+  sh.incl[threadIdx.x] = incl;
+  __syncthreads();
+  excl = threadIdx.x == 0 ? 0.0f : sh.incl[threadIdx.x - 1];
+  total = sh.incl[kNT - 1];
+}
+
+// Mass of the sampler weights over this CTA's slice: a streaming reduction
+// with the same coalesced access pattern as phase 1.
+template <typename T, int MODE, bool ALIGNED>
+__device__ float slice_mass(RowsShared &sh, const T *rowA, const T *rowB, int V, int g_lo,
+                            int g_hi, int kind, const SampleParams &sp) {
+  constexpr int VW = Elem<T>::kPerVec;
+  float acc = 0.0f;
+  for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += kNT * kUnroll) {
+    uint4 za[kUnroll], zb[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int g = g0 + u * kNT;
+      if (g < g_hi) {
+        za[u] = load_group<T, ALIGNED>(rowA, g, V);
+        if (kind != kWBonus) zb[u] = load_group<T, ALIGNED>(rowB, g, V);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int g = g0 + u * kNT;
+      if (g < g_hi) {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          if (ALIGNED || (int64_t)g * VW + e < V)
+            acc = __fadd_rn(acc, sample_weight(MODE, kind, sp, Elem<T>::get(za[u], e),
+                                               kind != kWBonus ? Elem<T>::get(zb[u], e) : 0.0f));
+        }
+      }
+    }
+  }
+  return block_sum(sh, acc);
+}
+
+// Search of this CTA's slice in index order for the first entry whose running
+// weight sum exceeds t.  Tiles of kNT*kSearchU groups; thread j of a tile owns
+// kSearchU consecutive groups (16 entries), a block scan routes t to one thread, and that
+// thread walks its entries.  If round-off leaves no crossing, the largest
+// index with positive weight is returned (-1 if the slice has none).
+template <typename T, int MODE, bool ALIGNED>
+__device__ int slice_search(RowsShared &sh, const T *rowA, const T *rowB, int V, int g_lo, int g_hi,
+                            int kind, const SampleParams &sp, float t) {
+  constexpr int VW = Elem<T>::kPerVec;
+  constexpr int kSearchU = 16 / VW;  // 16 entries per thread per tile
+  float base = 0.0f;
+  int lastpos = -1;
+  if (threadIdx.x == 0) sh.found = -1;
+  for (int tb = g_lo; tb < g_hi; tb += kNT * kSearchU) {
+    const int gs = tb + (int)threadIdx.x * kSearchU;
+    float w[kSearchU][VW];
+    float s = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kSearchU; ++u) {
+      const int g = gs + u;
+      if (g < g_hi) {
+        const uint4 za = load_group<T, ALIGNED, true>(rowA, g, V);
+        const uint4 zb = kind != kWBonus ? load_group<T, ALIGNED, true>(rowB, g, V) : za;
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          const int idx = g * VW + e;
+          w[u][e] = (ALIGNED || idx < V)
+                        ? sample_weight(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e))
+                        : 0.0f;
+          s = __fadd_rn(s, w[u][e]);
+          if (w[u][e] > 0.0f) lastpos = idx;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) w[u][e] = 0.0f;
+      }
+    }
+    float excl, incl, total;
+    block_scan(sh, s, excl, incl, total);
+    const float lo = __fadd_rn(base, excl), hi = __fadd_rn(base, incl);
+    if (lo <= t && t < hi) {  // only one thread: the intervals partition [base, base+total)
+      float c = lo;
+      int pick = -1, lastg = -1;
+#pragma unroll
+      for (int u = 0; u < kSearchU; ++u)
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          c = __fadd_rn(c, w[u][e]);
+          if (w[u][e] > 0.0f) lastg = (gs + u) * VW + e;
+          if (pick < 0 && c > t) pick = (gs + u) * VW + e;
+        }
+      sh.found = pick >= 0 ? pick : lastg;
+    }
+    __syncthreads();
+    const int f = sh.found;
+    __syncthreads();
+    if (f >= 0) return f;
+    base = __fadd_rn(base, total);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, off));
+  if (lane == 0) sh.lastpos[warp] = lastpos;
+  __syncthreads();
+  int r = -1;
+  for (int k = 0; k < kNW; ++k) r = max(r, sh.lastpos[k]);
+  __syncthreads();
+  return r;
+}
+
+template <typename T, int MODE, bool ALIGNED>
+__global__ void __launch_bounds__(kNT) rows_kernel(RowArgs a) {
+  constexpr int VW = Elem<T>::kPerVec;
+  __shared__ RowsShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int S = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int64_t p = (int64_t)blockIdx.x / S;  // position index b*(K+1) + i
+  const int K = a.K, V = a.V;
+  const int64_t b = p / (K + 1);
+  const int i = (int)(p - b * (K + 1));
+  const bool pair = i < K;
+  const T *tgt = static_cast<const T *>(a.target);
+  const T *dft = static_cast<const T *>(a.draft);
+  const T *rowA = tgt + (b * (K + 1) + i) * (int64_t)V;
+  const T *rowB = dft + (b * K + (pair ? i : 0)) * (int64_t)V;
+  const int g_lo = rank * a.groups_per_slice;
+  const int g_hi = min(a.num_groups, g_lo + a.groups_per_slice);
+  const float lam_seq = a.lam[b];
+
+  // ---------------------------------------------------------------- phase 1
+  float mA = -INFINITY, sA = 0.0f, mB = -INFINITY, sB = 0.0f;
+  for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += kNT * kUnroll) {
+    uint4 za[kUnroll], zb[kUnroll];
+    bool ok[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int g = g0 + u * kNT;
+      ok[u] = g < g_hi;
+      if (ok[u]) {
+        za[u] = load_group<T, ALIGNED>(rowA, g, V);
+        if (pair) zb[u] = load_group<T, ALIGNED>(rowB, g, V);
+      }
+    }
+    // A-row value of element e of group u: the target logit, or in logit mode
+    // the mixed logit (entries past V stay -inf).
+    auto a_val = [&](int u, int e) -> float {
+      const float zt = Elem<T>::get(za[u], e);
+      if (MODE == kLogitMix && pair) {
+        const float zq = Elem<T>::get(zb[u], e);
+        return zq == -INFINITY ? -INFINITY : mix_logit(zt, zq, lam_seq);
+      }
+      return zt;
+    };
+    float bmA = -INFINITY, bmB = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (ok[u]) {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          bmA = fmaxf(bmA, a_val(u, e));
+          if (pair) bmB = fmaxf(bmB, Elem<T>::get(zb[u], e));
+        }
+      }
+    if (bmA > mA) {
+      sA = __fmul_rn(sA, exp_shifted(mA, bmA));
+      mA = bmA;
+    }
+    if (pair && bmB > mB) {
+      sB = __fmul_rn(sB, exp_shifted(mB, bmB));
+      mB = bmB;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (ok[u]) {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          sA = __fadd_rn(sA, exp_shifted(a_val(u, e), mA));
+          if (pair) sB = __fadd_rn(sB, exp_shifted(Elem<T>::get(zb[u], e), mB));
+        }
+      }
+  }
+  warp_merge_stats(mA, sA);
+  warp_merge_stats(mB, sB);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    sh.red[warp][0] = mA;
+    sh.red[warp][1] = sA;
+    sh.red[warp][2] = mB;
+    sh.red[warp][3] = sB;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
+    for (int w = 0; w < kNW; ++w) {
+      merge_stats(m0, s0, sh.red[w][0], sh.red[w][1]);
+      merge_stats(m1, s1, sh.red[w][2], sh.red[w][3]);
+    }
+    sh.part[0] = m0;
+    sh.part[1] = s0;
+    sh.part[2] = m1;
+    sh.part[3] = s1;
+  }
+  cluster.sync();  // partials of every rank are visible
+  if (rank == 0 && threadIdx.x == 0) {
+    float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
+    for (int r = 0; r < S; ++r) {
+      const float *pr = cluster.map_shared_rank(sh.part, r);
+      merge_stats(m0, s0, pr[0], pr[1]);
+      merge_stats(m1, s1, pr[2], pr[3]);
+    }
+    a.ws_stats[p] = make_float4(m0, s0, m1, s1);
+    __threadfence();
+    const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
+    const int last = prev == (unsigned)K;
+    if (last) __threadfence();
+    for (int r = 0; r < S; ++r) *cluster.map_shared_rank(&sh.last, r) = last;
+  }
+  cluster.sync();  // sh.last is set in every rank; rank 0 is done reading partials
+  if (!sh.last) return;
+
+  // ---------------------------------------------------------------- phase 2
+  if (rank == 0 && warp == 0) {
+    __threadfence();
+    const bool lam_ok = lambda_valid(lam_seq);
+    bool lane_ok = true;
+    int n = K;
+    for (int i0 = 0; i0 < K; i0 += 32) {
+      const int j = i0 + lane;
+      bool rejected = false;
+      if (j < K) {
+        const int x = a.tokens[b * K + j];
+        const bool tok_ok = x >= 0 && x < V;
+        lane_ok = lane_ok && tok_ok;
+        if (tok_ok && lam_ok) {
+          const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + j]);
+          const PosStats st{st4.x, st4.y, st4.z, st4.w};
+          const float zt_x = Elem<T>::load(tgt + (b * (K + 1) + j) * (int64_t)V + x);
+          const float zq_x = Elem<T>::load(dft + (b * K + j) * (int64_t)V + x);
+          float px = 0.0f, qx = 0.0f;
+          const float ratio =
+              accept_ratio(MODE, st, zt_x, zq_x, lam_seq, a.dbg_ptilde ? &px : nullptr, &qx);
+          rejected = !accept_test(a.u_accept[b * K + j], ratio);
+          if (a.dbg_ptilde) a.dbg_ptilde[b * K + j] = px;
+          if (a.dbg_q) a.dbg_q[b * K + j] = qx;
+        }
+      }
+      const unsigned rej = __ballot_sync(0xffffffffu, rejected);
+      if (rej != 0u && n == K) n = i0 + __ffs(rej) - 1;
+    }
+    const bool valid = lam_ok && __all_sync(0xffffffffu, lane_ok);
+    if (a.dbg_lse) {
+      for (int j = lane; j <= K; j += 32) {
+        const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + j]);
+        a.dbg_lse[(b * (K + 1) + j) * 2 + 0] = st4.x + lg2(st4.y) * kLn2;
+        a.dbg_lse[(b * (K + 1) + j) * 2 + 1] = j < K ? st4.z + lg2(st4.w) * kLn2 : 0.0f;
+      }
+    }
+    for (int j = lane; j <= K; j += 32) {
+      int out = -1;
+      if (valid && j < n) out = a.tokens[b * K + j];
+      if (!valid || j != n) a.out_tokens[b * (K + 1) + j] = out;
+    }
+    if (lane == 0) {
+      a.out_n[b] = valid ? n : -1;
+      Broadcast bc;
+      bc.n = valid ? n : -1;
+      bc.u = a.u_resample[b];
+      const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + (valid ? n : 0)]);
+      bc.sp.mA = st4.x;
+      bc.sp.invSA = __fdiv_rn(1.0f, st4.y);
+      bc.sp.mB = st4.z;
+      bc.sp.invSB = __fdiv_rn(1.0f, st4.w);
+      bc.sp.lam = lam_seq;
+      if (n == K)
+        bc.kind = kWBonus;
+      else if (MODE == kProbMix && !(lam_seq < 1.0f))
+        bc.kind = kWMixture;  // p~ = q: the residual is identically zero
+      else
+        bc.kind = kWResidual;
+      for (int r = 0; r < S; ++r) *cluster.map_shared_rank(&sh.bc, r) = bc;
+    }
+  }
+  cluster.sync();  // broadcast visible everywhere
+  const Broadcast bc = sh.bc;
+  if (bc.n < 0) return;
+  const T *sA_row = tgt + (b * (K + 1) + bc.n) * (int64_t)V;
+  const T *sB_row = dft + (b * K + (bc.n < K ? bc.n : 0)) * (int64_t)V;
+  int kind = bc.kind;
+  float R = 0.0f;
+  int attempt = 0;
+  for (;; ++attempt) {
+    const float mass = slice_mass<T, MODE, ALIGNED>(sh, sA_row, sB_row, V, g_lo, g_hi, kind, bc.sp);
+    if (threadIdx.x == 0)
+      for (int r = 0; r < S; ++r) cluster.map_shared_rank(sh.masses[attempt], r)[rank] = mass;
+    cluster.sync();  // all slice masses exchanged
+    R = 0.0f;
+    for (int r = 0; r < S; ++r) R = __fadd_rn(R, sh.masses[attempt][r]);
+    if (R > 0.0f || kind != kWResidual || attempt == 1) break;
+    kind = kWMixture;  // zero residual mass (round-off only): draw from p~ instead
+  }
+  if (!(R > 0.0f)) {
+    if (rank == 0 && threadIdx.x == 0) a.out_tokens[b * (K + 1) + bc.n] = -1;
+    return;
+  }
+  const float t = __fmul_rn(bc.u, R);
+  int rstar = -1;
+  float tloc = INFINITY;
+  float c = 0.0f;
+  for (int r = 0; r < S; ++r) {
+    const float cn = __fadd_rn(c, sh.masses[attempt][r]);
+    if (cn > t) {
+      rstar = r;
+      tloc = __fsub_rn(t, c);
+      break;
+    }
+    c = cn;
+  }
+  if (rstar < 0) {  // u*R not below the total (u >= 1 or round-off): last slice with mass
+    for (int r = S - 1; r >= 0; --r)
+      if (sh.masses[attempt][r] > 0.0f) {
+        rstar = r;
+        break;
+      }
+    tloc = INFINITY;
+  }
+  if (rank != rstar) return;
+  const int tok =
+      slice_search<T, MODE, ALIGNED>(sh, sA_row, sB_row, V, g_lo, g_hi, kind, bc.sp, tloc);
+  if (threadIdx.x == 0) a.out_tokens[b * (K + 1) + bc.n] = tok;
+}
+
+template <typename T, int MODE, bool ALIGNED>
+cudaError_t launch_one(const RowArgs &a, int S, int64_t grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kNT, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rows_kernel<T, MODE, ALIGNED>, a);
+}
+
+template <typename T, int MODE, bool ALIGNED>
+cudaError_t prepare_one() {
+  return cudaFuncSetAttribute(rows_kernel<T, MODE, ALIGNED>,
+                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+}  // namespace
+
+cudaError_t rows_prepare() {
+  cudaError_t e = cudaSuccess;
+  cudaError_t r;
+#define SPECV_PREP(T, M, A) \
+  if ((r = prepare_one<T, M, A>()) != cudaSuccess) e = r;
+  SPECV_PREP(float, kProbMix, true)
+  SPECV_PREP(float, kProbMix, false)
+  SPECV_PREP(float, kLogitMix, true)
+  SPECV_PREP(float, kLogitMix, false)
+  SPECV_PREP(uint16_t, kProbMix, true)
+  SPECV_PREP(uint16_t, kProbMix, false)
+  SPECV_PREP(uint16_t, kLogitMix, true)
+  SPECV_PREP(uint16_t, kLogitMix, false)
+#undef SPECV_PREP
+  return e;
+}
+
+cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
+                        int64_t grid, cudaStream_t stream) {
+  if (dtype_bf16) {
+    if (mode == kProbMix)
+      return aligned ? launch_one<uint16_t, kProbMix, true>(a, S, grid, stream)
+                     : launch_one<uint16_t, kProbMix, false>(a, S, grid, stream);
+    return aligned ? launch_one<uint16_t, kLogitMix, true>(a, S, grid, stream)
+                   : launch_one<uint16_t, kLogitMix, false>(a, S, grid, stream);
+  }
+  if (mode == kProbMix)
+    return aligned ? launch_one<float, kProbMix, true>(a, S, grid, stream)
+                   : launch_one<float, kProbMix, false>(a, S, grid, stream);
+  return aligned ? launch_one<float, kLogitMix, true>(a, S, grid, stream)
+                 : launch_one<float, kLogitMix, false>(a, S, grid, stream);
+}
+
+}  // namespace specv

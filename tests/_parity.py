@@ -1,0 +1,104 @@
+"""Comparison of the CUDA verify step with the fp64 oracle (test helper).
+
+Decisions are compared exactly except where a uniform lies within BAND of a
+decision boundary: |u_i - min(1, ratio_i)| for a decided position, or the
+distance of u_resample to the nearest boundary of the CDF it was drawn
+through.  Those sequences are counted, and their GPU output must still be a
+valid outcome: an accepted prefix of the draft, then one token that has
+positive probability under the distribution of that step, then -1.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+BAND = 1e-5          # decision-boundary band
+TOL_F32 = 1e-5       # |p_gpu - p_oracle| for fp32 logits
+TOL_BF16 = 2e-3      # |p_gpu - p_oracle| for bf16 logits
+
+
+def to_host(x):
+    return {k: (v.detach().cpu() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+
+
+def run_oracle(xh, mode, seqs=None):
+    """Oracle on all sequences, or on the listed ones (a gathered sub-batch)."""
+    if seqs is not None:
+        idx = torch.as_tensor(seqs, dtype=torch.long)
+        xh = {k: v.index_select(0, idx) for k, v in xh.items()}
+    return oracle.verify(xh["target_logits"], xh["draft_logits"], xh["draft_tokens"],
+                         xh["u_accept"], xh["u_resample"], xh["lam"], mode=mode)
+
+
+def _valid_outcome(xh_b, mode, n, toks):
+    """Is (n, toks) a possible output for this sequence (any uniforms)?"""
+    K = xh_b["draft_tokens"].shape[0]
+    if not (0 <= n <= K):
+        return False
+    drafts = xh_b["draft_tokens"].numpy()
+    if list(toks[:n]) != list(drafts[:n]) or any(t != -1 for t in toks[n + 1:]):
+        return False
+    t = int(toks[n])
+    V = xh_b["target_logits"].shape[-1]
+    if not (0 <= t < V):
+        return False
+    lam = float(xh_b["lam"])
+    pt, q = oracle.rows(xh_b["target_logits"], xh_b["draft_logits"], lam, mode)
+    if n == K:
+        return pt[K, t] > 0
+    resid = np.maximum(0.0, pt[n] - q[n])
+    return resid[t] > 0 or (resid.sum() < 1e-12 and pt[n, t] > 0)
+
+
+def compare(xh, mode, gpu_tokens, gpu_n, orc, seqs=None, band=BAND):
+    """Returns a report dict; raises AssertionError on any mismatch outside the band."""
+    gt = np.asarray(gpu_tokens)
+    gn = np.asarray(gpu_n)
+    seqs = list(range(gn.shape[0])) if seqs is None else list(seqs)
+    near = exact = near_same = 0
+    mism = []
+    near_tight = 0
+    for j, b in enumerate(seqs):
+        on, ot = int(orc.n_accepted[j]), orc.tokens[j]
+        if on == -1:
+            if not (gn[b] == -1 and (gt[b] == -1).all()):
+                mism.append((b, "invalid", on, gn[b]))
+            continue
+        am, cm = float(orc.accept_margin[j]), float(orc.cdf_margin[j])
+        if am < band or cm < band:
+            near += 1
+            if am < 1e-7 or cm < 1e-7:
+                near_tight += 1
+            if gn[b] == on and (gt[b] == ot).all():
+                near_same += 1
+                continue
+            xb = {k: v[b] for k, v in xh.items()}
+            if not _valid_outcome(xb, mode, int(gn[b]), gt[b]):
+                mism.append((b, "invalid-outcome-near-band", on, int(gn[b]), ot.tolist(),
+                             gt[b].tolist()))
+            continue
+        if gn[b] != on or not (gt[b] == ot).all():
+            mism.append((b, "mismatch", on, int(gn[b]), ot.tolist(), gt[b].tolist(), am, cm))
+        else:
+            exact += 1
+    rep = dict(sequences=len(seqs), exact=exact, near_band=near, near_band_same=near_same,
+               near_band_1e7=near_tight, mismatches=len(mism))
+    assert not mism, f"{len(mism)} mismatches outside the {band} band: {mism[:5]} report={rep}"
+    return rep
+
+
+def check_probabilities(xh, mode, dbg, orc, seqs=None):
+    """p~(x_i), q(x_i) against the oracle within the dtype's tolerance."""
+    tol = TOL_BF16 if xh["target_logits"].dtype == torch.bfloat16 else TOL_F32
+    seqs = list(range(dbg["ptilde_x"].shape[0])) if seqs is None else list(seqs)
+    px = dbg["ptilde_x"].cpu().numpy()[seqs]
+    qx = dbg["q_x"].cpu().numpy()[seqs]
+    ok = ~np.isnan(orc.ptilde_x)
+    err_p = np.abs(px - orc.ptilde_x)[ok].max(initial=0.0)
+    err_q = np.abs(qx - orc.q_x)[ok].max(initial=0.0)
+    rel_p = (np.abs(px - orc.ptilde_x) / np.maximum(orc.ptilde_x, 1e-30))[ok].max(initial=0.0)
+    assert err_p <= tol and err_q <= tol, (err_p, err_q, tol)
+    return dict(max_abs_err_ptilde=float(err_p), max_abs_err_q=float(err_q),
+                max_rel_err_ptilde=float(rel_p))

@@ -1,0 +1,85 @@
+"""The C-ABI boundary without a GPU: the library loads, exports every entry
+point that include/*.h declares, and rejects bad arguments on the host
+(status codes, nothing launched).  No compute call is made here."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_specv_gb300 as specv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return specv.load(build_if_missing=True)
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(specv_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_symbols()
+    assert "specv_verify" in declared and len(declared) >= 6
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert set(specv.EXPORTED_SYMBOLS) <= set(declared)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.specv_version() >= 100
+    for code, name in [(0, "SPECV_OK"), (1, "SPECV_ERR_INVALID_ARG"), (2, "SPECV_ERR_UNSUPPORTED"),
+                       (3, "SPECV_ERR_CUDA"), (4, "SPECV_ERR_NO_MEMORY")]:
+        assert specv.status_string(code) == name
+    assert specv.status_string(99) == "SPECV_ERR_UNKNOWN"
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _call(B=2, K=3, V=100, dtype=0, mode=0, null=None):
+    ptrs = [FAKE] * 8
+    if null is not None:
+        ptrs[null] = None
+    t, d, tok, ua, ur, lam, ot, on = ptrs
+    return specv.raw_call("specv_verify", t, d, tok, ua, ur, lam, B, K, V, dtype, mode, ot, on,
+                          None)
+
+
+@pytest.mark.parametrize("null", range(8))
+def test_null_pointers_are_rejected(lib, null):
+    assert _call(null=null) == 1
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(B=-5), dict(K=0), dict(K=-1), dict(K=4097),
+                                dict(V=0), dict(V=-7), dict(dtype=2), dict(dtype=-1),
+                                dict(mode=2), dict(B=1 << 40, K=4000, V=1 << 30)])
+def test_bad_sizes_and_enums_are_rejected(lib, kw):
+    assert _call(**kw) == 1
+
+
+def test_debug_entry_point_validates_too(lib):
+    st = specv.raw_call("specv_verify_debug", None, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 1, 0, 0,
+                        FAKE, FAKE, None, None, None, None)
+    assert st == 1
+
+
+def test_plan_selects_kernels(lib):
+    p5 = specv.plan(1_000_000, 4, 32, specv.F32)
+    assert p5["kernel"] == "tile" and p5["workspace_bytes"] == 0
+    p4 = specv.plan(256, 8, 128256, specv.F32)
+    assert p4["kernel"] == "rows" and p4["ctas"] == 256 * 9 * p4["cluster"]
+    assert p4["workspace_bytes"] >= 256 * 9 * 16 + 256 * 4
+    p2 = specv.plan(1, 8, 128256, specv.BF16)
+    assert p2["kernel"] == "rows" and p2["cluster"] > 1
+    with pytest.raises(specv.SpecvError):
+        specv.plan(0, 4, 32)

@@ -1,0 +1,227 @@
+"""GPU parity: the CUDA verify step (through the C ABI) against the fp64 oracle.
+
+Decisions (n_accepted and every emitted token) must be bit-exact except where
+a uniform lies within 1e-5 of a decision or CDF boundary; those sequences are
+counted and must still hold a valid outcome.  The probabilities p~(x_i) and
+q(x_i) the kernels computed must match the oracle within 1e-5 (fp32 logits)
+or 2e-3 (bf16 logits).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests import _parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def specv():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for the gpu tests")
+    import speculative_decoding_verification_specv_gb300 as m
+    m.load(build_if_missing=True)
+    return m
+
+
+@pytest.fixture
+def cluster_env():
+    old = os.environ.get("SPECV_CLUSTER_SIZE")
+    yield
+    if old is None:
+        os.environ.pop("SPECV_CLUSTER_SIZE", None)
+    else:
+        os.environ["SPECV_CLUSTER_SIZE"] = old
+
+
+def _run(specv, x, mode, debug=True):
+    args = (x["target_logits"], x["draft_logits"], x["draft_tokens"], x["u_accept"],
+            x["u_resample"], x["lam"])
+    tok, n = specv.verify(*args, mode=mode)
+    dbg = specv.verify_debug(*args, mode=mode) if debug else None
+    torch.cuda.synchronize()
+    if dbg is not None:
+        # the debug entry point runs the same kernels: same decisions
+        assert torch.equal(dbg["tokens"], tok) and torch.equal(dbg["n_accepted"], n)
+    return tok.cpu().numpy(), n.cpu().numpy(), dbg
+
+
+def _check(specv, x, mode, seqs=None, debug=True):
+    tok, n, dbg = _run(specv, x, mode, debug)
+    xh = _parity.to_host(x)
+    orc = _parity.run_oracle(xh, mode, seqs)
+    rep = _parity.compare(xh, mode, tok, n, orc, seqs)
+    if dbg is not None:
+        rep.update(_parity.check_probabilities(xh, mode, dbg, orc, seqs))
+    return rep, tok, n
+
+
+SMALL = {
+    1: workloads.WORKLOADS[1],
+    2: workloads.WORKLOADS[2],
+    3: workloads.WORKLOADS[3],
+    4: workloads.WORKLOADS[4].scaled(B=16),
+    5: workloads.WORKLOADS[5].scaled(B=50_000),
+}
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_parity_workloads(specv, cfg, mode):
+    w = SMALL[cfg]
+    x = workloads.make_inputs(w, DEV)
+    rep, tok, n = _check(specv, x, mode)
+    print(f"workload {cfg} ({w.name}, B={w.B}) mode={mode}: {rep}")
+    assert rep["exact"] + rep["near_band"] == rep["sequences"]
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+def test_parity_full_size_batched_fp32_sampled(specv, mode):
+    """B=256, K=8, V=128256 fp32 as benchmarked; the oracle checks 32 sampled
+    sequences, and every drafted-equals-target sequence must accept all K."""
+    w = workloads.WORKLOADS[4]
+    x = workloads.make_inputs(w, DEV)
+    seqs = list(range(0, 128, 8)) + list(range(128, 256, 8))
+    rep, tok, n = _check(specv, x, mode, seqs=seqs)
+    print(f"full-size batched fp32 mode={mode}: {rep}")
+    assert (n[128:] == w.K).all()
+    assert ((tok[128:, :w.K] == x["draft_tokens"][128:].cpu().numpy())).all()
+    assert ((tok[128:, w.K] >= 0) & (tok[128:, w.K] < w.V)).all()
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+def test_parity_full_size_exactness_workload(specv, mode):
+    w = workloads.WORKLOADS[5]
+    x = workloads.make_inputs(w, DEV)
+    rep, _, _ = _check(specv, x, mode, debug=False)
+    print(f"full-size exactness workload mode={mode}: {rep}")
+
+
+@pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
+def test_every_cluster_size(specv, cluster_env, S):
+    os.environ["SPECV_CLUSTER_SIZE"] = str(S)
+    for w, mode in ((workloads.WORKLOADS[3].scaled(B=4), 0),
+                    (workloads.WORKLOADS[1].scaled(B=3, K=3, V=50001), 1)):
+        assert specv.plan(w.B, w.K, w.V, 1 if w.dtype == "bf16" else 0)["cluster"] == S
+        x = workloads.make_inputs(w, DEV)
+        rep, _, _ = _check(specv, x, mode)
+        print(f"S={S} {w.name} V={w.V}: {rep}")
+
+
+RAGGED = [
+    # (B, K, V, dtype, structure)
+    (3, 1, 1001, "f32", "corr:2.0:0.8:1.0"),       # rows kernel, unaligned rows
+    (2, 33, 515, "bf16", "corr:3.0:0.9:0.7"),      # K crosses one warp of positions
+    (5, 3, 33, "f32", "corr:2.0:0.8:1.0"),         # tile kernel, V just over a warp
+    (41, 4, 32, "f32", "broadcast:1.5"),           # tile kernel, ragged last tile
+    (7, 2, 257, "bf16", "corr:3.0:0.9:0.7"),       # first V past the tile kernel
+    (9, 2, 256, "bf16", "corr:3.0:0.9:0.7"),       # last V of the tile kernel
+    (2, 64, 4099, "bf16", "rho:3.0:0.5:0.95"),     # many positions, odd V
+    (1, 1, 1, "f32", "corr:2.0:0.8:1.0"),          # V = 1: certain tokens
+    (3, 2, 2, "f32", "corr:2.0:0.8:1.0"),
+    (1, 300, 3, "f32", "corr:2.0:0.8:1.0"),        # long draft, tiny vocabulary
+    (2, 4, 131071, "f32", "corr:3.0:0.85:1.0"),    # odd large V, fp32
+]
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+@pytest.mark.parametrize("shape", RAGGED, ids=lambda s: f"B{s[0]}K{s[1]}V{s[2]}{s[3]}")
+def test_ragged_shapes(specv, shape, mode):
+    B, K, V, dt, st = shape
+    w = workloads.Workload("ragged", B, K, V, dt, st, (0.35,), 9)
+    x = workloads.make_inputs(w, DEV)
+    rep, _, _ = _check(specv, x, mode)
+    print(f"{shape} mode={mode} plan={specv.plan(B, K, V, 1 if dt == 'bf16' else 0, mode)}: {rep}")
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [24, 1000, 20000])
+def test_misaligned_base_pointers(specv, dt, V):
+    """Inputs that start one element past a 16-byte boundary."""
+    w = workloads.Workload("misaligned", 3, 3, V, dt, "corr:2.0:0.8:1.0", (0.3,), 8)
+    x = workloads.make_inputs(w, DEV)
+    for key in ("target_logits", "draft_logits"):
+        t = x[key]
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=DEV)
+        v = buf[1:].view(t.shape)
+        v.copy_(t)
+        assert v.data_ptr() % 16 != 0 and v.is_contiguous()
+        x[key] = v
+    _check(specv, x, 0)
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+@pytest.mark.parametrize("V", [32, 3001, 128256])
+def test_identical_draft_accepts_all(specv, mode, V):
+    w = workloads.WORKLOADS[4].scaled(B=6, V=V)
+    x = workloads.make_inputs(w, DEV)
+    x["draft_logits"] = x["target_logits"][:, :w.K].contiguous()
+    for lam in (0.0, 0.2, 1.0):
+        x["lam"] = torch.full((w.B,), lam, dtype=torch.float32, device=DEV)
+        tok, n, _ = _run(specv, x, mode, debug=False)
+        assert (n == w.K).all(), (lam, n)
+        assert (tok[:, :w.K] == x["draft_tokens"].cpu().numpy()).all()
+
+
+def test_lambda_one_and_zero_uniforms_accept(specv):
+    w = workloads.WORKLOADS[3].scaled(B=4, V=5003)
+    x = workloads.make_inputs(w, DEV, lam=1.0)
+    _, n, _ = _run(specv, x, 0, debug=False)
+    assert (n == w.K).all()
+    x = workloads.make_inputs(w, DEV)
+    x["u_accept"].zero_()
+    for mode in (0, 1):
+        _, n, _ = _run(specv, x, mode, debug=False)
+        assert (n == w.K).all()
+
+
+@pytest.mark.parametrize("V", [32, 4099])
+def test_invalid_inputs_give_minus_one(specv, V):
+    w = workloads.WORKLOADS[1].scaled(B=5, V=V)
+    x = workloads.make_inputs(w, DEV)
+    x["draft_tokens"][1, 2] = V          # out of range
+    x["draft_tokens"][2, 0] = -3         # negative
+    x["lam"][3] = 1.5                    # not a convex weight
+    x["lam"][4] = float("nan")
+    tok, n, _ = _run(specv, x, 0, debug=False)
+    for b in (1, 2, 3, 4):
+        assert n[b] == -1 and (tok[b] == -1).all()
+    assert n[0] >= 0
+    xh = _parity.to_host(x)
+    orc = _parity.run_oracle(xh, 0)
+    _parity.compare(xh, 0, tok, n, orc)
+
+
+def test_deterministic_and_stream_ordered(specv):
+    w = workloads.WORKLOADS[3].scaled(B=8)
+    x = workloads.make_inputs(w, DEV)
+    args = (x["target_logits"], x["draft_logits"], x["draft_tokens"], x["u_accept"],
+            x["u_resample"], x["lam"])
+    t0, n0 = specv.verify(*args)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        t1, n1 = specv.verify(*args, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(t0, t1) and torch.equal(n0, n1)
+
+
+def test_binding_rejects_bad_tensors(specv):
+    w = workloads.WORKLOADS[1]
+    x = workloads.make_inputs(w, DEV)
+    with pytest.raises(TypeError):
+        specv.verify(x["target_logits"].double(), x["draft_logits"].double(), x["draft_tokens"],
+                     x["u_accept"], x["u_resample"], x["lam"])
+    with pytest.raises(ValueError):
+        specv.verify(x["target_logits"], x["draft_logits"][:, :2].contiguous(),
+                     x["draft_tokens"], x["u_accept"], x["u_resample"], x["lam"])
+    with pytest.raises(ValueError):
+        cpu = {k: v.cpu() for k, v in x.items()}
+        specv.verify(cpu["target_logits"], cpu["draft_logits"], cpu["draft_tokens"],
+                     cpu["u_accept"], cpu["u_resample"], cpu["lam"])
