@@ -82,9 +82,12 @@ typedef enum {
  *                                      or bonus (n = K) token at index n, then -1
  *   out_n_accepted [B]          int32  n = number of accepted drafts (0..K), -1 if invalid
  *
- * Each logit is read from HBM once for the statistics pass; the rejected
- * row pair (or the bonus row) of each sequence is read a second time,
- * usually from L2, by the sampler.
+ * Each logit is read from HBM once.  With the resident row kernel the
+ * replacement or bonus token is drawn from the copy of the row held in
+ * shared memory; with the streaming row kernel (misaligned rows, or slices
+ * too large for shared memory) the rejected row pair or the bonus row is
+ * read a second time, usually from L2.  out_n_accepted[b] = -2 reports an
+ * internal copy timeout (a bounded wait that expired; not expected).
  */
 specv_status specv_verify(const void *target_logits, const void *draft_logits,
                           const int32_t *draft_tokens, const float *u_accept,
@@ -116,9 +119,14 @@ specv_status specv_verify_debug(const void *target_logits, const void *draft_log
 /*
  * specv_plan -- host-only query of the launch specv_verify would make for
  * these sizes (no device work, no allocation).  Outputs may be NULL:
- *   kernel:  0 = small-vocabulary tile kernel, 1 = cluster row kernel
+ *   kernel:  0 = small-vocabulary tile kernel, 1 = streaming cluster row
+ *            kernel, 2 = resident cluster row kernel (slices staged in shared
+ *            memory by TMA; chosen when rows start on 16-byte boundaries and
+ *            a slice fits shared memory, and the grid is a single wave),
+ *            3 = small-vocabulary tile kernel with TMA-staged, double-buffered
+ *            tiles (16-byte aligned rows)
  *   cluster: CTAs per thread-block cluster splitting each row (1 for kernel 0)
- *   ctas:    total CTAs launched
+ *   ctas:    CTAs launched by a row kernel; tiles of sequences for kernels 0, 3
  *   workspace_bytes: scratch bytes allocated per call
  * Returns SPECV_ERR_INVALID_ARG for sizes specv_verify would reject.
  */

@@ -15,10 +15,16 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultSMs = 152;        // used by specv_plan when no device is visible
 constexpr int kTileSmemBudget = 48 * 1024;
+constexpr int kTmaTileStageBytes = 20 * 1024;  // target + draft rows of one staged tile
 constexpr int kTileMaxV = 256;
 constexpr int kTileMinSeqs = 4;
 constexpr int kTileMaxSeqs = 64;
 constexpr int32_t kMaxK = 4096;
+// Resident row kernel: the staged slices of one CTA (target + draft) may use
+// up to this much shared memory; the planner aims below kResidentTarget so
+// that three CTAs fit an SM.
+constexpr int kResidentMaxSmem = 200 * 1024;
+constexpr int kResidentTarget = 96 * 1024;
 
 struct DeviceState {
   bool ready = false;
@@ -56,7 +62,10 @@ specv_status ensure_device(int *sms_out) {
       return SPECV_ERR_CUDA;
     }
     if (major < 10 || !cluster_ok) return SPECV_ERR_UNSUPPORTED;
-    if ((e = specv::rows_prepare()) != cudaSuccess || (e = specv::tile_prepare(kTileSmemBudget)) != cudaSuccess) {
+    if ((e = specv::rows_prepare()) != cudaSuccess ||
+        (e = specv::resident_prepare(kResidentMaxSmem)) != cudaSuccess ||
+        (e = specv::tile_prepare(kTileSmemBudget)) != cudaSuccess ||
+        (e = specv::tile_tma_prepare(kTileSmemBudget)) != cudaSuccess) {
       note_cuda_error(e);
       return SPECV_ERR_CUDA;
     }
@@ -68,13 +77,14 @@ specv_status ensure_device(int *sms_out) {
 }
 
 struct Plan {
-  int kernel;            // 0 tile, 1 rows
-  int cluster;           // CTAs per cluster (rows kernel)
-  int64_t ctas;          // CTAs of the rows kernel (tile kernel: tiles)
+  int kernel;            // 0 tile, 1 streaming row kernel, 2 resident row kernel, 3 TMA tile
+  int cluster;           // CTAs per cluster (row kernels)
+  int64_t ctas;          // CTAs of the row kernels (tile kernel: tiles)
   int64_t ws_bytes;      // scratch bytes
   int tile_seqs;
   int smem_t, smem_d, smem_total;
   int groups_per_slice, num_groups;
+  int res_smem;          // dynamic shared memory of the resident kernel
 };
 
 int64_t round16(int64_t x) { return (x + 15) / 16 * 16; }
@@ -95,24 +105,51 @@ int cluster_from_env() {
   return (v == 1 || v == 2 || v == 4 || v == 8 || v == 16) ? v : 0;
 }
 
-// The launch plan.  Short rows whose whole sequences fit a shared-memory tile
-// go to the tile kernel; everything else to the cluster row kernel, with the
-// cluster size doubled (up to 16) while the grid has fewer than 4 CTAs per SM
-// and each CTA would still stream at least 4 KiB of every row.
-specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, Plan *p) {
+// "stream" or "resident" forces a row-kernel variant (tuning and tests).
+int variant_from_env() {
+  const char *s = std::getenv("SPECV_ROWS_VARIANT");
+  if (!s) return 0;
+  if (std::strcmp(s, "stream") == 0) return 1;
+  if (std::strcmp(s, "resident") == 0) return 2;
+  return 0;
+}
+
+// The launch plan.
+//  - Short rows whose whole sequences fit a shared-memory tile: tile kernel.
+//  - Row kernels: the streaming cluster size is the smallest power of two
+//    (<= 16) that gives the grid >= 8 CTAs per SM and each CTA <= 512 KiB of
+//    (target + draft) slice, without going under 4 KiB of a row per CTA.
+//  - The resident row kernel (16-byte aligned rows, slice in shared memory)
+//    pays a fixed latency per CTA that only a single wave of clusters hides,
+//    so it is chosen when its grid (smallest cluster size whose slice fits
+//    96 KiB, doubled while the grid has < 4 CTAs per SM) stays within 2 CTAs
+//    per SM; otherwise the streaming row kernel runs.
+//  SPECV_CLUSTER_SIZE and SPECV_ROWS_VARIANT override the choices.
+specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, bool aligned, Plan *p) {
   const int elem = dtype == SPECV_BF16 ? 2 : 4;
   std::memset(p, 0, sizeof(*p));
   const int64_t seq_bytes = (int64_t)(2 * K + 1) * V * elem + (int64_t)(K + 1) * 16;
   if (V <= kTileMaxV && seq_bytes * kTileMinSeqs + 64 <= kTileSmemBudget) {
-    int ts = (int)((kTileSmemBudget - 64) / seq_bytes);
-    if (ts > kTileMaxSeqs) ts = kTileMaxSeqs;
+    const int64_t data_bytes = (int64_t)(2 * K + 1) * V * elem;
+    const bool tma = aligned && ((int64_t)V * elem) % 16 == 0 && data_bytes <= kTmaTileStageBytes;
+    int ts;
+    if (tma) {
+      // two alternating tile buffers of <= 20 KiB each: several CTAs per SM
+      ts = (int)(kTmaTileStageBytes / data_bytes);
+      if (ts > specv::kTmaTileMaxSeqs) ts = specv::kTmaTileMaxSeqs;
+      if (ts >= 8) ts -= ts % 8;
+    } else {
+      ts = (int)((kTileSmemBudget - 64) / seq_bytes);
+      if (ts > kTileMaxSeqs) ts = kTileMaxSeqs;
+    }
     if (ts > B) ts = (int)B;
-    p->kernel = 0;
+    p->kernel = tma ? 3 : 0;
     p->cluster = 1;
     p->tile_seqs = ts;
     p->smem_t = (int)round16((int64_t)ts * (K + 1) * V * elem);
     p->smem_d = (int)round16((int64_t)ts * K * V * elem);
-    p->smem_total = p->smem_t + p->smem_d + ts * (K + 1) * 16;
+    p->smem_total = tma ? 128 + 2 * (p->smem_t + p->smem_d) + ts * (K + 1) * 16
+                        : p->smem_t + p->smem_d + ts * (K + 1) * 16;
     p->ctas = (B + ts - 1) / ts;  // tiles
     p->ws_bytes = 0;
     return SPECV_OK;
@@ -120,19 +157,53 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, Plan
   const int64_t P = B * (K + 1);
   const int vw = 16 / elem;
   const int64_t row_bytes = (int64_t)V * elem;
-  int S = cluster_from_env();
-  if (S == 0) {
-    S = 1;
-    while (S < specv::kMaxCluster && P * S < 4LL * sms && row_bytes / (2 * S) >= 4096) S *= 2;
+  const int64_t G = (V + vw - 1) / vw;
+  const int env_S = cluster_from_env();
+  const int env_var = variant_from_env();
+  const bool can_resident = aligned && (row_bytes % 16 == 0) && env_var != 1;
+  auto slice_smem = [&](int S) { return 2 * ((G + S - 1) / S) * 16; };
+  int S = 0;
+  int kernel = 1;
+  if (can_resident) {
+    if (env_S) {
+      if (slice_smem(env_S) <= kResidentMaxSmem) S = env_S;
+    } else {
+      for (int s = 1; s <= specv::kMaxCluster; s *= 2)
+        if (slice_smem(s) <= kResidentTarget) {
+          S = s;
+          break;
+        }
+      if (S == 0 && slice_smem(specv::kMaxCluster) <= kResidentMaxSmem) S = specv::kMaxCluster;
+      if (S)
+        while (S < specv::kMaxCluster && P * S < 4LL * sms && row_bytes / (2 * S) >= 4096) S *= 2;
+      if (S && env_var != 2 && P * S > 2LL * sms) S = 0;  // several waves: streaming is faster
+    }
+    if (S) kernel = 2;
   }
-  while (S > 1 && P * S > INT32_MAX) S /= 2;
-  if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
-  p->kernel = 1;
+  if (kernel == 2 && P * S > INT32_MAX) kernel = 1;
+  if (env_var == 2 && kernel != 2) return SPECV_ERR_UNSUPPORTED;
+  if (kernel == 1) {
+    S = env_S;
+    if (S == 0) {
+      S = 1;
+      while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
+             (P * S < 8LL * sms || 2 * row_bytes / S > 512 * 1024))
+        S *= 2;
+    }
+    while (S > 1 && P * S > INT32_MAX) S /= 2;
+    if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
+  }
+  p->kernel = kernel;
   p->cluster = S;
   p->ctas = P * S;
-  p->num_groups = (int)((V + vw - 1) / vw);
-  p->groups_per_slice = (p->num_groups + S - 1) / S;
-  p->ws_bytes = round16(P * 16) + round16(B * 4);
+  p->num_groups = (int)G;
+  p->groups_per_slice = (int)((G + S - 1) / S);
+  if (kernel == 2) {
+    p->res_smem = (int)slice_smem(S);
+    p->ws_bytes = round16(P * 8) + round16(B * 4);
+  } else {
+    p->ws_bytes = round16(P * 16) + round16(B * 4);
+  }
   return SPECV_OK;
 }
 
@@ -146,13 +217,15 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
   int sms = kDefaultSMs;
   specv_status s = ensure_device(&sms);
   if (s != SPECV_OK) return s;
-  Plan p;
-  if ((s = make_plan(B, K, V, dtype, sms, &p)) != SPECV_OK) return s;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const int bf16 = dtype == SPECV_BF16;
   const int elem = bf16 ? 2 : 4;
+  const bool aligned = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
+                       ((int64_t)V * elem % 16 == 0);
+  Plan p;
+  if ((s = make_plan(B, K, V, dtype, sms, aligned, &p)) != SPECV_OK) return s;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   cudaError_t e;
-  if (p.kernel == 0) {
+  if (p.kernel == 0 || p.kernel == 3) {
     specv::TileArgs a;
     a.target = target;
     a.draft = draft;
@@ -174,10 +247,12 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
                  ((int64_t)(K + 1) * V * elem % 16 == 0) && ((int64_t)K * V * elem % 16 == 0);
     a.smem_target_bytes = p.smem_t;
     a.smem_draft_bytes = p.smem_d;
-    const int per_sm = specv::tile_blocks_per_sm(bf16, mode, p.smem_total);
+    const int per_sm = p.kernel == 3 ? specv::tile_tma_blocks_per_sm(bf16, mode, p.smem_total)
+                                     : specv::tile_blocks_per_sm(bf16, mode, p.smem_total);
     int64_t grid = (int64_t)sms * per_sm;
     if (grid > p.ctas) grid = p.ctas;
-    e = specv::tile_launch(a, bf16, mode, grid, p.smem_total, stream);
+    e = p.kernel == 3 ? specv::tile_tma_launch(a, bf16, mode, grid, p.smem_total, stream)
+                      : specv::tile_launch(a, bf16, mode, grid, p.smem_total, stream);
     if (e != cudaSuccess) {
       note_cuda_error(e);
       return SPECV_ERR_CUDA;
@@ -191,29 +266,52 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     (void)cudaGetLastError();
     return SPECV_ERR_NO_MEMORY;
   }
-  specv::RowArgs a;
-  a.target = target;
-  a.draft = draft;
-  a.tokens = tokens;
-  a.u_accept = ua;
-  a.u_resample = ur;
-  a.lam = lam;
-  a.B = B;
-  a.K = K;
-  a.V = V;
-  a.out_tokens = out_tokens;
-  a.out_n = out_n;
-  a.ws_stats = static_cast<float4 *>(ws);
-  a.ws_count = reinterpret_cast<unsigned *>(static_cast<char *>(ws) + round16(B * (K + 1) * 16));
-  a.dbg_ptilde = dbg_ptilde;
-  a.dbg_q = dbg_q;
-  a.dbg_lse = dbg_lse;
-  a.groups_per_slice = p.groups_per_slice;
-  a.num_groups = p.num_groups;
-  const bool aligned = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
-                       ((int64_t)V * elem % 16 == 0);
-  e = cudaMemsetAsync(a.ws_count, 0, (size_t)B * sizeof(unsigned), stream);
-  if (e == cudaSuccess) e = specv::rows_launch(a, bf16, mode, aligned, p.cluster, p.ctas, stream);
+  if (p.kernel == 2) {
+    specv::ResArgs r;
+    r.target = target;
+    r.draft = draft;
+    r.tokens = tokens;
+    r.u_accept = ua;
+    r.u_resample = ur;
+    r.lam = lam;
+    r.B = B;
+    r.K = K;
+    r.V = V;
+    r.out_tokens = out_tokens;
+    r.out_n = out_n;
+    r.rec = static_cast<int2 *>(ws);
+    r.count = reinterpret_cast<unsigned *>(static_cast<char *>(ws) + round16(B * (K + 1) * 8));
+    r.dbg_ptilde = dbg_ptilde;
+    r.dbg_q = dbg_q;
+    r.dbg_lse = dbg_lse;
+    r.groups_per_slice = p.groups_per_slice;
+    r.num_groups = p.num_groups;
+    e = cudaMemsetAsync(r.count, 0, (size_t)B * sizeof(unsigned), stream);
+    if (e == cudaSuccess)
+      e = specv::resident_launch(r, bf16, mode, p.cluster, p.ctas, p.res_smem, stream);
+  } else {
+    specv::RowArgs a;
+    a.target = target;
+    a.draft = draft;
+    a.tokens = tokens;
+    a.u_accept = ua;
+    a.u_resample = ur;
+    a.lam = lam;
+    a.B = B;
+    a.K = K;
+    a.V = V;
+    a.out_tokens = out_tokens;
+    a.out_n = out_n;
+    a.ws_stats = static_cast<float4 *>(ws);
+    a.ws_count = reinterpret_cast<unsigned *>(static_cast<char *>(ws) + round16(B * (K + 1) * 16));
+    a.dbg_ptilde = dbg_ptilde;
+    a.dbg_q = dbg_q;
+    a.dbg_lse = dbg_lse;
+    a.groups_per_slice = p.groups_per_slice;
+    a.num_groups = p.num_groups;
+    e = cudaMemsetAsync(a.ws_count, 0, (size_t)B * sizeof(unsigned), stream);
+    if (e == cudaSuccess) e = specv::rows_launch(a, bf16, mode, aligned, p.cluster, p.ctas, stream);
+  }
   const cudaError_t ef = cudaFreeAsync(ws, stream);
   if (e == cudaSuccess) e = ef;
   if (e != cudaSuccess) {
@@ -262,11 +360,11 @@ specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, spec
     (void)cudaGetLastError();
   }
   Plan p;
-  specv_status s = make_plan(B, K, V, dtype, sms, &p);
+  specv_status s = make_plan(B, K, V, dtype, sms, true, &p);
   if (s != SPECV_OK) return s;
   if (kernel) *kernel = p.kernel;
   if (cluster) *cluster = p.cluster;
-  if (ctas) *ctas = p.kernel == 0 ? p.ctas : p.ctas;
+  if (ctas) *ctas = p.ctas;
   if (workspace_bytes) *workspace_bytes = p.ws_bytes;
   return SPECV_OK;
 }

@@ -9,6 +9,9 @@ namespace specv {
 constexpr int kRowThreads = 256;   // threads per CTA of the cluster row kernel
 constexpr int kMaxCluster = 16;    // largest cluster (non-portable size, opt-in)
 constexpr int kTileThreads = 256;  // threads per CTA of the small-vocabulary kernel
+constexpr int kTmaTileMaxSeqs = 32;        // sequences per tile of the TMA tile kernel
+constexpr int kResidentChunkGroups = 1024;  // 16-byte groups per TMA chunk (16 KiB per row)
+constexpr int kResidentMaxChunks = 8;       // chunks per row slice (128 KiB per row at most)
 
 // Arguments of the cluster row kernel (one cluster per (sequence, position)).
 struct RowArgs {
@@ -51,13 +54,45 @@ struct TileArgs {
   int tile_seqs;             // sequences per tile
   int64_t num_tiles;
   int vec_copy;              // 1: tiles start on 16-byte boundaries and span whole vectors
-  int smem_target_bytes;     // bytes of the staged target block (16-byte padded)
-  int smem_draft_bytes;      // bytes of the staged draft block (16-byte padded)
+  int smem_target_bytes;     // bytes of a staged target block (16-byte padded)
+  int smem_draft_bytes;      // bytes of a staged draft block (16-byte padded)
 };
+
+// Arguments of the resident cluster row kernel (slices staged in shared memory,
+// sampling decided per position).
+struct ResArgs {
+  const void *target;        // [B][K+1][V]
+  const void *draft;         // [B][K][V]
+  const int32_t *tokens;     // [B][K]
+  const float *u_accept;     // [B][K]
+  const float *u_resample;   // [B]
+  const float *lam;          // [B]
+  int64_t B;
+  int K;
+  int V;
+  int32_t *out_tokens;       // [B][K+1]
+  int32_t *out_n;            // [B]
+  int2 *rec;                 // scratch [B][K+1]: (status, token) per position
+  unsigned *count;           // scratch [B]: positions published so far (zeroed per call)
+  float *dbg_ptilde;         // optional [B][K]
+  float *dbg_q;              // optional [B][K]
+  float *dbg_lse;            // optional [B][K+1][2]
+  int groups_per_slice;      // 16-byte groups of a row staged by one CTA
+  int num_groups;            // V / elements per 16 bytes (V * sizeof(dtype) % 16 == 0)
+};
+
+cudaError_t resident_prepare(int max_smem);
+cudaError_t resident_launch(const ResArgs &a, int dtype_bf16, int mode, int S, int64_t grid,
+                            int smem, cudaStream_t stream);
 
 cudaError_t rows_prepare();
 cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
                         int64_t grid, cudaStream_t stream);
+
+cudaError_t tile_tma_prepare(int max_smem_bytes);
+int tile_tma_blocks_per_sm(int dtype_bf16, int mode, int smem_bytes);
+cudaError_t tile_tma_launch(const TileArgs &a, int dtype_bf16, int mode, int64_t grid,
+                            int smem_bytes, cudaStream_t stream);
 
 cudaError_t tile_prepare(int max_smem_bytes);
 int tile_blocks_per_sm(int dtype_bf16, int mode, int smem_bytes);

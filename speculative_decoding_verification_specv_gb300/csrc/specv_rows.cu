@@ -32,6 +32,7 @@
 // cluster does phase 2, and the only barriers are hardware cluster barriers.
 #include <cooperative_groups.h>
 
+#include "specv_block.cuh"
 #include "specv_device.cuh"
 #include "specv_internal.h"
 
@@ -42,7 +43,6 @@ namespace specv {
 namespace {
 
 constexpr int kNT = kRowThreads;  // threads per CTA
-constexpr int kNW = kNT / 32;
 constexpr int kUnroll = 4;        // 16-byte groups per thread per batch
 
 struct Broadcast {
@@ -53,14 +53,11 @@ struct Broadcast {
 };
 
 struct __align__(16) RowsShared {
-  float red[kNW][4];
+  BlockScratch<kNT> bs;
   float part[4];
   int last;
   Broadcast bc;
   float masses[2][kMaxCluster];
-  float incl[kNT];
-  int found;
-  int lastpos[kNW];
 };
 
 // Load group g (VW consecutive elements) of a row as one 16-byte vector.  In
@@ -87,52 +84,6 @@ __device__ __forceinline__ uint4 load_group(const T *row, int64_t g, int V) {
     }
     return v;
   }
-}
-
-// Sum of one float per thread in a fixed order (warp butterflies, then the
-// warps in index order); every thread returns the same total.
-__device__ __forceinline__ float block_sum(RowsShared &sh, float x) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, off));
-  if (lane == 0) sh.red[warp][0] = x;
-  __syncthreads();
-  float t = 0.0f;
-#pragma unroll
-  for (int w = 0; w < kNW; ++w) t = __fadd_rn(t, sh.red[w][0]);
-  __syncthreads();
-  return t;
-}
-
-// Inclusive block scan of one float per thread; returns the exclusive value
-// (exactly the previous thread's inclusive value) and the block total.
-__device__ __forceinline__ void block_scan(RowsShared &sh, float x, float &excl, float &incl,
-                                           float &total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float v = x;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    float y = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v = __fadd_rn(v, y);
-  }
-  if (lane == 31) sh.red[warp][0] = v;
-  __syncthreads();
-  if (warp == 0) {
-    float ws = lane < kNW ? sh.red[lane][0] : 0.0f;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      float y = __shfl_up_sync(0xffffffffu, ws, off);
-      if (lane >= off) ws = __fadd_rn(ws, y);
-    }
-    if (lane < kNW) sh.red[lane][2] = ws;  // inclusive warp offsets
-  }
-  __syncthreads();
-  float woff = warp == 0 ? 0.0f : sh.red[warp - 1][2];
-  incl = warp == 0 ? v : __fadd_rn(woff, v);
-  sh.incl[threadIdx.x] = incl;
-  __syncthreads();
-  excl = threadIdx.x == 0 ? 0.0f : sh.incl[threadIdx.x - 1];
-  total = sh.incl[kNT - 1];
 }
 
 // Mass of the sampler weights over this CTA's slice: a streaming reduction
@@ -165,7 +116,7 @@ __device__ float slice_mass(RowsShared &sh, const T *rowA, const T *rowB, int V,
       }
     }
   }
-  return block_sum(sh, acc);
+  return block_sum<kNT>(sh.bs, acc);
 }
 
 // Search of this CTA's slice in index order for the first entry whose running
@@ -180,7 +131,7 @@ __device__ int slice_search(RowsShared &sh, const T *rowA, const T *rowB, int V,
   constexpr int kSearchU = 16 / VW;  // 16 entries per thread per tile
   float base = 0.0f;
   int lastpos = -1;
-  if (threadIdx.x == 0) sh.found = -1;
+  if (threadIdx.x == 0) sh.bs.found = -1;
   for (int tb = g_lo; tb < g_hi; tb += kNT * kSearchU) {
     const int gs = tb + (int)threadIdx.x * kSearchU;
     float w[kSearchU][VW];
@@ -206,7 +157,7 @@ __device__ int slice_search(RowsShared &sh, const T *rowA, const T *rowB, int V,
       }
     }
     float excl, incl, total;
-    block_scan(sh, s, excl, incl, total);
+    block_scan<kNT>(sh.bs, s, excl, incl, total);
     const float lo = __fadd_rn(base, excl), hi = __fadd_rn(base, incl);
     if (lo <= t && t < hi) {  // only one thread: the intervals partition [base, base+total)
       float c = lo;
@@ -219,24 +170,15 @@ __device__ int slice_search(RowsShared &sh, const T *rowA, const T *rowB, int V,
           if (w[u][e] > 0.0f) lastg = (gs + u) * VW + e;
           if (pick < 0 && c > t) pick = (gs + u) * VW + e;
         }
-      sh.found = pick >= 0 ? pick : lastg;
+      sh.bs.found = pick >= 0 ? pick : lastg;
     }
     __syncthreads();
-    const int f = sh.found;
+    const int f = sh.bs.found;
     __syncthreads();
     if (f >= 0) return f;
     base = __fadd_rn(base, total);
   }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-    lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, off));
-  if (lane == 0) sh.lastpos[warp] = lastpos;
-  __syncthreads();
-  int r = -1;
-  for (int k = 0; k < kNW; ++k) r = max(r, sh.lastpos[k]);
-  __syncthreads();
-  return r;
+  return block_max_index<kNT>(sh.bs, lastpos);
 }
 
 template <typename T, int MODE, bool ALIGNED>
@@ -311,26 +253,13 @@ __global__ void __launch_bounds__(kNT) rows_kernel(RowArgs a) {
         }
       }
   }
-  warp_merge_stats(mA, sA);
-  warp_merge_stats(mB, sB);
+  block_merge_stats<kNT>(sh.bs, mA, sA, mB, sB);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) {
-    sh.red[warp][0] = mA;
-    sh.red[warp][1] = sA;
-    sh.red[warp][2] = mB;
-    sh.red[warp][3] = sB;
-  }
-  __syncthreads();
   if (threadIdx.x == 0) {
-    float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
-    for (int w = 0; w < kNW; ++w) {
-      merge_stats(m0, s0, sh.red[w][0], sh.red[w][1]);
-      merge_stats(m1, s1, sh.red[w][2], sh.red[w][3]);
-    }
-    sh.part[0] = m0;
-    sh.part[1] = s0;
-    sh.part[2] = m1;
-    sh.part[3] = s1;
+    sh.part[0] = mA;
+    sh.part[1] = sA;
+    sh.part[2] = mB;
+    sh.part[3] = sB;
   }
   cluster.sync();  // partials of every rank are visible
   if (rank == 0 && threadIdx.x == 0) {

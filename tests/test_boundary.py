@@ -75,11 +75,14 @@ def test_debug_entry_point_validates_too(lib):
 
 def test_plan_selects_kernels(lib):
     p5 = specv.plan(1_000_000, 4, 32, specv.F32)
-    assert p5["kernel"] == "tile" and p5["workspace_bytes"] == 0
+    assert p5["kernel"] == "tile-tma" and p5["workspace_bytes"] == 0
+    assert specv.plan(5, 3, 33, specv.F32)["kernel"] == "tile"  # rows not on 16-byte boundaries
     p4 = specv.plan(256, 8, 128256, specv.F32)
-    assert p4["kernel"] == "rows" and p4["ctas"] == 256 * 9 * p4["cluster"]
+    assert p4["kernel"] == "rows-stream" and p4["ctas"] == 256 * 9 * p4["cluster"]
     assert p4["workspace_bytes"] >= 256 * 9 * 16 + 256 * 4
     p2 = specv.plan(1, 8, 128256, specv.BF16)
-    assert p2["kernel"] == "rows" and p2["cluster"] > 1
+    assert p2["kernel"] == "rows-resident" and p2["cluster"] > 1
+    # a slice of one row of 2^24 fp32 logits cannot fit shared memory
+    assert specv.plan(2, 2, 1 << 24, specv.F32)["kernel"] == "rows-stream"
     with pytest.raises(specv.SpecvError):
         specv.plan(0, 4, 32)

@@ -31,12 +31,14 @@ def specv():
 
 @pytest.fixture
 def cluster_env():
-    old = os.environ.get("SPECV_CLUSTER_SIZE")
+    keys = ("SPECV_CLUSTER_SIZE", "SPECV_ROWS_VARIANT")
+    old = {k: os.environ.get(k) for k in keys}
     yield
-    if old is None:
-        os.environ.pop("SPECV_CLUSTER_SIZE", None)
-    else:
-        os.environ["SPECV_CLUSTER_SIZE"] = old
+    for k, v in old.items():
+        if v is None:
+            os.environ.pop(k, None)
+        else:
+            os.environ[k] = v
 
 
 def _run(specv, x, mode, debug=True):
@@ -103,14 +105,36 @@ def test_parity_full_size_exactness_workload(specv, mode):
 
 
 @pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
-def test_every_cluster_size(specv, cluster_env, S):
+@pytest.mark.parametrize("variant", ["stream", "resident"])
+def test_every_cluster_size(specv, cluster_env, variant, S):
     os.environ["SPECV_CLUSTER_SIZE"] = str(S)
-    for w, mode in ((workloads.WORKLOADS[3].scaled(B=4), 0),
-                    (workloads.WORKLOADS[1].scaled(B=3, K=3, V=50001), 1)):
-        assert specv.plan(w.B, w.K, w.V, 1 if w.dtype == "bf16" else 0)["cluster"] == S
+    os.environ["SPECV_ROWS_VARIANT"] = variant
+    cases = ((workloads.WORKLOADS[3].scaled(B=4), 0),
+             (workloads.WORKLOADS[1].scaled(B=3, K=3, V=50000), 1),
+             (workloads.WORKLOADS[4].scaled(B=2, K=2, V=4096), 0))
+    ran = 0
+    for w, mode in cases:
+        dt = 1 if w.dtype == "bf16" else 0
+        try:
+            plan = specv.plan(w.B, w.K, w.V, dt)
+        except specv.SpecvError:
+            continue  # this slice does not fit shared memory at this cluster size
+        assert plan["cluster"] == S and plan["kernel"] == "rows-" + variant
         x = workloads.make_inputs(w, DEV)
         rep, _, _ = _check(specv, x, mode)
-        print(f"S={S} {w.name} V={w.V}: {rep}")
+        ran += 1
+        print(f"{variant} S={S} {w.name} V={w.V}: {rep}")
+    assert ran >= 1
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+@pytest.mark.parametrize("cfg", [2, 3, 4])
+def test_streaming_variant_on_workloads(specv, cluster_env, cfg, mode):
+    os.environ["SPECV_ROWS_VARIANT"] = "stream"
+    w = SMALL[cfg]
+    x = workloads.make_inputs(w, DEV)
+    rep, _, _ = _check(specv, x, mode)
+    print(f"streaming variant, workload {cfg}: {rep}")
 
 
 RAGGED = [
