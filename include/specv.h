@@ -134,6 +134,35 @@ specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, spec
                         int32_t *kernel, int32_t *cluster, int64_t *ctas,
                         int64_t *workspace_bytes);
 
+/*
+ * specv_verify_noalloc -- specv_verify for callers that cannot let a library
+ * allocate device memory while they run: an engine that hands all of HBM to
+ * its own pools up front, a decode loop where an allocation could stall or
+ * fail, or code that must never see an out-of-memory error from this call.
+ * (The pages have no counterpart: this is an interface choice of this
+ * library, not part of the method.)
+ *
+ * Same arguments, semantics and outputs as specv_verify; it always runs the
+ * streaming cluster row kernel, whose scratch (position statistics and
+ * per-sequence counters) lives in a fixed 1 MiB array inside the library's
+ * device image instead of memory allocated per call.  Limits and rules:
+ *   - B * (K+1) <= 49152 and B <= 65536; larger calls return
+ *     SPECV_ERR_INVALID_ARG and launch nothing;
+ *   - the array exists once per GPU and is shared by every call on that GPU:
+ *     calls whose work overlaps on the GPU (other streams, other host
+ *     threads) race on it; serialise them (e.g. use one stream);
+ *   - the first call on a device looks up the array's address (this also
+ *     loads the library's device code there): make it before any CUDA graph
+ *     capture;
+ *   - no cudaMalloc/cudaFree or other allocating call is made (the counters
+ *     are cleared with cudaMemsetAsync on `stream`).
+ */
+specv_status specv_verify_noalloc(const void *target_logits, const void *draft_logits,
+                                  const int32_t *draft_tokens, const float *u_accept,
+                                  const float *u_resample, const float *lambda, int64_t B,
+                                  int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,
+                                  int32_t *out_tokens, int32_t *out_n_accepted, void *stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char *specv_status_string(specv_status status);
 
