@@ -40,7 +40,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rows_kernel_batched_v128256_f32.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_specv_gb300", "csrc", f)
-                  for f in ("specv_rows.cu", "specv_device.cuh")]
+                  for f in ("specv_rows.cu", "specv_device.cuh", "specv_block.cuh",
+                            "specv_internal.h")]
 
 
 def parse():
