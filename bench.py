@@ -47,7 +47,7 @@ KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_specv_gb
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="specv", choices=["specv", "reference"])
     ap.add_argument("--config", type=int, default=4, choices=sorted(workloads.WORKLOADS))

@@ -15,7 +15,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultSMs = 152;        // used by specv_plan when no device is visible
 constexpr int kTileSmemBudget = 48 * 1024;
-constexpr int kTmaTileStageBytes = 20 * 1024;  // target + draft rows of one staged tile
+constexpr int kTmaTileStageBytes = 40 * 1024;  // target + draft rows of one staged tile
 constexpr int kTileMaxV = 256;
 constexpr int kTileMinSeqs = 4;
 constexpr int kTileMaxSeqs = 64;
@@ -65,7 +65,7 @@ specv_status ensure_device(int *sms_out) {
     if ((e = specv::rows_prepare()) != cudaSuccess ||
         (e = specv::resident_prepare(kResidentMaxSmem)) != cudaSuccess ||
         (e = specv::tile_prepare(kTileSmemBudget)) != cudaSuccess ||
-        (e = specv::tile_tma_prepare(kTileSmemBudget)) != cudaSuccess) {
+        (e = specv::tile_tma_prepare(2 * kTmaTileStageBytes + 16 * 1024)) != cudaSuccess) {
       note_cuda_error(e);
       return SPECV_ERR_CUDA;
     }
@@ -134,10 +134,14 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, bool
     const bool tma = aligned && ((int64_t)V * elem) % 16 == 0 && data_bytes <= kTmaTileStageBytes;
     int ts;
     if (tma) {
-      // two alternating tile buffers of <= 20 KiB each: several CTAs per SM
+      // two alternating tile buffers of <= 40 KiB each; one round of stage-A
+      // row tasks (2K+1 per sequence) for the CTA's threads; at most one
+      // stage-B lane group per sequence
       ts = (int)(kTmaTileStageBytes / data_bytes);
+      const int by_rows = specv::kTileThreads / (2 * K + 1);
+      if (ts > by_rows && by_rows >= 1) ts = by_rows;
       if (ts > specv::kTmaTileMaxSeqs) ts = specv::kTmaTileMaxSeqs;
-      if (ts >= 8) ts -= ts % 8;
+      if (ts < 1) ts = 1;
     } else {
       ts = (int)((kTileSmemBudget - 64) / seq_bytes);
       if (ts > kTileMaxSeqs) ts = kTileMaxSeqs;

@@ -140,10 +140,11 @@ __device__ __forceinline__ float accept_ratio(int mode, const PosStats &st, floa
   float db = __fsub_rn(zq_x, st.mB);
   float d = __fsub_rn(da, db);
   float e = (d == 0.0f) ? 1.0f : ex2(__fmul_rn(d, kLog2e));
-  float r = __fmul_rn(e, __fdiv_rn(st.sB, st.sA));
+  // sB / sA with the SFU reciprocal (a few ulp); exactly 1 for equal sums
+  float r = __fmul_rn(e, st.sB == st.sA ? 1.0f : __fdividef(st.sB, st.sA));
   if (ptilde_x != nullptr) {
-    float q = __fdiv_rn(ex2(__fmul_rn(db, kLog2e)), st.sB);
-    float pa = __fdiv_rn(ex2(__fmul_rn(da, kLog2e)), st.sA);
+    float q = __fdividef(ex2(__fmul_rn(db, kLog2e)), st.sB);
+    float pa = __fdividef(ex2(__fmul_rn(da, kLog2e)), st.sA);
     *q_x = q;
     *ptilde_x = (mode == kProbMix) ? __fmaf_rn(lam, q, __fmul_rn(__fsub_rn(1.0f, lam), pa)) : pa;
   }
@@ -169,6 +170,20 @@ enum : int { kWResidual = 0, kWBonus = 1, kWMixture = 2 };
 struct SampleParams {
   float mA, invSA, mB, invSB, lam;
 };
+
+// Sampler parameters of a position from its statistics.  The reciprocals are
+// SFU approximations: a common factor on a weight vector does not move its
+// normalised CDF beyond round-off, and equal sums give equal reciprocals.
+__device__ __forceinline__ SampleParams make_sample_params(float mA, float sA, float mB, float sB,
+                                                           float lam) {
+  SampleParams p;
+  p.mA = mA;
+  p.invSA = __fdividef(1.0f, sA);
+  p.mB = mB;
+  p.invSB = __fdividef(1.0f, sB);
+  p.lam = lam;
+  return p;
+}
 
 __device__ __forceinline__ float sample_weight(int mode, int kind, const SampleParams &p, float zt,
                                                float zq) {

@@ -189,8 +189,10 @@ __device__ void finalize_sequence(const ResArgs &a, int64_t b) {
     if (j <= K) st = __ldcg(&a.rec[b * (K + 1) + j]).x;
     const unsigned rej = __ballot_sync(0xffffffffu, j < K && st == kRecRejected);
     if (rej != 0u && n == K) n = j0 + __ffs(rej) - 1;
-    if (__any_sync(0xffffffffu, st == kRecError)) bad = kRecError;
-    else if (bad == 0 && __any_sync(0xffffffffu, st == kRecInvalid)) bad = kRecInvalid;
+    const bool any_err = __any_sync(0xffffffffu, st == kRecError);  // every lane votes
+    const bool any_inv = __any_sync(0xffffffffu, st == kRecInvalid);
+    if (any_err) bad = kRecError;
+    else if (bad == 0 && any_inv) bad = kRecInvalid;
   }
   if (bad != 0) {
     for (int j = lane; j <= K; j += 32) a.out_tokens[b * (K + 1) + j] = -1;

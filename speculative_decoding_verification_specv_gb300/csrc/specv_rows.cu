@@ -308,7 +308,8 @@ __global__ void __launch_bounds__(kNT) rows_kernel(RowArgs a) {
       const unsigned rej = __ballot_sync(0xffffffffu, rejected);
       if (rej != 0u && n == K) n = i0 + __ffs(rej) - 1;
     }
-    const bool valid = lam_ok && __all_sync(0xffffffffu, lane_ok);
+    const bool all_tok = __all_sync(0xffffffffu, lane_ok);  // every lane votes
+    const bool valid = lam_ok && all_tok;
     if (a.dbg_lse) {
       for (int j = lane; j <= K; j += 32) {
         const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + j]);

@@ -6,15 +6,16 @@
 // brings a tile into shared memory; two tile buffers alternate, so the next
 // tile is in flight while this one is processed.  Per tile:
 //   stage A: one thread per row computes (max, sum-exp) of the p~ source
-//            row (target, or mixed in logit mode) or of the draft row with
-//            16-byte shared-memory reads; the walk over a row starts at a
+//            row (target, or mixed in logit mode) or of the draft row in one
+//            pass of 16-byte shared-memory reads; the walk starts at a
 //            per-position offset (the same for the target and draft row of a
 //            position, so identical rows give identical statistics) that
 //            spreads simultaneous reads over the banks;
-//   stage B: one warp per sequence: lane j tests position j, a ballot gives
-//            the first rejection, and the inverse CDF runs as a warp scan
-//            (one pass when V <= 32: the scan total is the mass and the
-//            crossing lane is the token).
+//   stage B: a group of kLanes lanes per sequence (kLanes = 8; four
+//            sequences per warp in lockstep): lanes 0..K-1 of the group test
+//            positions 0..K-1, a ballot gives the first rejection, and the
+//            inverse CDF is a segmented scan across the group, each lane
+//            owning a contiguous run of 16-byte groups of the row.
 // The per-sequence scalars (tokens, uniforms, lambda) are loaded into
 // registers before stage A so their latency overlaps it.  No scratch memory.
 #include "specv_block.cuh"
@@ -26,8 +27,7 @@ namespace specv {
 namespace {
 
 constexpr int kNT = kTileThreads;
-constexpr int kNW = kNT / 32;
-constexpr int kSeqPerWarp = kTmaTileMaxSeqs / kNW;  // prefetched sequences per warp
+constexpr int kLanes = kTmaTileLanes;          // lanes per sequence in stage B
 
 template <typename T>
 __device__ __forceinline__ float sval(const T *p);
@@ -41,106 +41,40 @@ __device__ __forceinline__ float sval<uint16_t>(const uint16_t *p) {
 }
 
 // (max, sum-exp) of one staged row (or the mixed row of a pair) of G groups,
-// walked from group `rot` onwards.
+// one pass from group `rot` onwards: a per-group max, a rescale when it
+// grows, and 2^(z*log2e - m*log2e) with one FFMA per entry (the rounding of
+// m*log2e is a common factor of the row and cancels in every probability).
 template <typename T, int MODE>
 __device__ __forceinline__ float2 row_stats(const uint4 *ra, const uint4 *rb, int G, int rot,
                                             bool mixed, float lam) {
   constexpr int VW = Elem<T>::kPerVec;
-  float m = -INFINITY;
+  float m = -INFINITY, mL = -INFINITY, s = 0.0f;
+  int g = rot;
   for (int k = 0; k < G; ++k) {
-    int g = k + rot;
-    g = g >= G ? g - G : g;
+    float z[VW];
     const uint4 va = ra[g];
     if (MODE == kLogitMix && mixed) {
       const uint4 vb = rb[g];
 #pragma unroll
-      for (int e = 0; e < VW; ++e)
-        m = fmaxf(m, mix_logit(Elem<T>::get(va, e), Elem<T>::get(vb, e), lam));
+      for (int e = 0; e < VW; ++e) z[e] = mix_logit(Elem<T>::get(va, e), Elem<T>::get(vb, e), lam);
     } else {
 #pragma unroll
-      for (int e = 0; e < VW; ++e) m = fmaxf(m, Elem<T>::get(va, e));
+      for (int e = 0; e < VW; ++e) z[e] = Elem<T>::get(va, e);
     }
-  }
-  float s = 0.0f;
-  for (int k = 0; k < G; ++k) {
-    int g = k + rot;
-    g = g >= G ? g - G : g;
-    const uint4 va = ra[g];
-    if (MODE == kLogitMix && mixed) {
-      const uint4 vb = rb[g];
+    float bm = z[0];
 #pragma unroll
-      for (int e = 0; e < VW; ++e)
-        s = __fadd_rn(s, exp_shifted(mix_logit(Elem<T>::get(va, e), Elem<T>::get(vb, e), lam), m));
-    } else {
-#pragma unroll
-      for (int e = 0; e < VW; ++e) s = __fadd_rn(s, exp_shifted(Elem<T>::get(va, e), m));
+    for (int e = 1; e < VW; ++e) bm = fmaxf(bm, z[e]);
+    if (bm > m) {
+      const float nmL = __fmul_rn(bm, kLog2e);
+      s = __fmul_rn(s, ex2(__fsub_rn(mL, nmL)));
+      m = bm;
+      mL = nmL;
     }
+#pragma unroll
+    for (int e = 0; e < VW; ++e) s = __fadd_rn(s, ex2(__fmaf_rn(z[e], kLog2e, -mL)));
+    g = (g + 1 == G) ? 0 : g + 1;
   }
   return make_float2(m, s);
-}
-
-__device__ __forceinline__ float warp_incl_scan(float v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v = __fadd_rn(v, y);
-  }
-  return v;
-}
-
-// Inverse CDF over one staged row (pair) by one warp, entries in index order
-// in tiles of 32 (lane l takes entry v0 + l).  Returns the token, or -1 if the
-// weights have no mass; *mass receives the total.  For V <= 32 the mass and
-// the search are one scan; otherwise a mass scan precedes the search scan,
-// both accumulating identically.
-template <typename T, int MODE>
-__device__ int warp_sample(const T *ra, const T *rb, int V, int kind, const SampleParams &sp,
-                           float u, float *mass) {
-  const int lane = threadIdx.x & 31;
-  if (V <= 32) {
-    float w = 0.0f;
-    if (lane < V) w = sample_weight(MODE, kind, sp, sval<T>(ra + lane), kind != kWBonus ? sval<T>(rb + lane) : 0.0f);
-    const float incl = warp_incl_scan(w);
-    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0.0f;
-    const float R = __shfl_sync(0xffffffffu, incl, 31);
-    *mass = R;
-    if (!(R > 0.0f)) return -1;
-    const float t = __fmul_rn(u, R);
-    const unsigned hit = __ballot_sync(0xffffffffu, lane < V && excl <= t && t < incl);
-    if (hit) return __ffs(hit) - 1;
-    const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0f);
-    return 31 - __clz(pos);  // u*R not below the total: the last entry with mass
-  }
-  float R = 0.0f;
-  for (int v0 = 0; v0 < V; v0 += 32) {
-    const int v = v0 + lane;
-    float w = 0.0f;
-    if (v < V) w = sample_weight(MODE, kind, sp, sval<T>(ra + v), kind != kWBonus ? sval<T>(rb + v) : 0.0f);
-    R = __fadd_rn(R, __shfl_sync(0xffffffffu, warp_incl_scan(w), 31));
-  }
-  *mass = R;
-  if (!(R > 0.0f)) return -1;
-  const float t = __fmul_rn(u, R);
-  float base = 0.0f;
-  int lastpos = -1;
-  for (int v0 = 0; v0 < V; v0 += 32) {
-    const int v = v0 + lane;
-    float w = 0.0f;
-    if (v < V) w = sample_weight(MODE, kind, sp, sval<T>(ra + v), kind != kWBonus ? sval<T>(rb + v) : 0.0f);
-    if (w > 0.0f) lastpos = v;
-    const float incl = warp_incl_scan(w);
-    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0.0f;
-    const float lo = __fadd_rn(base, excl), hi = __fadd_rn(base, incl);
-    const unsigned hit = __ballot_sync(0xffffffffu, v < V && lo <= t && t < hi);
-    if (hit) return v0 + __ffs(hit) - 1;
-    base = __fadd_rn(base, __shfl_sync(0xffffffffu, incl, 31));
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, off));
-  return lastpos;
 }
 
 template <typename T, int MODE>
@@ -149,13 +83,18 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
   const int K = a.K, V = a.V, TS = a.tile_seqs;
-  const int G = V / VW;  // 16-byte groups per row
+  const int G = V / VW;                      // 16-byte groups per row
+  const int C = (G + kLanes - 1) / kLanes;   // groups per lane in stage B
   const int stage_bytes = a.smem_target_bytes + a.smem_draft_bytes;
   unsigned char *stage0 = smem + 128;
   float *st_s = reinterpret_cast<float *>(stage0 + 2 * stage_bytes);  // [TS][K+1][4]
   const T *tgt = static_cast<const T *>(a.target);
   const T *dft = static_cast<const T *>(a.draft);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gl = lane % kLanes;                         // lane within the sequence group
+  const int gsh = lane - gl;                            // first lane of the group
+  const unsigned gmask = ((1u << kLanes) - 1u) << gsh;  // the group's lanes
+  const int sq = threadIdx.x / kLanes;                  // stage-B sequence of this thread
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[0], 1);
@@ -188,27 +127,22 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
     const int nseq = (int)((a.B - b0) < TS ? (a.B - b0) : TS);
     const T *st_t = reinterpret_cast<const T *>(stage0 + stage * stage_bytes);
     const T *st_d = reinterpret_cast<const T *>(stage0 + stage * stage_bytes + a.smem_target_bytes);
+    const bool mine = sq < nseq;  // this thread's group has a sequence in stage B
+    const int64_t b = b0 + (mine ? sq : 0);
 
-    // prefetch the per-sequence scalars of this warp's sequences
-    float p_lam[kSeqPerWarp], p_ur[kSeqPerWarp], p_ua[kSeqPerWarp];
-    int p_tok[kSeqPerWarp];
-#pragma unroll
-    for (int m = 0; m < kSeqPerWarp; ++m) {
-      const int s = warp + m * kNW;
-      p_lam[m] = p_ur[m] = p_ua[m] = 0.0f;
-      p_tok[m] = 0;
-      if (s < nseq) {
-        const int64_t b = b0 + s;
-        p_lam[m] = a.lam[b];
-        p_ur[m] = a.u_resample[b];
-        if (lane < K) {
-          p_tok[m] = a.tokens[b * K + lane];
-          p_ua[m] = a.u_accept[b * K + lane];
-        }
+    // prefetch this group's per-sequence scalars (lane j < K of the group: x_j, u_j)
+    float p_lam = 0.0f, p_ur = 0.0f, p_ua = 0.0f;
+    int p_tok = 0;
+    if (mine) {
+      p_lam = a.lam[b];
+      p_ur = a.u_resample[b];
+      if (gl < K) {
+        p_tok = a.tokens[b * K + gl];
+        p_ua = a.u_accept[b * K + gl];
       }
     }
 
-    const bool ok = !dead && __syncthreads_and(mbar_wait(&bar[stage], parity)) != 0;
+    const bool ok = __syncthreads_and(dead ? 0 : (int)mbar_wait(&bar[stage], parity)) != 0;
     dead = !ok;
 
     // stage A: one thread per row; A-rows (p~ source) of all positions first,
@@ -216,7 +150,7 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
     const int nA = ok ? nseq * (K + 1) : 0, nB = ok ? nseq * K : 0;
     for (int task = threadIdx.x; task < nA + nB; task += kNT) {
       int pos, s, i;
-      bool isA = task < nA;
+      const bool isA = task < nA;
       if (isA) {
         pos = task;
         s = pos / (K + 1);
@@ -230,91 +164,149 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
       const int rot = pos % G;
       const uint4 *rt = reinterpret_cast<const uint4 *>(st_t + (int64_t)pos * V);
       const uint4 *rd = reinterpret_cast<const uint4 *>(st_d + ((int64_t)s * K + (i < K ? i : 0)) * V);
-      const float lam = a.lam[b0 + s];
       float2 r;
       if (isA)
-        r = row_stats<T, MODE>(rt, rd, G, rot, i < K, lam);
+        r = row_stats<T, MODE>(rt, rd, G, rot, i < K, a.lam[b0 + s]);
       else
-        r = row_stats<T, kProbMix>(rd, rd, G, rot, false, lam);
+        r = row_stats<T, kProbMix>(rd, rd, G, rot, false, 0.0f);
       st_s[pos * 4 + (isA ? 0 : 2)] = r.x;
       st_s[pos * 4 + (isA ? 1 : 3)] = r.y;
     }
     __syncthreads();
 
-    // stage B: one warp per sequence (unrolled: the prefetched scalars stay in registers)
-#pragma unroll
-    for (int m = 0; m < kSeqPerWarp; ++m) {
-      const int s = warp + m * kNW;
-      if (s >= nseq) break;
-      const int64_t b = b0 + s;
-      const float lam = p_lam[m];
-      if (!ok) {  // a copy did not complete in time: report, skip
-        for (int j = lane; j <= K; j += 32) a.out_tokens[b * (K + 1) + j] = -1;
-        if (lane == 0) a.out_n[b] = -2;
-        continue;
+    // stage B: kLanes lanes per sequence (all lanes of a warp stay converged;
+    // groups without a sequence compute on placeholders and write nothing)
+    if (!ok) {
+      if (mine) {
+        for (int j = gl; j <= K; j += kLanes) a.out_tokens[b * (K + 1) + j] = -1;
+        if (gl == 0) a.out_n[b] = -2;
       }
+    } else {
+      const int sl = mine ? sq : 0;  // staged sequence slot (a valid one for idle groups)
+      const float lam = p_lam;
       const bool lam_ok = lambda_valid(lam);
       bool lane_ok = true;
       int n = K;
-      for (int i0 = 0; i0 < K; i0 += 32) {
-        const int j = i0 + lane;
+      for (int i0 = 0; i0 < K; i0 += kLanes) {
+        const int j = i0 + gl;
         bool rejected = false;
         if (j < K) {
-          const int x = i0 == 0 ? p_tok[m] : a.tokens[b * K + j];
-          const float u = i0 == 0 ? p_ua[m] : a.u_accept[b * K + j];
+          const int x = i0 == 0 ? p_tok : a.tokens[b * K + j];
+          const float u = i0 == 0 ? p_ua : a.u_accept[b * K + j];
           const bool tok_ok = x >= 0 && x < V;
           lane_ok = lane_ok && tok_ok;
           if (tok_ok && lam_ok) {
-            const int pos = s * (K + 1) + j;
-            const PosStats st{st_s[pos * 4 + 0], st_s[pos * 4 + 1], st_s[pos * 4 + 2],
-                              st_s[pos * 4 + 3]};
+            const int pos = sl * (K + 1) + j;
+            const float4 st4 = reinterpret_cast<const float4 *>(st_s)[pos];
+            const PosStats st{st4.x, st4.y, st4.z, st4.w};
             const float zt_x = sval<T>(st_t + (int64_t)pos * V + x);
-            const float zq_x = sval<T>(st_d + ((int64_t)s * K + j) * V + x);
+            const float zq_x = sval<T>(st_d + ((int64_t)sl * K + j) * V + x);
             float px = 0.0f, qx = 0.0f;
-            const float ratio =
-                accept_ratio(MODE, st, zt_x, zq_x, lam, a.dbg_ptilde ? &px : nullptr, &qx);
+            const bool dbg = mine && a.dbg_ptilde != nullptr;
+            const float ratio = accept_ratio(MODE, st, zt_x, zq_x, lam, dbg ? &px : nullptr, &qx);
             rejected = !accept_test(u, ratio);
-            if (a.dbg_ptilde) {
+            if (dbg) {
               a.dbg_ptilde[b * K + j] = px;
               a.dbg_q[b * K + j] = qx;
             }
           }
         }
-        const unsigned rej = __ballot_sync(0xffffffffu, rejected);
+        const unsigned rej = (__ballot_sync(0xffffffffu, rejected) & gmask) >> gsh;
         if (rej != 0u && n == K) n = i0 + __ffs(rej) - 1;
       }
-      const bool valid = lam_ok && __all_sync(0xffffffffu, lane_ok);
-      if (a.dbg_lse) {
-        for (int j = lane; j <= K; j += 32) {
-          const int pos = s * (K + 1) + j;
+      // the ballot runs on every lane: groups differ in lam_ok (no short-circuit)
+      const unsigned bad_tok = __ballot_sync(0xffffffffu, !lane_ok) & gmask;
+      const bool valid = lam_ok && bad_tok == 0u;
+      if (mine && a.dbg_lse) {
+        for (int j = gl; j <= K; j += kLanes) {
+          const int pos = sl * (K + 1) + j;
           a.dbg_lse[(b * (K + 1) + j) * 2 + 0] = st_s[pos * 4 + 0] + lg2(st_s[pos * 4 + 1]) * kLn2;
           a.dbg_lse[(b * (K + 1) + j) * 2 + 1] =
               j < K ? st_s[pos * 4 + 2] + lg2(st_s[pos * 4 + 3]) * kLn2 : 0.0f;
         }
       }
-      for (int j = lane; j <= K; j += 32) {
-        int out = -1;
-        if (valid && j < n) out = j == lane ? p_tok[m] : a.tokens[b * K + j];  // lane j prefetched x_j
-        if (!valid || j != n) a.out_tokens[b * (K + 1) + j] = out;
+      if (mine) {
+        for (int j = gl; j <= K; j += kLanes) {
+          int out = -1;
+          if (valid && j < n) out = j == gl ? p_tok : a.tokens[b * K + j];  // lane j prefetched x_j
+          if (!valid || j != n) a.out_tokens[b * (K + 1) + j] = out;
+        }
+        if (gl == 0) a.out_n[b] = valid ? n : -1;
       }
-      if (lane == 0) a.out_n[b] = valid ? n : -1;
-      if (!valid) continue;
-      const int pos = s * (K + 1) + n;
-      SampleParams sp;
-      sp.mA = st_s[pos * 4 + 0];
-      sp.invSA = __fdiv_rn(1.0f, st_s[pos * 4 + 1]);
-      sp.mB = st_s[pos * 4 + 2];
-      sp.invSB = __fdiv_rn(1.0f, st_s[pos * 4 + 3]);
-      sp.lam = lam;
-      int kind = (n == K) ? kWBonus
-                          : ((MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual);
-      const T *ra = st_t + (int64_t)pos * V;
-      const T *rb = st_d + ((int64_t)s * K + (n < K ? n : 0)) * V;
-      float R = 0.0f;
-      int tok = warp_sample<T, MODE>(ra, rb, V, kind, sp, p_ur[m], &R);
-      if (!(R > 0.0f) && kind == kWResidual)  // zero residual mass (round-off only): p~ instead
-        tok = warp_sample<T, MODE>(ra, rb, V, kWMixture, sp, p_ur[m], &R);
-      if (lane == 0) a.out_tokens[b * (K + 1) + n] = tok;
+      // sampling: lane gl owns groups [gl*C, gl*C + C) of the row (pair) at n
+      const int nn = valid ? n : 0;
+      const int pos = sl * (K + 1) + nn;
+      const float4 st4 = reinterpret_cast<const float4 *>(st_s)[pos];
+      const SampleParams sp = make_sample_params(st4.x, st4.y, st4.z, st4.w, lam);
+      int kind = (nn == K) ? kWBonus
+                           : ((MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual);
+      const uint4 *ra = reinterpret_cast<const uint4 *>(st_t + (int64_t)pos * V);
+      const uint4 *rb = reinterpret_cast<const uint4 *>(st_d + ((int64_t)sl * K + (nn < K ? nn : 0)) * V);
+      int tok = -1;
+      for (int attempt = 0; attempt < 2; ++attempt) {
+        float mysum = 0.0f;
+        int mylast = -1;
+        for (int c = 0; c < C; ++c) {
+          const int g = gl * C + c;
+          if (g < G) {
+            const uint4 za = ra[g];
+            const uint4 zb = kind != kWBonus ? rb[g] : za;
+#pragma unroll
+            for (int e = 0; e < VW; ++e) {
+              const float w = sample_weight(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e));
+              mysum = __fadd_rn(mysum, w);
+              if (w > 0.0f) mylast = g * VW + e;
+            }
+          }
+        }
+        // segmented inclusive scan of the lane sums over the group
+        float incl = mysum;
+#pragma unroll
+        for (int off = 1; off < kLanes; off <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, incl, off, kLanes);
+          if (gl >= off) incl = __fadd_rn(incl, y);
+        }
+        float excl = __shfl_up_sync(0xffffffffu, incl, 1, kLanes);
+        if (gl == 0) excl = 0.0f;
+        const float R = __shfl_sync(0xffffffffu, incl, kLanes - 1, kLanes);
+        const bool retry = !(R > 0.0f) && kind == kWResidual;
+        // Every ballot and shuffle below runs on all 32 lanes (the four groups
+        // of a warp differ in R, retry and owner); results are selected after.
+        const bool have = R > 0.0f;
+        const float t = __fmul_rn(p_ur, R);
+        const bool own = have && excl <= t && t < incl;  // at most one lane of a group
+        int pick = -1;
+        if (own) {  // walk this lane's entries in order (no warp collectives inside)
+          float c0 = excl;
+          int lastg = -1;
+          for (int c = 0; c < C && pick < 0; ++c) {
+            const int g = gl * C + c;
+            if (g < G) {
+              const uint4 za = ra[g];
+              const uint4 zb = kind != kWBonus ? rb[g] : za;
+#pragma unroll
+              for (int e = 0; e < VW; ++e) {
+                const float w =
+                    sample_weight(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e));
+                c0 = __fadd_rn(c0, w);
+                if (w > 0.0f) lastg = g * VW + e;
+                if (pick < 0 && c0 > t) pick = g * VW + e;
+              }
+            }
+          }
+          if (pick < 0) pick = lastg;
+        }
+        const unsigned owner = (__ballot_sync(0xffffffffu, own) & gmask) >> gsh;
+        const int picked = __shfl_sync(0xffffffffu, pick, owner != 0u ? __ffs(owner) - 1 : 0, kLanes);
+        int lastpos = mylast;  // u*R not below the total (round-off): the last entry with mass
+#pragma unroll
+        for (int off = kLanes / 2; off > 0; off >>= 1)
+          lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, off, kLanes));
+        if (!retry && have) tok = owner != 0u ? picked : lastpos;
+        if (!__any_sync(0xffffffffu, retry)) break;
+        if (retry) kind = kWMixture;  // zero residual mass (round-off only): p~ instead
+      }
+      if (mine && valid && gl == 0) a.out_tokens[b * (K + 1) + n] = tok;
     }
     __syncthreads();  // every thread is done with this stage's rows and stats
     if (threadIdx.x == 0 && !dead && tile + 2 * (int64_t)gridDim.x < a.num_tiles) {
