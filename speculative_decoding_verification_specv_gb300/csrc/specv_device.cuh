@@ -197,4 +197,20 @@ __device__ __forceinline__ float sample_weight(int mode, int kind, const SampleP
   return pa;
 }
 
+// sample_weight without branches on `kind`: every candidate is computed and
+// one is selected, for warps whose lanes serve sequences of different kinds
+// (a bonus sequence next to a residual one).  Same values as sample_weight;
+// the candidates not selected may be non-finite and are discarded.
+__device__ __forceinline__ float sample_weight_sel(int mode, int kind, const SampleParams &p,
+                                                   float zt, float zq) {
+  const float a = (mode == kProbMix) ? zt : mix_logit(zt, zq, p.lam);
+  const float pa = __fmul_rn(exp_shifted(a, p.mA), p.invSA);
+  const float pq = __fmul_rn(exp_shifted(zq, p.mB), p.invSB);
+  const float bonus = (mode == kProbMix) ? pa : __fmul_rn(exp_shifted(zt, p.mA), p.invSA);
+  const float resid = fmaxf(0.0f, __fsub_rn(pa, pq));
+  const float mixed =
+      (mode == kProbMix) ? __fmaf_rn(p.lam, pq, __fmul_rn(__fsub_rn(1.0f, p.lam), pa)) : pa;
+  return kind == kWBonus ? bonus : (kind == kWResidual ? resid : mixed);
+}
+
 }  // namespace specv

@@ -118,6 +118,31 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
     if (first + gridDim.x < a.num_tiles) issue(first + gridDim.x, 1);
   }
 
+  // This thread's first stage-A task of a full tile (the same in every full
+  // tile): computed once, so full tiles need no integer division per row.
+  const int fA = TS * (K + 1), fB = TS * K;
+  const bool has_task = (int)threadIdx.x < fA + fB;
+  int t_pos = 0, t_rd = 0, t_rot = 0, t_s = 0;
+  bool t_isA = false, t_mixed = false;
+  if (has_task) {
+    int s_, i_;
+    t_isA = (int)threadIdx.x < fA;
+    if (t_isA) {
+      t_pos = threadIdx.x;
+      s_ = t_pos / (K + 1);
+      i_ = t_pos - s_ * (K + 1);
+    } else {
+      const int t2 = threadIdx.x - fA;
+      s_ = t2 / K;
+      i_ = t2 - s_ * K;
+      t_pos = s_ * (K + 1) + i_;
+    }
+    t_s = s_;
+    t_mixed = t_isA && i_ < K;
+    t_rd = (s_ * K + (i_ < K ? i_ : 0)) * V;
+    t_rot = t_pos % G;
+  }
+
   int k = 0;
   bool dead = false;  // a copy of this CTA timed out: no more waits, report -2
   for (int64_t tile = first; tile < a.num_tiles; tile += gridDim.x, ++k) {
@@ -148,7 +173,20 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
     // stage A: one thread per row; A-rows (p~ source) of all positions first,
     // then the draft rows
     const int nA = ok ? nseq * (K + 1) : 0, nB = ok ? nseq * K : 0;
-    for (int task = threadIdx.x; task < nA + nB; task += kNT) {
+    const bool full = nseq == TS;
+    if (ok && full && has_task) {
+      const uint4 *rt = reinterpret_cast<const uint4 *>(st_t + (int64_t)t_pos * V);
+      const uint4 *rd = reinterpret_cast<const uint4 *>(st_d + t_rd);
+      float2 r;
+      if (t_isA)
+        r = row_stats<T, MODE>(rt, rd, G, t_rot, t_mixed, a.lam[b0 + t_s]);
+      else
+        r = row_stats<T, kProbMix>(rd, rd, G, t_rot, false, 0.0f);
+      st_s[t_pos * 4 + (t_isA ? 0 : 2)] = r.x;
+      st_s[t_pos * 4 + (t_isA ? 1 : 3)] = r.y;
+    }
+    // remaining tasks (several per thread, or the last, partial tile)
+    for (int task = full ? threadIdx.x + kNT : threadIdx.x; task < nA + nB; task += kNT) {
       int pos, s, i;
       const bool isA = task < nA;
       if (isA) {
@@ -176,7 +214,10 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
 
     // stage B: kLanes lanes per sequence (all lanes of a warp stay converged;
     // groups without a sequence compute on placeholders and write nothing)
-    if (!ok) {
+    const bool warp_busy = __any_sync(0xffffffffu, mine);  // warp-uniform
+    if (!warp_busy) {
+      // no sequence of this tile in this warp
+    } else if (!ok) {
       if (mine) {
         for (int j = gl; j <= K; j += kLanes) a.out_tokens[b * (K + 1) + j] = -1;
         if (gl == 0) a.out_n[b] = -2;
@@ -253,7 +294,7 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
             const uint4 zb = kind != kWBonus ? rb[g] : za;
 #pragma unroll
             for (int e = 0; e < VW; ++e) {
-              const float w = sample_weight(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e));
+              const float w = sample_weight_sel(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e));
               mysum = __fadd_rn(mysum, w);
               if (w > 0.0f) mylast = g * VW + e;
             }
@@ -287,7 +328,7 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
 #pragma unroll
               for (int e = 0; e < VW; ++e) {
                 const float w =
-                    sample_weight(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e));
+                    sample_weight_sel(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e));
                 c0 = __fadd_rn(c0, w);
                 if (w > 0.0f) lastg = g * VW + e;
                 if (pick < 0 && c0 > t) pick = g * VW + e;
