@@ -27,8 +27,15 @@
  * Conventions for every entry point:
  *   - All array pointers are DEVICE pointers to contiguous row-major memory
  *     owned by the caller; the library never frees or retains them.  The
- *     only memory the library allocates is a small scratch workspace
- *     (per call, stream-ordered on `stream`, released on `stream`).
+ *     only memory the library allocates is a small scratch workspace for the
+ *     row kernels (16*B*(K+1) + 4*B bytes at most), one per (device, stream):
+ *     created on the first call on that stream that needs it, reused by
+ *     every later call on the stream (calls on one stream are ordered, so
+ *     they never overlap), kept until the process exits.  A call made while
+ *     `stream` is being captured into a CUDA graph uses the stream's existing
+ *     workspace (the graph then refers to it: replay such a graph only where
+ *     it cannot overlap other calls on that stream); if there is none yet it
+ *     takes stream-ordered memory for that call alone (graph-owned).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are asynchronous: they return after the launch;
  *     faults surface at the caller's next synchronisation.

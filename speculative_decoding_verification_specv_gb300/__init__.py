@@ -196,7 +196,7 @@ def plan(B: int, K: int, V: int, dtype: int = F32, mode: int = PROB_MIX) -> dict
     st = load().specv_plan(int(B), int(K), int(V), int(dtype), int(mode), ctypes.byref(kern),
                            ctypes.byref(clus), ctypes.byref(ctas), ctypes.byref(ws))
     _check(st, "specv_plan")
-    names = {0: "tile", 1: "rows-stream", 2: "rows-resident", 3: "tile-tma"}
+    names = {0: "tile", 1: "rows-stream", 2: "rows-resident", 3: "tile-tma", 4: "rows-spec"}
     return dict(kernel=names.get(kern.value, str(kern.value)), cluster=clus.value,
                 ctas=ctas.value, workspace_bytes=ws.value)
 

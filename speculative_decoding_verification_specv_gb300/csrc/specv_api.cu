@@ -6,6 +6,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "specv.h"
 #include "specv_internal.h"
@@ -14,6 +15,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultSMs = 152;        // used by specv_plan when no device is visible
+constexpr int64_t kDefaultL2 = 126LL * 1024 * 1024;
 constexpr int kTileSmemBudget = 48 * 1024;
 constexpr int kTmaTileStageBytes = 40 * 1024;  // target + draft rows of one staged tile
 constexpr int kTileMaxV = 256;
@@ -30,10 +32,88 @@ struct DeviceState {
   bool ready = false;
   cudaError_t err = cudaSuccess;
   int sms = kDefaultSMs;
+  int64_t l2 = kDefaultL2;
 };
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
+
+// Row-kernel scratch kept per (device, stream), in two parts: an array of
+// per-sequence arrival counters, which starts at zero (cleared once when it is
+// created) and which every completed launch leaves at zero again (the last
+// cluster of each sequence resets its counter), and a data buffer for the
+// position statistics or records, which needs no clearing.  Counters sit in a
+// region of their own, so calls of any shape and kernel on one stream can
+// share it.  A call therefore needs no allocation and no clearing step.
+// Buffers are never freed while the process runs: a CUDA graph captured on a
+// stream may hold the pointers.
+struct Workspace {
+  int dev;
+  cudaStream_t stream;
+  unsigned *count;
+  int64_t count_len;
+  void *data;
+  size_t data_bytes;
+};
+std::vector<Workspace> g_ws;
+constexpr size_t kWsMinBytes = 64 * 1024;
+
+size_t grow_to(size_t need) {
+  size_t sz = kWsMinBytes;
+  while (sz < need) sz *= 2;
+  return sz;
+}
+
+// The cached scratch of (dev, stream) with room for B counters and
+// data_bytes, creating or growing it unless the stream is being captured.
+// false if none can be used (the caller then takes stream-ordered memory).
+bool cached_workspace(int dev, cudaStream_t stream, int64_t B, size_t data_bytes, unsigned **count,
+                      void **data) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  Workspace *w = nullptr;
+  for (Workspace &x : g_ws)
+    if (x.dev == dev && x.stream == stream) w = &x;
+  if (w != nullptr && w->count_len >= B && w->data_bytes >= data_bytes) {
+    *count = w->count;
+    *data = w->data;
+    return true;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return false;  // no allocation while capturing
+  if (w == nullptr) {
+    g_ws.push_back(Workspace{dev, stream, nullptr, 0, nullptr, 0});
+    w = &g_ws.back();
+  }
+  // grow a part by replacing it (the old part stays allocated: a graph may use it)
+  if (w->count_len < B) {
+    const size_t sz = grow_to((size_t)B * sizeof(unsigned));
+    void *ptr = nullptr;
+    if (cudaMalloc(&ptr, sz) != cudaSuccess || cudaMemsetAsync(ptr, 0, sz, stream) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    w->count = static_cast<unsigned *>(ptr);
+    w->count_len = (int64_t)(sz / sizeof(unsigned));
+  }
+  if (w->data_bytes < data_bytes) {
+    const size_t sz = grow_to(data_bytes);
+    void *ptr = nullptr;
+    if (cudaMalloc(&ptr, sz) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    w->data = ptr;
+    w->data_bytes = sz;
+  }
+  *count = w->count;
+  *data = w->data;
+  return true;
+}
+
 thread_local char g_last_cuda_error[256] = "";
 
 void note_cuda_error(cudaError_t e) {
@@ -43,7 +123,7 @@ void note_cuda_error(cudaError_t e) {
 
 // One-time per-device set-up: opt the kernels into 16-CTA clusters and the
 // tile kernel into its shared-memory size; read the SM count.
-specv_status ensure_device(int *sms_out) {
+specv_status ensure_device(int *sms_out, int64_t *l2_out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {
@@ -54,10 +134,11 @@ specv_status ensure_device(int *sms_out) {
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState &st = g_dev[dev];
   if (!st.ready) {
-    int major = 0, cluster_ok = 0, sms = 0;
+    int major = 0, cluster_ok = 0, sms = 0, l2 = 0;
     if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&cluster_ok, cudaDevAttrClusterLaunch, dev)) != cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess) {
       note_cuda_error(e);
       return SPECV_ERR_CUDA;
     }
@@ -70,14 +151,17 @@ specv_status ensure_device(int *sms_out) {
       return SPECV_ERR_CUDA;
     }
     st.sms = sms;
+    if (l2 > 0) st.l2 = l2;
     st.ready = true;
   }
   if (sms_out) *sms_out = st.sms;
+  if (l2_out) *l2_out = st.l2;
   return SPECV_OK;
 }
 
 struct Plan {
-  int kernel;            // 0 tile, 1 streaming row kernel, 2 resident row kernel, 3 TMA tile
+  int kernel;            // 0 tile, 1 streaming row kernel, 2 resident row kernel, 3 TMA tile,
+                         // 4 resident row kernel reading in place (speculative sampling)
   int cluster;           // CTAs per cluster (row kernels)
   int64_t ctas;          // CTAs of the row kernels (tile kernel: tiles)
   int64_t ws_bytes;      // scratch bytes
@@ -105,12 +189,13 @@ int cluster_from_env() {
   return (v == 1 || v == 2 || v == 4 || v == 8 || v == 16) ? v : 0;
 }
 
-// "stream" or "resident" forces a row-kernel variant (tuning and tests).
+// "stream", "resident" or "spec" forces a row-kernel variant (tuning and tests).
 int variant_from_env() {
   const char *s = std::getenv("SPECV_ROWS_VARIANT");
   if (!s) return 0;
   if (std::strcmp(s, "stream") == 0) return 1;
   if (std::strcmp(s, "resident") == 0) return 2;
+  if (std::strcmp(s, "spec") == 0) return 4;
   return 0;
 }
 
@@ -125,7 +210,8 @@ int variant_from_env() {
 //    96 KiB, doubled while the grid has < 4 CTAs per SM) stays within 2 CTAs
 //    per SM; otherwise the streaming row kernel runs.
 //  SPECV_CLUSTER_SIZE and SPECV_ROWS_VARIANT override the choices.
-specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, bool aligned, Plan *p) {
+specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, int64_t l2, bool aligned,
+                       Plan *p) {
   const int elem = dtype == SPECV_BF16 ? 2 : 4;
   std::memset(p, 0, sizeof(*p));
   const int64_t seq_bytes = (int64_t)(2 * K + 1) * V * elem + (int64_t)(K + 1) * 16;
@@ -164,7 +250,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, bool
   const int64_t G = (V + vw - 1) / vw;
   const int env_S = cluster_from_env();
   const int env_var = variant_from_env();
-  const bool can_resident = aligned && (row_bytes % 16 == 0) && env_var != 1;
+  const bool can_resident = aligned && (row_bytes % 16 == 0) && env_var != 1 && env_var != 4;
   auto slice_smem = [&](int S) { return 2 * ((G + S - 1) / S) * 16; };
   int S = 0;
   int kernel = 1;
@@ -186,7 +272,18 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, bool
   }
   if (kernel == 2 && P * S > INT32_MAX) kernel = 1;
   if (env_var == 2 && kernel != 2) return SPECV_ERR_UNSUPPORTED;
-  if (kernel == 1) {
+  // in-place variant: every position decides and samples at once, re-reading
+  // its own slice while it is still in L2 -- when the whole working set fits L2
+  const int64_t work_bytes = (int64_t)(2 * K + 1) * B * row_bytes;
+  const bool inplace_ok = aligned && (row_bytes % 16 == 0) && env_var != 1 && env_var != 2;
+  // (measured slower than the streaming kernel at 107 MB / 1536 CTAs: the
+  // speculative samples of every rejecting position outweigh the shorter
+  // tail, so it runs only when asked for)
+  (void)work_bytes;
+  (void)l2;
+  if (kernel == 1 && inplace_ok && env_var == 4) kernel = 4;
+  if (env_var == 4 && kernel != 4) return SPECV_ERR_UNSUPPORTED;
+  if (kernel == 1 || kernel == 4) {
     S = env_S;
     if (S == 0) {
       S = 1;
@@ -202,8 +299,8 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, bool
   p->ctas = P * S;
   p->num_groups = (int)G;
   p->groups_per_slice = (int)((G + S - 1) / S);
-  if (kernel == 2) {
-    p->res_smem = (int)slice_smem(S);
+  if (kernel == 2 || kernel == 4) {
+    p->res_smem = kernel == 2 ? (int)slice_smem(S) : 0;
     p->ws_bytes = round16(P * 8) + round16(B * 4);
   } else {
     p->ws_bytes = round16(P * 16) + round16(B * 4);
@@ -219,14 +316,15 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     return SPECV_ERR_INVALID_ARG;
   if (!sizes_ok(B, K, V, dtype, mode)) return SPECV_ERR_INVALID_ARG;
   int sms = kDefaultSMs;
-  specv_status s = ensure_device(&sms);
+  int64_t l2 = kDefaultL2;
+  specv_status s = ensure_device(&sms, &l2);
   if (s != SPECV_OK) return s;
   const int bf16 = dtype == SPECV_BF16;
   const int elem = bf16 ? 2 : 4;
   const bool aligned = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
                        ((int64_t)V * elem % 16 == 0);
   Plan p;
-  if ((s = make_plan(B, K, V, dtype, sms, aligned, &p)) != SPECV_OK) return s;
+  if ((s = make_plan(B, K, V, dtype, sms, l2, aligned, &p)) != SPECV_OK) return s;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   cudaError_t e;
   if (p.kernel == 0 || p.kernel == 3) {
@@ -263,14 +361,28 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     }
     return SPECV_OK;
   }
+  int dev = 0;
+  (void)cudaGetDevice(&dev);
+  // scratch: counters [B] then position data, from the stream's cache or,
+  // failing that, stream-ordered memory for this call (counters cleared)
+  const size_t data_bytes = (size_t)(p.ws_bytes - round16(B * 4));
+  unsigned *cnt = nullptr;
+  void *wdata = nullptr;
   void *ws = nullptr;
-  e = cudaMallocAsync(&ws, (size_t)p.ws_bytes, stream);
-  if (e != cudaSuccess) {
-    note_cuda_error(e);
-    (void)cudaGetLastError();
-    return SPECV_ERR_NO_MEMORY;
+  e = cudaSuccess;
+  const bool per_call = !cached_workspace(dev, stream, B, data_bytes, &cnt, &wdata);
+  if (per_call) {
+    e = cudaMallocAsync(&ws, (size_t)p.ws_bytes, stream);
+    if (e != cudaSuccess) {
+      note_cuda_error(e);
+      (void)cudaGetLastError();
+      return SPECV_ERR_NO_MEMORY;
+    }
+    cnt = static_cast<unsigned *>(ws);
+    wdata = static_cast<char *>(ws) + round16(B * 4);
+    e = cudaMemsetAsync(cnt, 0, (size_t)B * sizeof(unsigned), stream);
   }
-  if (p.kernel == 2) {
+  if (p.kernel == 2 || p.kernel == 4) {
     specv::ResArgs r;
     r.target = target;
     r.draft = draft;
@@ -283,16 +395,16 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     r.V = V;
     r.out_tokens = out_tokens;
     r.out_n = out_n;
-    r.rec = static_cast<int2 *>(ws);
-    r.count = reinterpret_cast<unsigned *>(static_cast<char *>(ws) + round16(B * (K + 1) * 8));
+    r.rec = static_cast<int2 *>(wdata);
+    r.count = cnt;
     r.dbg_ptilde = dbg_ptilde;
     r.dbg_q = dbg_q;
     r.dbg_lse = dbg_lse;
     r.groups_per_slice = p.groups_per_slice;
     r.num_groups = p.num_groups;
-    e = cudaMemsetAsync(r.count, 0, (size_t)B * sizeof(unsigned), stream);
     if (e == cudaSuccess)
-      e = specv::resident_launch(r, bf16, mode, p.cluster, p.ctas, p.res_smem, stream);
+      e = specv::resident_launch(r, bf16, mode, p.kernel == 2, p.cluster, p.ctas, p.res_smem,
+                                 stream);
   } else {
     specv::RowArgs a;
     a.target = target;
@@ -306,18 +418,19 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     a.V = V;
     a.out_tokens = out_tokens;
     a.out_n = out_n;
-    a.ws_stats = static_cast<float4 *>(ws);
-    a.ws_count = reinterpret_cast<unsigned *>(static_cast<char *>(ws) + round16(B * (K + 1) * 16));
+    a.ws_stats = static_cast<float4 *>(wdata);
+    a.ws_count = cnt;
     a.dbg_ptilde = dbg_ptilde;
     a.dbg_q = dbg_q;
     a.dbg_lse = dbg_lse;
     a.groups_per_slice = p.groups_per_slice;
     a.num_groups = p.num_groups;
-    e = cudaMemsetAsync(a.ws_count, 0, (size_t)B * sizeof(unsigned), stream);
     if (e == cudaSuccess) e = specv::rows_launch(a, bf16, mode, aligned, p.cluster, p.ctas, stream);
   }
-  const cudaError_t ef = cudaFreeAsync(ws, stream);
-  if (e == cudaSuccess) e = ef;
+  if (per_call) {
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = ef;
+  }
   if (e != cudaSuccess) {
     note_cuda_error(e);
     return SPECV_ERR_CUDA;
@@ -355,16 +468,19 @@ specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, spec
                         int64_t *workspace_bytes) {
   if (!sizes_ok(B, K, V, dtype, mode)) return SPECV_ERR_INVALID_ARG;
   int sms = kDefaultSMs;
+  int64_t l2 = kDefaultL2;
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) {
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
       sms = v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) == cudaSuccess && v > 0) l2 = v;
+    (void)cudaGetLastError();
   } else {
     (void)cudaGetLastError();
   }
   Plan p;
-  specv_status s = make_plan(B, K, V, dtype, sms, true, &p);
+  specv_status s = make_plan(B, K, V, dtype, sms, l2, true, &p);
   if (s != SPECV_OK) return s;
   if (kernel) *kernel = p.kernel;
   if (cluster) *cluster = p.cluster;

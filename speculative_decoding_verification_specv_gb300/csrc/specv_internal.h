@@ -83,8 +83,10 @@ struct ResArgs {
 };
 
 cudaError_t resident_prepare(int max_smem);
-cudaError_t resident_launch(const ResArgs &a, int dtype_bf16, int mode, int S, int64_t grid,
-                            int smem, cudaStream_t stream);
+// staged = true: slices staged in shared memory by TMA; false: read in place
+// from global memory (the sampler re-reads the slice, from L2 when it fits).
+cudaError_t resident_launch(const ResArgs &a, int dtype_bf16, int mode, bool staged, int S,
+                            int64_t grid, int smem, cudaStream_t stream);
 
 cudaError_t rows_prepare();
 cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,

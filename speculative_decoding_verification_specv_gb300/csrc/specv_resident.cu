@@ -44,8 +44,12 @@ constexpr int kMaxChunks = kResidentMaxChunks;
 // status of a position record
 enum : int { kRecAccepted = 1, kRecRejected = 0, kRecBonus = 2, kRecInvalid = -1, kRecError = -2 };
 
+constexpr int kNW = kNT / 32;
+
 struct __align__(16) ResShared {
   BlockScratch<kNT> bs;
+  float wmass[kNW];          // sampler weight mass of each warp's chunk
+  int found;
   float4 part[kMaxCluster];  // CTA partial statistics, indexed by source rank
   int perr[kMaxCluster];     // CTA copy-timeout flags, indexed by source rank
   float masses[2][kMaxCluster];
@@ -55,8 +59,22 @@ struct __align__(16) ResShared {
   int last;
 };
 
-// Online (max, sum-exp) over this thread's groups of one staged chunk.
-template <typename T, int MODE>
+// 16-byte group loads: from shared memory (staged slices) or from global
+// memory (the streaming variant; statistics pass without L1 allocation, the
+// sampler's second read through the read-only path, usually an L2 hit).
+template <bool STAGED>
+__device__ __forceinline__ uint4 ld_group(const uint4 *p) {
+  if constexpr (STAGED) return *p;
+  else return __ldg(p);
+}
+template <bool STAGED>
+__device__ __forceinline__ uint4 ld_group_stream(const uint4 *p) {
+  if constexpr (STAGED) return *p;
+  else return ld_stream16(p);
+}
+
+// Online (max, sum-exp) over this thread's groups of one chunk of the slice.
+template <typename T, int MODE, bool STAGED>
 __device__ __forceinline__ void chunk_stats(const uint4 *cA, const uint4 *cB, int cnt, bool pair,
                                             float lam, float &mA, float &sA, float &mB, float &sB) {
   constexpr int VW = Elem<T>::kPerVec;
@@ -69,8 +87,8 @@ __device__ __forceinline__ void chunk_stats(const uint4 *cA, const uint4 *cB, in
       const int g = g0 + u * kNT;
       ok[u] = g < cnt;
       if (ok[u]) {
-        za[u] = cA[g];
-        if (pair) zb[u] = cB[g];
+        za[u] = ld_group_stream<STAGED>(cA + g);
+        if (pair) zb[u] = ld_group_stream<STAGED>(cB + g);
       }
     }
     auto a_val = [&](int u, int e) -> float {
@@ -108,73 +126,119 @@ __device__ __forceinline__ void chunk_stats(const uint4 *cA, const uint4 *cB, in
   }
 }
 
-// Sampler weight mass of the staged slice (strided over threads, fixed-order
-// block sum).
-template <typename T, int MODE>
-__device__ float staged_mass(BlockScratch<kNT> &bs, const uint4 *bA, const uint4 *bB, int ng,
-                             int kind, const SampleParams &sp) {
+// Sampler weights of the slice, by warp chunks: warp w owns the contiguous
+// groups [w*Cw, (w+1)*Cw) and its lanes stride through them.  Each warp's
+// mass goes to wmass[w] (fixed-order butterfly); the CTA mass is their sum in
+// warp order, so the search below routes by exactly these numbers.
+template <typename T, int MODE, bool STAGED>
+__device__ float chunk_masses(ResShared &sh, const uint4 *bA, const uint4 *bB, int ng, int kind,
+                              const SampleParams &sp) {
   constexpr int VW = Elem<T>::kPerVec;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int Cw = (ng + kNW - 1) / kNW;
+  const int lo = warp * Cw, hi = min(ng, lo + Cw);
   float acc = 0.0f;
-  for (int g = threadIdx.x; g < ng; g += kNT) {
-    const uint4 za = bA[g];
-    const uint4 zb = kind != kWBonus ? bB[g] : za;
+  for (int g = lo + lane; g < hi; g += 32) {
+    const uint4 za = ld_group<STAGED>(bA + g);
+    const uint4 zb = kind != kWBonus ? ld_group<STAGED>(bB + g) : za;
 #pragma unroll
     for (int e = 0; e < VW; ++e)
       acc = __fadd_rn(acc, sample_weight(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e)));
   }
-  return block_sum<kNT>(bs, acc);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+  if (lane == 0) sh.wmass[warp] = acc;
+  __syncthreads();
+  float m = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kNW; ++w) m = __fadd_rn(m, sh.wmass[w]);
+  return m;
 }
 
-// Index-order search of the staged slice for the first entry whose running
-// weight sum exceeds t: tiles of kNT groups (one per thread), a block scan
-// routes t to one thread, that thread walks its entries.  Returns the slice-
-// local element index; if round-off leaves no crossing, the largest index
-// with positive weight (-1 if none).
-template <typename T, int MODE>
-__device__ int staged_search(BlockScratch<kNT> &bs, const uint4 *bA, const uint4 *bB, int ng,
-                             int kind, const SampleParams &sp, float t) {
+// Index-order search of the slice for the first entry whose running weight
+// sum exceeds t, using the warp masses of chunk_masses: the warp whose range
+// holds t walks it in tiles of 32 groups with warp scans (no CTA barriers
+// inside).  Returns the slice-local element index; if round-off leaves no
+// crossing, the last entry with positive weight of the routed warp's range
+// (-1 if none).  Call after chunk_masses, with the same kind and parameters.
+template <typename T, int MODE, bool STAGED>
+__device__ int chunk_search(ResShared &sh, const uint4 *bA, const uint4 *bB, int ng, int kind,
+                            const SampleParams &sp, float t) {
   constexpr int VW = Elem<T>::kPerVec;
-  float base = 0.0f;
-  int lastpos = -1;
-  if (threadIdx.x == 0) bs.found = -1;
-  for (int tb = 0; tb < ng; tb += kNT) {
-    const int g = tb + (int)threadIdx.x;
-    float w[VW];
-    float s = 0.0f;
-    if (g < ng) {
-      const uint4 za = bA[g];
-      const uint4 zb = kind != kWBonus ? bB[g] : za;
-#pragma unroll
-      for (int e = 0; e < VW; ++e) {
-        w[e] = sample_weight(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e));
-        s = __fadd_rn(s, w[e]);
-        if (w[e] > 0.0f) lastpos = g * VW + e;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < VW; ++e) w[e] = 0.0f;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int Cw = (ng + kNW - 1) / kNW;
+  // route: the first warp whose cumulative mass exceeds t, else the last with mass
+  int wstar = -1, wlast = -1;
+  float base = 0.0f, wbase = 0.0f, tw = t;
+  for (int w = 0; w < kNW; ++w) {
+    const float nb = __fadd_rn(base, sh.wmass[w]);
+    if (sh.wmass[w] > 0.0f) wlast = w;
+    if (wstar < 0 && nb > t) {
+      wstar = w;
+      wbase = base;
     }
-    float excl, incl, total;
-    block_scan<kNT>(bs, s, excl, incl, total);
-    const float lo = __fadd_rn(base, excl), hi = __fadd_rn(base, incl);
-    if (lo <= t && t < hi) {  // the intervals partition [base, base + total): one thread
-      float c = lo;
-      int pick = -1, lastg = -1;
-#pragma unroll
-      for (int e = 0; e < VW; ++e) {
-        c = __fadd_rn(c, w[e]);
-        if (w[e] > 0.0f) lastg = g * VW + e;
-        if (pick < 0 && c > t) pick = g * VW + e;
-      }
-      bs.found = pick >= 0 ? pick : lastg;
-    }
-    __syncthreads();
-    const int f = bs.found;
-    __syncthreads();
-    if (f >= 0) return f;
-    base = __fadd_rn(base, total);
+    base = nb;
   }
-  return block_max_index<kNT>(bs, lastpos);
+  if (wstar < 0) {
+    wstar = wlast;
+    tw = INFINITY;
+  }
+  if (threadIdx.x == 0) sh.found = -1;
+  __syncthreads();
+  if (warp == wstar) {
+    const int lo = warp * Cw, hi = min(ng, lo + Cw);
+    float run = wbase;
+    int lastpos = -1, res = -1;
+    for (int g0 = lo; g0 < hi && res < 0; g0 += 32) {
+      const int g = g0 + lane;
+      float w[VW];
+      float gs = 0.0f;
+      if (g < hi) {
+        const uint4 za = ld_group<STAGED>(bA + g);
+        const uint4 zb = kind != kWBonus ? ld_group<STAGED>(bB + g) : za;
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          w[e] = sample_weight(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e));
+          gs = __fadd_rn(gs, w[e]);
+          if (w[e] > 0.0f) lastpos = g * VW + e;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) w[e] = 0.0f;
+      }
+      float incl = gs;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl = __fadd_rn(incl, y);
+      }
+      float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) excl = 0.0f;
+      const float lo_v = __fadd_rn(run, excl), hi_v = __fadd_rn(run, incl);
+      const bool own = g < hi && lo_v <= tw && tw < hi_v;  // at most one lane
+      int pick = -1;
+      if (own) {
+        float c = lo_v;
+        int lastg = -1;
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          c = __fadd_rn(c, w[e]);
+          if (w[e] > 0.0f) lastg = g * VW + e;
+          if (pick < 0 && c > tw) pick = g * VW + e;
+        }
+        if (pick < 0) pick = lastg;
+      }
+      const unsigned owner = __ballot_sync(0xffffffffu, own);
+      const int picked = __shfl_sync(0xffffffffu, pick, owner ? __ffs(owner) - 1 : 0);
+      if (owner) res = picked;
+      run = __fadd_rn(run, __shfl_sync(0xffffffffu, incl, 31));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, off));
+    if (lane == 0) sh.found = res >= 0 ? res : lastpos;
+  }
+  __syncthreads();
+  return sh.found;
 }
 
 // The last cluster of sequence b: first rejection over the position records,
@@ -205,7 +269,7 @@ __device__ void finalize_sequence(const ResArgs &a, int64_t b) {
   if (lane == 0) a.out_n[b] = n;
 }
 
-template <typename T, int MODE>
+template <typename T, int MODE, bool STAGED>
 __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
   constexpr int VW = Elem<T>::kPerVec;
   extern __shared__ __align__(128) unsigned char dsm[];
@@ -222,25 +286,46 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
   const T *rowB = static_cast<const T *>(a.draft) + (b * K + (pair ? i : 0)) * (int64_t)a.V;
   const int g_lo = rank * a.groups_per_slice;
   const int ng = max(0, min(a.num_groups, g_lo + a.groups_per_slice) - g_lo);
-  uint4 *bA = reinterpret_cast<uint4 *>(dsm);
-  uint4 *bB = bA + a.groups_per_slice;
+  // the slice: staged in shared memory, or read in place from global memory
+  const uint4 *gA = reinterpret_cast<const uint4 *>(rowA + (int64_t)g_lo * VW);
+  const uint4 *gB = reinterpret_cast<const uint4 *>(rowB + (int64_t)g_lo * VW);
+  uint4 *stA = reinterpret_cast<uint4 *>(dsm);
+  uint4 *stB = stA + a.groups_per_slice;
+  const uint4 *bA = STAGED ? stA : gA;
+  const uint4 *bB = STAGED ? stB : gB;
   const int nch = (ng + kChunkGroups - 1) / kChunkGroups;
   const float lam = a.lam[b];
 
-  // ---------------------------------------------------------------- staging
-  if (threadIdx.x == 0) {
-    for (int c = 0; c < nch; ++c) mbar_init(&sh.bar[c], 1);
-    mbar_fence_init();
+  // decision inputs, loaded now so their latency overlaps the statistics pass
+  int x = 0;
+  float u_acc = 0.0f, zt_x = 0.0f, zq_x = 0.0f;
+  bool tok_ok = true;
+  if (threadIdx.x == 0 && pair) {
+    x = a.tokens[b * K + i];
+    u_acc = a.u_accept[b * K + i];
+    tok_ok = x >= 0 && x < a.V;
+    if (tok_ok) {
+      zt_x = Elem<T>::load(rowA + x);
+      zq_x = Elem<T>::load(rowB + x);
+    }
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int c = 0; c < nch; ++c) {
-      const int g0 = c * kChunkGroups;
-      const int cnt = min(kChunkGroups, ng - g0);
-      const uint32_t bytes = (uint32_t)cnt * 16u;
-      mbar_arrive_expect_tx(&sh.bar[c], pair ? 2u * bytes : bytes);
-      tma_load_1d(bA + g0, rowA + (int64_t)(g_lo + g0) * VW, bytes, &sh.bar[c]);
-      if (pair) tma_load_1d(bB + g0, rowB + (int64_t)(g_lo + g0) * VW, bytes, &sh.bar[c]);
+
+  // ---------------------------------------------------------------- staging
+  if constexpr (STAGED) {
+    if (threadIdx.x == 0) {
+      for (int c = 0; c < nch; ++c) mbar_init(&sh.bar[c], 1);
+      mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int c = 0; c < nch; ++c) {
+        const int g0 = c * kChunkGroups;
+        const int cnt = min(kChunkGroups, ng - g0);
+        const uint32_t bytes = (uint32_t)cnt * 16u;
+        mbar_arrive_expect_tx(&sh.bar[c], pair ? 2u * bytes : bytes);
+        tma_load_1d(stA + g0, gA + g0, bytes, &sh.bar[c]);
+        if (pair) tma_load_1d(stB + g0, gB + g0, bytes, &sh.bar[c]);
+      }
     }
   }
 
@@ -248,9 +333,12 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
   float mA = -INFINITY, sA = 0.0f, mB = -INFINITY, sB = 0.0f;
   int err = 0;
   for (int c = 0; c < nch; ++c) {
-    if (!mbar_wait(&sh.bar[c], 0)) err = 1;
+    if constexpr (STAGED) {
+      if (!mbar_wait(&sh.bar[c], 0)) err = 1;
+    }
     const int g0 = c * kChunkGroups;
-    chunk_stats<T, MODE>(bA + g0, bB + g0, min(kChunkGroups, ng - g0), pair, lam, mA, sA, mB, sB);
+    chunk_stats<T, MODE, STAGED>(bA + g0, bB + g0, min(kChunkGroups, ng - g0), pair, lam, mA, sA,
+                                 mB, sB);
   }
   err = __syncthreads_or(err);
   block_merge_stats<kNT>(sh.bs, mA, sA, mB, sB);
@@ -281,25 +369,20 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
     } else if (!pair) {
       status = kRecBonus;
       kind = kWBonus;
+    } else if (!tok_ok) {
+      status = kRecInvalid;
     } else {
-      const int x = a.tokens[b * K + i];
-      if (x < 0 || x >= a.V) {
-        status = kRecInvalid;
-      } else {
-        const float zt_x = Elem<T>::load(rowA + x);
-        const float zq_x = Elem<T>::load(rowB + x);
-        float px = 0.0f, qx = 0.0f;
-        const PosStats st{m0, s0, m1, s1};
-        const float ratio =
-            accept_ratio(MODE, st, zt_x, zq_x, lam, (rank == 0 && a.dbg_ptilde) ? &px : nullptr, &qx);
-        const bool acc = accept_test(a.u_accept[b * K + i], ratio);
-        if (rank == 0 && a.dbg_ptilde) {
-          a.dbg_ptilde[b * K + i] = px;
-          a.dbg_q[b * K + i] = qx;
-        }
-        status = acc ? kRecAccepted : kRecRejected;
-        if (!acc) kind = (MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual;
+      float px = 0.0f, qx = 0.0f;
+      const PosStats st{m0, s0, m1, s1};
+      const float ratio =
+          accept_ratio(MODE, st, zt_x, zq_x, lam, (rank == 0 && a.dbg_ptilde) ? &px : nullptr, &qx);
+      const bool acc = accept_test(u_acc, ratio);
+      if (rank == 0 && a.dbg_ptilde) {
+        a.dbg_ptilde[b * K + i] = px;
+        a.dbg_q[b * K + i] = qx;
       }
+      status = acc ? kRecAccepted : kRecRejected;
+      if (!acc) kind = (MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual;
     }
     if (rank == 0 && a.dbg_lse) {
       a.dbg_lse[p * 2 + 0] = m0 + lg2(s0) * kLn2;
@@ -313,20 +396,15 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
   const int status = sh.status;
   int kind = sh.kind;
 
-  // ---------------------------------------------- sampling from shared memory
+  // ------------------------------------- sampling (rejecting / bonus positions)
   int publisher = 0;  // rank that publishes the record
   int token = -1;
   if (kind >= 0) {
-    SampleParams sp;
-    sp.mA = m0;
-    sp.invSA = __fdiv_rn(1.0f, s0);
-    sp.mB = m1;
-    sp.invSB = __fdiv_rn(1.0f, s1);
-    sp.lam = lam;
+    const SampleParams sp = make_sample_params(m0, s0, m1, s1, lam);
     float R = 0.0f;
     int attempt = 0;
     for (;; ++attempt) {
-      const float mass = staged_mass<T, MODE>(sh.bs, bA, bB, ng, kind, sp);
+      const float mass = chunk_masses<T, MODE, STAGED>(sh, bA, bB, ng, kind, sp);
       if (threadIdx.x == 0)
         for (int r = 0; r < S; ++r) cluster.map_shared_rank(sh.masses[attempt], r)[rank] = mass;
       cluster.sync();  // all slice masses exchanged
@@ -358,7 +436,7 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
       }
       publisher = rstar;
       if (rank == rstar) {
-        const int local = staged_search<T, MODE>(sh.bs, bA, bB, ng, kind, sp, tloc);
+        const int local = chunk_search<T, MODE, STAGED>(sh, bA, bB, ng, kind, sp, tloc);
         token = local >= 0 ? g_lo * VW + local : -1;
       }
     }
@@ -372,6 +450,7 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
     const unsigned prev = atomicAdd(&a.count[b], 1u);
     if (prev == (unsigned)K) {
       __threadfence();
+      a.count[b] = 0;  // every position has arrived: leave the counter zero for the next call
       sh.last = 1;
     }
   }
@@ -379,12 +458,12 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
   if (sh.last && threadIdx.x < 32) finalize_sequence(a, b);
 }
 
-template <typename T, int MODE>
+template <typename T, int MODE, bool STAGED>
 cudaError_t launch_one(const ResArgs &a, int S, int64_t grid, int smem, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kNT, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.dynamicSmemBytes = STAGED ? (size_t)smem : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -393,36 +472,50 @@ cudaError_t launch_one(const ResArgs &a, int S, int64_t grid, int smem, cudaStre
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, resident_kernel<T, MODE>, a);
+  return cudaLaunchKernelEx(&cfg, resident_kernel<T, MODE, STAGED>, a);
+}
+
+template <typename T, int MODE, bool STAGED>
+cudaError_t prepare_one(int max_smem) {
+  cudaError_t e = cudaFuncSetAttribute(resident_kernel<T, MODE, STAGED>,
+                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess || !STAGED) return e;
+  return cudaFuncSetAttribute(resident_kernel<T, MODE, STAGED>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
 }
 
 template <typename T, int MODE>
-cudaError_t prepare_one(int max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(resident_kernel<T, MODE>,
-                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(resident_kernel<T, MODE>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+cudaError_t launch_variant(const ResArgs &a, bool staged, int S, int64_t grid, int smem,
+                           cudaStream_t stream) {
+  return staged ? launch_one<T, MODE, true>(a, S, grid, smem, stream)
+                : launch_one<T, MODE, false>(a, S, grid, smem, stream);
 }
 
 }  // namespace
 
 cudaError_t resident_prepare(int max_smem) {
   cudaError_t e = cudaSuccess, r;
-  if ((r = prepare_one<float, kProbMix>(max_smem)) != cudaSuccess) e = r;
-  if ((r = prepare_one<float, kLogitMix>(max_smem)) != cudaSuccess) e = r;
-  if ((r = prepare_one<uint16_t, kProbMix>(max_smem)) != cudaSuccess) e = r;
-  if ((r = prepare_one<uint16_t, kLogitMix>(max_smem)) != cudaSuccess) e = r;
+#define SPECV_PREP(T, M, ST) \
+  if ((r = prepare_one<T, M, ST>(max_smem)) != cudaSuccess) e = r;
+  SPECV_PREP(float, kProbMix, true)
+  SPECV_PREP(float, kLogitMix, true)
+  SPECV_PREP(uint16_t, kProbMix, true)
+  SPECV_PREP(uint16_t, kLogitMix, true)
+  SPECV_PREP(float, kProbMix, false)
+  SPECV_PREP(float, kLogitMix, false)
+  SPECV_PREP(uint16_t, kProbMix, false)
+  SPECV_PREP(uint16_t, kLogitMix, false)
+#undef SPECV_PREP
   return e;
 }
 
-cudaError_t resident_launch(const ResArgs &a, int dtype_bf16, int mode, int S, int64_t grid,
-                            int smem, cudaStream_t stream) {
+cudaError_t resident_launch(const ResArgs &a, int dtype_bf16, int mode, bool staged, int S,
+                            int64_t grid, int smem, cudaStream_t stream) {
   if (dtype_bf16)
-    return mode == kProbMix ? launch_one<uint16_t, kProbMix>(a, S, grid, smem, stream)
-                            : launch_one<uint16_t, kLogitMix>(a, S, grid, smem, stream);
-  return mode == kProbMix ? launch_one<float, kProbMix>(a, S, grid, smem, stream)
-                          : launch_one<float, kLogitMix>(a, S, grid, smem, stream);
+    return mode == kProbMix ? launch_variant<uint16_t, kProbMix>(a, staged, S, grid, smem, stream)
+                            : launch_variant<uint16_t, kLogitMix>(a, staged, S, grid, smem, stream);
+  return mode == kProbMix ? launch_variant<float, kProbMix>(a, staged, S, grid, smem, stream)
+                          : launch_variant<float, kLogitMix>(a, staged, S, grid, smem, stream);
 }
 
 }  // namespace specv

@@ -273,7 +273,10 @@ __global__ void __launch_bounds__(kNT) rows_kernel(RowArgs a) {
     __threadfence();
     const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
     const int last = prev == (unsigned)K;
-    if (last) __threadfence();
+    if (last) {
+      __threadfence();
+      a.ws_count[b] = 0;  // every position has arrived: leave the counter zero for the next call
+    }
     for (int r = 0; r < S; ++r) *cluster.map_shared_rank(&sh.last, r) = last;
   }
   cluster.sync();  // sh.last is set in every rank; rank 0 is done reading partials

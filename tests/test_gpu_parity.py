@@ -105,7 +105,7 @@ def test_parity_full_size_exactness_workload(specv, mode):
 
 
 @pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
-@pytest.mark.parametrize("variant", ["stream", "resident"])
+@pytest.mark.parametrize("variant", ["stream", "resident", "spec"])
 def test_every_cluster_size(specv, cluster_env, variant, S):
     os.environ["SPECV_CLUSTER_SIZE"] = str(S)
     os.environ["SPECV_ROWS_VARIANT"] = variant
@@ -129,12 +129,14 @@ def test_every_cluster_size(specv, cluster_env, variant, S):
 
 @pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
 @pytest.mark.parametrize("cfg", [2, 3, 4])
-def test_streaming_variant_on_workloads(specv, cluster_env, cfg, mode):
-    os.environ["SPECV_ROWS_VARIANT"] = "stream"
+@pytest.mark.parametrize("variant", ["stream", "spec"])
+def test_row_variants_on_workloads(specv, cluster_env, variant, cfg, mode):
+    os.environ["SPECV_ROWS_VARIANT"] = variant
     w = SMALL[cfg]
     x = workloads.make_inputs(w, DEV)
+    assert specv.plan(w.B, w.K, w.V, 1 if w.dtype == "bf16" else 0)["kernel"] == "rows-" + variant
     rep, _, _ = _check(specv, x, mode)
-    print(f"streaming variant, workload {cfg}: {rep}")
+    print(f"{variant} variant, workload {cfg}: {rep}")
 
 
 RAGGED = [
@@ -249,3 +251,49 @@ def test_binding_rejects_bad_tensors(specv):
         cpu = {k: v.cpu() for k, v in x.items()}
         specv.verify(cpu["target_logits"], cpu["draft_logits"], cpu["draft_tokens"],
                      cpu["u_accept"], cpu["u_resample"], cpu["lam"])
+
+
+def test_streams_and_graph_capture_share_nothing_wrongly(specv):
+    """Per-stream scratch: concurrent calls on two streams, a graph captured on
+    a stream that already has scratch, and one captured on a fresh stream
+    (stream-ordered scratch inside the graph) all give the eager results."""
+    w = workloads.WORKLOADS[3].scaled(B=6)
+    xs = [workloads.make_inputs(w, DEV, seed_offset=k) for k in range(2)]
+    ref = []
+    for x in xs:
+        t, n = specv.verify(x["target_logits"], x["draft_logits"], x["draft_tokens"],
+                            x["u_accept"], x["u_resample"], x["lam"])
+        ref.append((t.clone(), n.clone()))
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for k, s in enumerate((s1, s2)):
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            x = xs[k]
+            outs.append(specv.verify(x["target_logits"], x["draft_logits"], x["draft_tokens"],
+                                     x["u_accept"], x["u_resample"], x["lam"], stream=s))
+    torch.cuda.synchronize()
+    for (t, n), (rt, rn) in zip(outs, ref):
+        assert torch.equal(t, rt) and torch.equal(n, rn)
+    for warm in (True, False):
+        x = xs[0]
+        tok = torch.empty_like(ref[0][0])
+        nn = torch.empty_like(ref[0][1])
+        s = torch.cuda.Stream()
+        if warm:  # the stream gets its scratch before the capture
+            with torch.cuda.stream(s):
+                specv.verify(x["target_logits"], x["draft_logits"], x["draft_tokens"],
+                             x["u_accept"], x["u_resample"], x["lam"], out_tokens=tok,
+                             out_n_accepted=nn, stream=s)
+            s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            specv.verify(x["target_logits"], x["draft_logits"], x["draft_tokens"], x["u_accept"],
+                         x["u_resample"], x["lam"], out_tokens=tok, out_n_accepted=nn,
+                         stream=torch.cuda.current_stream())
+        for _ in range(3):
+            tok.fill_(-9)
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(tok, ref[0][0]) and torch.equal(nn, ref[0][1])
