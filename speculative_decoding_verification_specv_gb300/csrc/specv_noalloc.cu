@@ -6,8 +6,9 @@
 // would synchronise or fail (inside a latency-critical decode loop, or under
 // a memory budget that is already fully committed), and callers that must
 // guarantee the call never returns an out-of-memory error.  specv_verify
-// takes its small scratch workspace from the stream-ordered allocator on
-// every call; specv_verify_noalloc instead uses a fixed scratch array that is
+// allocates its small scratch workspace itself (once per stream, or per call
+// while a graph is being captured); specv_verify_noalloc instead uses a fixed
+// scratch array that is
 // part of the library's device image (a file-scope __device__ array, created
 // when the library's device code is loaded on a GPU and kept until the
 // process exits).
