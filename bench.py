@@ -69,6 +69,29 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, ws, device):
+    """The largest value of x over all ranks (the slowest rank's time); x on one
+    rank is returned unchanged."""
+    if ws == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(rows_per_step, steps, ws, slowest_ms):
+    """Whole-job rows/s: every rank verifies rows_per_step rows per step (weak
+    scaling), all ranks' rows over the slowest rank's time."""
+    return rows_per_step * steps * ws / (slowest_ms / 1e3)
+
+
+# kernel function timed for the roofline, by the planner's kernel name
+PLAN_KERNEL_FUNCTION = {"tile": "tile_kernel", "rows-stream": "rows_kernel",
+                        "rows-resident": "resident_kernel", "tile-tma": "tile_tma_kernel",
+                        "rows-spec": "resident_kernel"}
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -324,13 +347,9 @@ def main():
     per_call_ms = [a.elapsed_time(b) for a, b in ev]
     if flush_buf is not None:  # the timed region holds the flushes: count the steps only
         total_ms = sum(per_call_ms)
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, ws, dev)
     rows_per_step = w.B * w.K
-    value = rows_per_step * K * ws / (total_ms / 1e3)
+    value = job_throughput(rows_per_step, K, ws, total_ms)
     mean_accepted = float(out_n.float().mean().item())
 
     # end to end: pinned host inputs -> device, verify, result -> host, every step
@@ -367,13 +386,8 @@ def main():
         b.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-        e_ms = a.elapsed_time(b)
-        if ws > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": rows_per_step * e_steps * ws / (e_ms / 1e3), "unit": UNIT,
+        e_ms = max_over_ranks(a.elapsed_time(b), ws, dev)
+        e2e = {"value": job_throughput(rows_per_step, e_steps, ws, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
                "ms_per_step": e_ms / e_steps}
         del dev_in, host
@@ -395,7 +409,7 @@ def main():
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
                 "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                "kernel": "rows_kernel" if plan["kernel"] == "rows" else "tile_kernel",
+                "kernel": PLAN_KERNEL_FUNCTION.get(plan["kernel"], plan["kernel"]),
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "launch_ms_mean": kern_ms, "launch_ms_min": min(per_call_ms),
                 "timing": ("CUDA events around each replay of a CUDA graph holding one "

@@ -131,10 +131,16 @@ specv_status specv_verify_debug(const void *target_logits, const void *draft_log
  *            memory by TMA; chosen when rows start on 16-byte boundaries and
  *            a slice fits shared memory, and the grid is a single wave),
  *            3 = small-vocabulary tile kernel with TMA-staged, double-buffered
- *            tiles (16-byte aligned rows)
+ *            tiles (16-byte aligned rows),
+ *            4 = resident cluster row kernel that samples the rejected row
+ *            speculatively in place (only when the environment variable
+ *            SPECV_ROWS_VARIANT=spec asks for it; =stream and =resident force
+ *            kernels 1 and 2, and SPECV_CLUSTER_SIZE=1..16 (a power of two)
+ *            forces the cluster size of the row kernels)
  *   cluster: CTAs per thread-block cluster splitting each row (1 for kernel 0)
  *   ctas:    CTAs launched by a row kernel; tiles of sequences for kernels 0, 3
- *   workspace_bytes: scratch bytes allocated per call
+ *   workspace_bytes: scratch bytes of the row kernels' workspace (kept per
+ *            device and stream, see specv_verify)
  * Returns SPECV_ERR_INVALID_ARG for sizes specv_verify would reject.
  */
 specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,

@@ -189,6 +189,10 @@ def verify_debug(target_logits, draft_logits, draft_tokens, u_accept, u_resample
     return dict(tokens=out_tokens, n_accepted=out_n, ptilde_x=px, q_x=qx, lse=lse)
 
 
+# specv_plan's kernel codes
+KERNEL_NAMES = {0: "tile", 1: "rows-stream", 2: "rows-resident", 3: "tile-tma", 4: "rows-spec"}
+
+
 def plan(B: int, K: int, V: int, dtype: int = F32, mode: int = PROB_MIX) -> dict:
     """The launch specv_verify would make (host-only query)."""
     kern, clus = ctypes.c_int32(0), ctypes.c_int32(0)
@@ -196,8 +200,7 @@ def plan(B: int, K: int, V: int, dtype: int = F32, mode: int = PROB_MIX) -> dict
     st = load().specv_plan(int(B), int(K), int(V), int(dtype), int(mode), ctypes.byref(kern),
                            ctypes.byref(clus), ctypes.byref(ctas), ctypes.byref(ws))
     _check(st, "specv_plan")
-    names = {0: "tile", 1: "rows-stream", 2: "rows-resident", 3: "tile-tma", 4: "rows-spec"}
-    return dict(kernel=names.get(kern.value, str(kern.value)), cluster=clus.value,
+    return dict(kernel=KERNEL_NAMES.get(kern.value, str(kern.value)), cluster=clus.value,
                 ctas=ctas.value, workspace_bytes=ws.value)
 
 
