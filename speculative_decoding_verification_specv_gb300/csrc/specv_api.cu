@@ -168,6 +168,7 @@ struct Plan {
   int tile_seqs;
   int smem_t, smem_d, smem_total;
   int groups_per_slice, num_groups;
+  int seg_tiles, segs_per_slice;  // sampler segments of the streaming row kernel
   int res_smem;          // dynamic shared memory of the resident kernel
 };
 
@@ -303,7 +304,9 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, int6
     p->res_smem = kernel == 2 ? (int)slice_smem(S) : 0;
     p->ws_bytes = round16(P * 8) + round16(B * 4);
   } else {
-    p->ws_bytes = round16(P * 16) + round16(B * 4);
+    // position statistics, then the bonus rows' segment statistics
+    specv::rows_segments(p->groups_per_slice, &p->seg_tiles, &p->segs_per_slice);
+    p->ws_bytes = round16(P * 16) + round16(B * S * (int64_t)p->segs_per_slice * 8) + round16(B * 4);
   }
   return SPECV_OK;
 }
@@ -425,6 +428,9 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     a.dbg_lse = dbg_lse;
     a.groups_per_slice = p.groups_per_slice;
     a.num_groups = p.num_groups;
+    a.seg_tiles = p.seg_tiles;
+    a.segs_per_slice = p.segs_per_slice;
+    a.ws_seg = reinterpret_cast<float2 *>(static_cast<char *>(wdata) + round16(B * (K + 1) * 16));
     if (e == cudaSuccess) e = specv::rows_launch(a, bf16, mode, aligned, p.cluster, p.ctas, stream);
   }
   if (per_call) {

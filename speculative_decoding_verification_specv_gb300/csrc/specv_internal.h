@@ -14,6 +14,23 @@ constexpr int kTmaTileMaxSeqs = kTileThreads / kTmaTileLanes;  // sequences per 
 constexpr int kResidentChunkGroups = 1024;  // 16-byte groups per TMA chunk (16 KiB per row)
 constexpr int kResidentMaxChunks = 8;       // chunks per row slice (128 KiB per row at most)
 
+// Sampler segments of the streaming row kernel.  A CTA's slice of a row is cut
+// into segments of seg_tiles * kSegGroups consecutive 16-byte groups (the last
+// one may be short), at most kMaxSegs per slice; a warp reads a tile of
+// kSegGroups groups as kSegLaneGroups coalesced 16-byte loads per lane.
+constexpr int kSegLaneGroups = 4;
+constexpr int kSegGroups = 32 * kSegLaneGroups;
+constexpr int kMaxSegs = 512;
+
+// Segment geometry of a slice of groups_per_slice groups.
+inline void rows_segments(int groups_per_slice, int *seg_tiles, int *segs_per_slice) {
+  const int64_t tiles = ((int64_t)groups_per_slice + kSegGroups - 1) / kSegGroups;
+  const int64_t per_seg = (tiles + kMaxSegs - 1) / kMaxSegs;
+  *seg_tiles = (int)(per_seg < 1 ? 1 : per_seg);
+  const int64_t seg_groups = (int64_t)*seg_tiles * kSegGroups;
+  *segs_per_slice = (int)(((int64_t)groups_per_slice + seg_groups - 1) / seg_groups);
+}
+
 // Arguments of the cluster row kernel (one cluster per (sequence, position)).
 struct RowArgs {
   const void *target;        // [B][K+1][V]
@@ -34,6 +51,11 @@ struct RowArgs {
   float *dbg_lse;            // optional [B][K+1][2]
   int groups_per_slice;      // 16-byte groups of a row handled by one CTA
   int num_groups;            // ceil(V / elements per 16 bytes)
+  int seg_tiles;             // sampler segment = seg_tiles * kSegGroups groups
+  int segs_per_slice;        // segments of one CTA's slice (<= kMaxSegs)
+  float2 *ws_seg;            // optional scratch [B][S][segs_per_slice]: (max, sum-exp) of the
+                             // bonus row's segments, written in phase 1 (null: the sampler
+                             // reads the bonus row again)
 };
 
 // Arguments of the small-vocabulary tile kernel (a CTA holds whole sequences).

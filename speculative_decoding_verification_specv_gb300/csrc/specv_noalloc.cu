@@ -136,6 +136,9 @@ extern "C" specv_status specv_verify_noalloc(const void *target_logits, const vo
   a.dbg_lse = nullptr;
   a.groups_per_slice = (int)((G + S - 1) / S);
   a.num_groups = (int)G;
+  // no room for the bonus rows' segment statistics: the sampler reads the bonus row again
+  specv::rows_segments(a.groups_per_slice, &a.seg_tiles, &a.segs_per_slice);
+  a.ws_seg = nullptr;
   const bool aligned = ((uintptr_t)target_logits % 16 == 0) && ((uintptr_t)draft_logits % 16 == 0) &&
                        (row_bytes % 16 == 0);
   // the arrival counters must start at zero on every call (no allocation: a memset)

@@ -13,20 +13,25 @@
 // partials over DSMEM in rank order and publishes the position's statistics
 // to the scratch workspace.  The target and the draft row of a pair go
 // through the same instruction sequence, so identical rows give bitwise
-// identical statistics (and an acceptance ratio of exactly 1).
+// identical statistics (and an acceptance ratio of exactly 1).  The bonus
+// row is read by warps in segments (runs of consecutive groups), and the
+// (max, sum-exp) of every segment is kept in the workspace as well.
 //
 // Phase 2 (the last cluster of sequence b to publish, found with one atomic
 // counter per sequence): rank 0's first warp evaluates the acceptance test
 // of every drafted position (the pages' loop: accept x_i iff
 // u_i < min(1, p~(x_i)/q(x_i))), takes the first rejection n, and writes the
-// accepted prefix.  The whole cluster then draws the token at index n by
-// inverse CDF: over normalize(max(0, p~ - q)) of row n if n < K, over the
-// target softmax of row K if every draft passed.  Each CTA sums the weights
-// of its slice with a streaming reduction, the S slice masses are exchanged
-// over DSMEM, and the CTA whose slice holds u * (total mass) finds the token
-// with block scans over tiles of its slice in index order.  (If round-off
-// makes that scan end below the routed target, the slice's last entry of
-// positive weight is taken.)
+// accepted prefix.  The token at index n is then drawn by inverse CDF: over
+// normalize(max(0, p~ - q)) of row n if n < K, over the target softmax of row
+// K if every draft passed.  The search runs over segments.  For a rejected
+// pair every warp sums the sampler weights of its segments of the slice, a
+// block scan gives the running segment sums in index order, the S slice
+// masses are exchanged over DSMEM, and the CTA whose slice holds
+// u * (total mass) picks the segment holding it; one warp walks that segment
+// in index order.  For the bonus row the segment masses follow from the
+// phase-1 segment statistics, so only the chosen segment is read again.
+// (Where round-off makes a walk end below its target, the last entry of
+// positive weight in the segment is taken.)
 //
 // No thread ever waits on another cluster: the counter only decides which
 // cluster does phase 2, and the only barriers are hardware cluster barriers.
@@ -43,6 +48,7 @@ namespace specv {
 namespace {
 
 constexpr int kNT = kRowThreads;  // threads per CTA
+constexpr int kNW = kNT / 32;     // warps per CTA
 constexpr int kUnroll = 4;        // 16-byte groups per thread per batch
 
 struct Broadcast {
@@ -58,15 +64,18 @@ struct __align__(16) RowsShared {
   int last;
   Broadcast bc;
   float masses[2][kMaxCluster];
+  float seg_lo;           // running sum before the chosen segment
+  float segm[kMaxSegs];   // sampler weight of each segment of the slice
+  float segi[kMaxSegs];   // running sums of segm in index order (inclusive)
 };
 
 // Load group g (VW consecutive elements) of a row as one 16-byte vector.  In
 // the aligned case every row starts on a 16-byte boundary and V is a multiple
 // of VW, so a group is one 16-byte load (streaming: no L1 allocation; cached:
-// through L1, for the search pass whose threads read consecutive groups).
-// Otherwise the vector is assembled from scalar loads and entries past V read
-// as -inf (they add nothing to a max or a sum).  Elements are widened to fp32
-// where they are used (Elem<T>::get), which keeps bf16 groups at 4 registers.
+// through L1, for the segment walk).  Otherwise the vector is assembled from
+// scalar loads and entries past V read as -inf (they add nothing to a max or
+// a sum).  Elements are widened to fp32 where they are used (Elem<T>::get),
+// which keeps bf16 groups at 4 registers.
 template <typename T, bool ALIGNED, bool CACHED = false>
 __device__ __forceinline__ uint4 load_group(const T *row, int64_t g, int V) {
   constexpr int VW = Elem<T>::kPerVec;
@@ -86,103 +95,268 @@ __device__ __forceinline__ uint4 load_group(const T *row, int64_t g, int V) {
   }
 }
 
-// Mass of the sampler weights over this CTA's slice: a streaming reduction
-// with the same coalesced access pattern as phase 1.
-template <typename T, int MODE, bool ALIGNED>
-__device__ float slice_mass(RowsShared &sh, const T *rowA, const T *rowB, int V, int g_lo,
-                            int g_hi, int kind, const SampleParams &sp) {
-  constexpr int VW = Elem<T>::kPerVec;
-  float acc = 0.0f;
-  for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += kNT * kUnroll) {
-    uint4 za[kUnroll], zb[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int g = g0 + u * kNT;
-      if (g < g_hi) {
-        za[u] = load_group<T, ALIGNED>(rowA, g, V);
-        if (kind != kWBonus) zb[u] = load_group<T, ALIGNED>(rowB, g, V);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int g = g0 + u * kNT;
-      if (g < g_hi) {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) {
-          if (ALIGNED || (int64_t)g * VW + e < V)
-            acc = __fadd_rn(acc, sample_weight(MODE, kind, sp, Elem<T>::get(za[u], e),
-                                               kind != kWBonus ? Elem<T>::get(zb[u], e) : 0.0f));
-        }
-      }
-    }
-  }
-  return block_sum<kNT>(sh.bs, acc);
+// A 16-byte vector of -inf entries.
+template <typename T>
+__device__ __forceinline__ uint4 neg_inf_group() {
+  const uint32_t w = sizeof(T) == 4 ? Elem<T>::kNegInfBits
+                                    : (Elem<T>::kNegInfBits << 16) | Elem<T>::kNegInfBits;
+  return make_uint4(w, w, w, w);
 }
 
-// Search of this CTA's slice in index order for the first entry whose running
-// weight sum exceeds t.  Tiles of kNT*kSearchU groups; thread j of a tile owns
-// kSearchU consecutive groups (16 entries), a block scan routes t to one thread, and that
-// thread walks its entries.  If round-off leaves no crossing, the largest
-// index with positive weight is returned (-1 if the slice has none).
-template <typename T, int MODE, bool ALIGNED>
-__device__ int slice_search(RowsShared &sh, const T *rowA, const T *rowB, int V, int g_lo, int g_hi,
-                            int kind, const SampleParams &sp, float t) {
+// Phase 1 of the bonus row: (max, sum-exp) of every segment of this CTA's
+// slice, written to out[s] for s < nseg (an empty segment gives (-inf, 0)),
+// and merged into lane 0's running statistics (the other lanes keep theirs
+// empty).  Warp w reads segments w, w + kNW, ...; each tile of a segment is
+// kSegLaneGroups coalesced 16-byte loads per lane.
+template <typename T, bool ALIGNED>
+__device__ void bonus_segment_stats(const T *row, int V, int g_lo, int g_hi, int seg_groups,
+                                    int nseg, float2 *out, float &mA, float &sA) {
   constexpr int VW = Elem<T>::kPerVec;
-  constexpr int kSearchU = 16 / VW;  // 16 entries per thread per tile
-  float base = 0.0f;
-  int lastpos = -1;
-  if (threadIdx.x == 0) sh.bs.found = -1;
-  for (int tb = g_lo; tb < g_hi; tb += kNT * kSearchU) {
-    const int gs = tb + (int)threadIdx.x * kSearchU;
-    float w[kSearchU][VW];
-    float s = 0.0f;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int s = warp; s < nseg; s += kNW) {
+    const int sg_lo = g_lo + s * seg_groups;
+    const int sg_hi = min(g_hi, sg_lo + seg_groups);
+    float ms = -INFINITY, ss = 0.0f;
+    for (int g0 = sg_lo; g0 < sg_hi; g0 += kSegGroups) {
+      uint4 z[kSegLaneGroups];
 #pragma unroll
-    for (int u = 0; u < kSearchU; ++u) {
-      const int g = gs + u;
-      if (g < g_hi) {
-        const uint4 za = load_group<T, ALIGNED, true>(rowA, g, V);
-        const uint4 zb = kind != kWBonus ? load_group<T, ALIGNED, true>(rowB, g, V) : za;
+      for (int u = 0; u < kSegLaneGroups; ++u) {
+        const int g = g0 + u * 32 + lane;
+        z[u] = g < sg_hi ? load_group<T, ALIGNED>(row, g, V) : neg_inf_group<T>();
+      }
+      float bm = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < VW; ++e) {
-          const int idx = g * VW + e;
-          w[u][e] = (ALIGNED || idx < V)
-                        ? sample_weight(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e))
-                        : 0.0f;
-          s = __fadd_rn(s, w[u][e]);
-          if (w[u][e] > 0.0f) lastpos = idx;
+      for (int u = 0; u < kSegLaneGroups; ++u)
+#pragma unroll
+        for (int e = 0; e < VW; ++e) bm = fmaxf(bm, Elem<T>::get(z[u], e));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+      float bs = 0.0f;
+      if (bm != -INFINITY) {  // warp-uniform
+#pragma unroll
+        for (int u = 0; u < kSegLaneGroups; ++u)
+#pragma unroll
+          for (int e = 0; e < VW; ++e) bs = __fadd_rn(bs, exp_shifted(Elem<T>::get(z[u], e), bm));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) bs = __fadd_rn(bs, __shfl_xor_sync(0xffffffffu, bs, off));
+      merge_stats(ms, ss, bm, bs);
+    }
+    if (lane == 0) {
+      out[s] = make_float2(ms, ss);
+      merge_stats(mA, sA, ms, ss);
+    }
+  }
+  __threadfence();  // the segment statistics are visible device-wide before this position publishes
+}
+
+// Sampler weight of each segment of this CTA's slice into sh.segm, then the
+// inclusive running sums in index order into sh.segi; returns the slice's mass
+// (equal to the last running sum).  Warp w takes segments w, w + kNW, ...
+template <typename T, int MODE, bool ALIGNED>
+__device__ float segment_masses(RowsShared &sh, const T *rowA, const T *rowB, int V, int g_lo,
+                                int g_hi, int seg_groups, int nseg, int kind,
+                                const SampleParams &sp) {
+  constexpr int VW = Elem<T>::kPerVec;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int s = warp; s < nseg; s += kNW) {
+    const int sg_lo = g_lo + s * seg_groups;
+    const int sg_hi = min(g_hi, sg_lo + seg_groups);
+    float acc = 0.0f;
+    for (int g0 = sg_lo; g0 < sg_hi; g0 += kSegGroups) {
+      uint4 za[kSegLaneGroups], zb[kSegLaneGroups];
+#pragma unroll
+      for (int u = 0; u < kSegLaneGroups; ++u) {
+        const int g = g0 + u * 32 + lane;
+        if (g < sg_hi) {
+          za[u] = load_group<T, ALIGNED>(rowA, g, V);
+          if (kind != kWBonus) zb[u] = load_group<T, ALIGNED>(rowB, g, V);
         }
-      } else {
+      }
 #pragma unroll
-        for (int e = 0; e < VW; ++e) w[u][e] = 0.0f;
+      for (int u = 0; u < kSegLaneGroups; ++u) {
+        const int g = g0 + u * 32 + lane;
+        if (g < sg_hi) {
+#pragma unroll
+          for (int e = 0; e < VW; ++e)
+            if (ALIGNED || (int64_t)g * VW + e < V)
+              acc = __fadd_rn(acc, sample_weight(MODE, kind, sp, Elem<T>::get(za[u], e),
+                                                 kind != kWBonus ? Elem<T>::get(zb[u], e) : 0.0f));
+        }
       }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+    if (lane == 0) sh.segm[s] = acc;
+  }
+  __syncthreads();
+  float base = 0.0f;
+  for (int s0 = 0; s0 < nseg; s0 += kNT) {
+    const int s = s0 + (int)threadIdx.x;
     float excl, incl, total;
-    block_scan<kNT>(sh.bs, s, excl, incl, total);
-    const float lo = __fadd_rn(base, excl), hi = __fadd_rn(base, incl);
-    if (lo <= t && t < hi) {  // only one thread: the intervals partition [base, base+total)
-      float c = lo;
-      int pick = -1, lastg = -1;
-#pragma unroll
-      for (int u = 0; u < kSearchU; ++u)
-#pragma unroll
-        for (int e = 0; e < VW; ++e) {
-          c = __fadd_rn(c, w[u][e]);
-          if (w[u][e] > 0.0f) lastg = (gs + u) * VW + e;
-          if (pick < 0 && c > t) pick = (gs + u) * VW + e;
-        }
-      sh.bs.found = pick >= 0 ? pick : lastg;
-    }
-    __syncthreads();
-    const int f = sh.bs.found;
-    __syncthreads();
-    if (f >= 0) return f;
+    block_scan<kNT>(sh.bs, s < nseg ? sh.segm[s] : 0.0f, excl, incl, total);
+    if (s < nseg) sh.segi[s] = __fadd_rn(base, incl);
     base = __fadd_rn(base, total);
   }
-  return block_max_index<kNT>(sh.bs, lastpos);
+  __syncthreads();
+  return base;
+}
+
+// The segment of this slice whose running-sum interval [segi[s-1], segi[s])
+// holds t (the intervals are disjoint: the running sums never decrease).  If
+// none does (t at or past the slice's mass: u >= 1 or round-off), the last
+// segment of positive mass, with t set to +inf so that its walk takes its last
+// entry of positive weight.  *lo gets the running sum before the segment.
+__device__ int find_segment(RowsShared &sh, int nseg, float &t, float *lo) {
+  if (threadIdx.x == 0) sh.bs.found = -1;
+  __syncthreads();
+  int lastpos = -1;
+  for (int s = threadIdx.x; s < nseg; s += kNT) {
+    const float l = s ? sh.segi[s - 1] : 0.0f;
+    if (l <= t && t < sh.segi[s]) sh.bs.found = s;
+    if (sh.segm[s] > 0.0f) lastpos = s;
+  }
+  __syncthreads();
+  int s = sh.bs.found;
+  __syncthreads();
+  if (s < 0) {
+    s = block_max_index<kNT>(sh.bs, lastpos);
+    t = INFINITY;
+  }
+  *lo = s > 0 ? sh.segi[s - 1] : 0.0f;
+  return s;
+}
+
+// One warp walks the groups [sg_lo, sg_hi) of the row(s) in index order,
+// starting from running sum c, and returns the first entry at which the
+// running sum of sampler weights exceeds t; if round-off leaves no crossing,
+// the last entry of positive weight (-1 if none).  Index order within a tile
+// is (load u, lane, element): the 32 lanes of one load are scanned together.
+template <typename T, int MODE, bool ALIGNED>
+__device__ int segment_walk(const T *rowA, const T *rowB, int V, int sg_lo, int sg_hi, int kind,
+                            const SampleParams &sp, float c, float t) {
+  constexpr int VW = Elem<T>::kPerVec;
+  const int lane = threadIdx.x & 31;
+  int lastpos = -1;
+  for (int g0 = sg_lo; g0 < sg_hi; g0 += kSegGroups) {
+    uint4 za[kSegLaneGroups], zb[kSegLaneGroups];
+#pragma unroll
+    for (int u = 0; u < kSegLaneGroups; ++u) {
+      const int g = g0 + u * 32 + lane;
+      za[u] = g < sg_hi ? load_group<T, ALIGNED, true>(rowA, g, V) : neg_inf_group<T>();
+      zb[u] = (g < sg_hi && kind != kWBonus) ? load_group<T, ALIGNED, true>(rowB, g, V) : za[u];
+    }
+#pragma unroll
+    for (int u = 0; u < kSegLaneGroups; ++u) {
+      const int g = g0 + u * 32 + lane;
+      float w[VW];
+      float s = 0.0f;
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        const int idx = g * VW + e;
+        w[e] = (g < sg_hi && (ALIGNED || idx < V))
+                   ? sample_weight(MODE, kind, sp, Elem<T>::get(za[u], e), Elem<T>::get(zb[u], e))
+                   : 0.0f;
+        s = __fadd_rn(s, w[e]);
+        if (w[e] > 0.0f) lastpos = idx;
+      }
+      float incl = s;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl = __fadd_rn(incl, y);
+      }
+      const float hi = __fadd_rn(c, incl);
+      const float prev = __shfl_up_sync(0xffffffffu, hi, 1);
+      const float lo = lane == 0 ? c : prev;
+      const unsigned cross = __ballot_sync(0xffffffffu, hi > t);
+      if (cross != 0u) {  // warp-uniform
+        const int L = __ffs(cross) - 1;
+        int pick = -1, lastl = -1;
+        float cc = lo;
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          cc = __fadd_rn(cc, w[e]);
+          if (w[e] > 0.0f) lastl = g * VW + e;
+          if (pick < 0 && cc > t) pick = g * VW + e;
+        }
+        pick = pick >= 0 ? pick : lastl;
+        return __shfl_sync(0xffffffffu, pick, L);
+      }
+      c = __shfl_sync(0xffffffffu, hi, 31);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, off));
+  return lastpos;
+}
+
+// Bonus token from the segment statistics phase 1 wrote for row K (run by
+// one CTA): the mass of a segment is s_seg * exp(m_seg - mA) / S_A, the target
+// softmax summed over it; block scans over the S slices' segments in index
+// order give the total and route u * total to one segment, which warp 0
+// walks.  Returns the token (valid in warp 0), or -1 if the row has no mass.
+template <typename T, int MODE, bool ALIGNED>
+__device__ int bonus_from_stats(RowsShared &sh, const RowArgs &a, const T *row, int S, int64_t b,
+                                const SampleParams &sp, float u) {
+  const int nseg = a.segs_per_slice;
+  const int total = S * nseg;
+  const float2 *st = a.ws_seg + b * (int64_t)S * nseg;
+  auto mass = [&](int j) -> float {
+    if (j >= total) return 0.0f;
+    const float2 v = __ldcg(&st[j]);
+    return v.x == -INFINITY ? 0.0f
+                            : __fmul_rn(__fmul_rn(v.y, exp_shifted(v.x, sp.mA)), sp.invSA);
+  };
+  float W = 0.0f;
+  for (int j0 = 0; j0 < total; j0 += kNT) {
+    float excl, incl, tot;
+    block_scan<kNT>(sh.bs, mass(j0 + (int)threadIdx.x), excl, incl, tot);
+    W = __fadd_rn(W, tot);
+  }
+  if (!(W > 0.0f)) return -1;
+  float t = __fmul_rn(u, W);
+  float base = 0.0f;
+  int found = -1, lastpos = -1;
+  if (threadIdx.x == 0) sh.bs.found = -1;
+  for (int j0 = 0; j0 < total; j0 += kNT) {
+    const int j = j0 + (int)threadIdx.x;
+    const float m = mass(j);
+    float excl, incl, tot;
+    block_scan<kNT>(sh.bs, m, excl, incl, tot);
+    const float l = __fadd_rn(base, excl), h = __fadd_rn(base, incl);
+    if (j < total && l <= t && t < h) {
+      sh.bs.found = j;
+      sh.seg_lo = l;
+    }
+    if (m > 0.0f) lastpos = j;
+    __syncthreads();
+    found = sh.bs.found;
+    __syncthreads();
+    if (found >= 0) break;
+    base = __fadd_rn(base, tot);
+  }
+  float lo = 0.0f;
+  if (found >= 0) {
+    lo = sh.seg_lo;
+  } else {  // u * W not below the total (u >= 1): the last segment with mass, its last entry
+    found = block_max_index<kNT>(sh.bs, lastpos);
+    t = INFINITY;
+  }
+  if ((threadIdx.x >> 5) != 0 || found < 0) return -1;
+  const int seg_groups = a.seg_tiles * kSegGroups;
+  const int r = found / nseg, s = found - r * nseg;
+  const int r_lo = r * a.groups_per_slice;
+  const int r_hi = min(a.num_groups, r_lo + a.groups_per_slice);
+  const int sg_lo = r_lo + s * seg_groups;
+  const int sg_hi = min(r_hi, sg_lo + seg_groups);
+  return segment_walk<T, MODE, ALIGNED>(row, row, a.V, sg_lo, sg_hi, kWBonus, sp, lo, t);
 }
 
 template <typename T, int MODE, bool ALIGNED>
-__global__ void __launch_bounds__(kNT) rows_kernel(RowArgs a) {
+__global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   constexpr int VW = Elem<T>::kPerVec;
   __shared__ RowsShared sh;
   cg::cluster_group cluster = cg::this_cluster();
@@ -203,6 +377,12 @@ __global__ void __launch_bounds__(kNT) rows_kernel(RowArgs a) {
 
   // ---------------------------------------------------------------- phase 1
   float mA = -INFINITY, sA = 0.0f, mB = -INFINITY, sB = 0.0f;
+  const int seg_groups = a.seg_tiles * kSegGroups;
+  const int nseg = a.segs_per_slice;
+  if (!pair && a.ws_seg != nullptr)
+    bonus_segment_stats<T, ALIGNED>(rowA, V, g_lo, g_hi, seg_groups, nseg,
+                                    a.ws_seg + (b * S + rank) * (int64_t)nseg, mA, sA);
+  else
   for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += kNT * kUnroll) {
     uint4 za[kUnroll], zb[kUnroll];
     bool ok[kUnroll];
@@ -350,11 +530,20 @@ __global__ void __launch_bounds__(kNT) rows_kernel(RowArgs a) {
   if (bc.n < 0) return;
   const T *sA_row = tgt + (b * (K + 1) + bc.n) * (int64_t)V;
   const T *sB_row = dft + (b * K + (bc.n < K ? bc.n : 0)) * (int64_t)V;
+  if (bc.kind == kWBonus && a.ws_seg != nullptr) {
+    // every draft accepted: the bonus row's segment statistics are in the workspace
+    if (rank != 0) return;
+    __threadfence();
+    const int tok = bonus_from_stats<T, MODE, ALIGNED>(sh, a, sA_row, S, b, bc.sp, bc.u);
+    if (threadIdx.x == 0) a.out_tokens[b * (K + 1) + bc.n] = tok;
+    return;
+  }
   int kind = bc.kind;
   float R = 0.0f;
   int attempt = 0;
   for (;; ++attempt) {
-    const float mass = slice_mass<T, MODE, ALIGNED>(sh, sA_row, sB_row, V, g_lo, g_hi, kind, bc.sp);
+    const float mass = segment_masses<T, MODE, ALIGNED>(sh, sA_row, sB_row, V, g_lo, g_hi,
+                                                        seg_groups, nseg, kind, bc.sp);
     if (threadIdx.x == 0)
       for (int r = 0; r < S; ++r) cluster.map_shared_rank(sh.masses[attempt], r)[rank] = mass;
     cluster.sync();  // all slice masses exchanged
@@ -389,9 +578,18 @@ __global__ void __launch_bounds__(kNT) rows_kernel(RowArgs a) {
     tloc = INFINITY;
   }
   if (rank != rstar) return;
+  float lo = 0.0f;
+  const int s = find_segment(sh, nseg, tloc, &lo);
+  if (warp != 0) return;
+  if (s < 0) {  // no entry of positive weight in the routed slice (not reached: its mass is > 0)
+    if (lane == 0) a.out_tokens[b * (K + 1) + bc.n] = -1;
+    return;
+  }
+  const int sg_lo = g_lo + s * seg_groups;
+  const int sg_hi = min(g_hi, sg_lo + seg_groups);
   const int tok =
-      slice_search<T, MODE, ALIGNED>(sh, sA_row, sB_row, V, g_lo, g_hi, kind, bc.sp, tloc);
-  if (threadIdx.x == 0) a.out_tokens[b * (K + 1) + bc.n] = tok;
+      segment_walk<T, MODE, ALIGNED>(sA_row, sB_row, V, sg_lo, sg_hi, kind, bc.sp, lo, tloc);
+  if (lane == 0) a.out_tokens[b * (K + 1) + bc.n] = tok;
 }
 
 template <typename T, int MODE, bool ALIGNED>

@@ -139,6 +139,24 @@ def test_row_variants_on_workloads(specv, cluster_env, variant, cfg, mode):
     print(f"{variant} variant, workload {cfg}: {rep}")
 
 
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+@pytest.mark.parametrize("V,dt", [(300000, "f32"), (300001, "f32"), (600000, "bf16")])
+def test_long_slices_multi_tile_segments(specv, cluster_env, V, dt, mode):
+    """One CTA per row and slices of 75000 groups: more groups than the sampler's
+    segment table holds in single tiles, so every segment spans two tiles.  Half
+    the sequences accept every draft (bonus rows sampled from the segment
+    statistics of the first pass), the rest reject (residual walk)."""
+    os.environ["SPECV_CLUSTER_SIZE"] = "1"
+    os.environ["SPECV_ROWS_VARIANT"] = "stream"
+    w = workloads.Workload("long-slices", 6, 3, V, dt, "half_equal:3.0:0.85:1.0", (0.2,), 11)
+    plan = specv.plan(w.B, w.K, w.V, 1 if dt == "bf16" else 0, mode)
+    assert plan["kernel"] == "rows-stream" and plan["cluster"] == 1
+    x = workloads.make_inputs(w, DEV)
+    rep, _, n = _check(specv, x, mode)
+    assert (n == w.K).any() and (n < w.K).any()
+    print(f"V={V} {dt} mode={mode}: {rep}")
+
+
 RAGGED = [
     # (B, K, V, dtype, structure)
     (3, 1, 1001, "f32", "corr:2.0:0.8:1.0"),       # rows kernel, unaligned rows
