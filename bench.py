@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rows_kernel_batched_v128256_f32.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_specv_gb300", "csrc", f)
                   for f in ("specv_rows.cu", "specv_device.cuh", "specv_block.cuh",
-                            "specv_internal.h")]
+                            "specv_segments.cuh", "specv_internal.h")]
 
 
 def parse():
@@ -89,7 +89,7 @@ def job_throughput(rows_per_step, steps, ws, slowest_ms):
 # kernel function timed for the roofline, by the planner's kernel name
 PLAN_KERNEL_FUNCTION = {"tile": "tile_kernel", "rows-stream": "rows_kernel",
                         "rows-resident": "resident_kernel", "tile-tma": "tile_tma_kernel",
-                        "rows-spec": "resident_kernel"}
+                        "rows-spec": "resident_kernel", "rows-sweep": "sweep_kernel"}
 
 
 def measured_peak():

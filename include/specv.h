@@ -136,7 +136,10 @@ specv_status specv_verify_debug(const void *target_logits, const void *draft_log
  *            speculatively in place (only when the environment variable
  *            SPECV_ROWS_VARIANT=spec asks for it; =stream and =resident force
  *            kernels 1 and 2, and SPECV_CLUSTER_SIZE=1..16 (a power of two)
- *            forces the cluster size of the row kernels)
+ *            forces the cluster size of the row kernels),
+ *            5 = sweep row kernel: persistent CTAs stream fixed-size chunks of
+ *            the rows through shared memory by bulk copies (only when
+ *            SPECV_ROWS_VARIANT=sweep asks for it; rows on 16-byte boundaries)
  *   cluster: CTAs per thread-block cluster splitting each row (1 for kernel 0)
  *   ctas:    CTAs launched by a row kernel; tiles of sequences for kernels 0, 3
  *   workspace_bytes: scratch bytes of the row kernels' workspace (kept per

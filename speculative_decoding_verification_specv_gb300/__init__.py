@@ -190,7 +190,8 @@ def verify_debug(target_logits, draft_logits, draft_tokens, u_accept, u_resample
 
 
 # specv_plan's kernel codes
-KERNEL_NAMES = {0: "tile", 1: "rows-stream", 2: "rows-resident", 3: "tile-tma", 4: "rows-spec"}
+KERNEL_NAMES = {0: "tile", 1: "rows-stream", 2: "rows-resident", 3: "tile-tma", 4: "rows-spec",
+                5: "rows-sweep"}
 
 
 def plan(B: int, K: int, V: int, dtype: int = F32, mode: int = PROB_MIX) -> dict:

@@ -27,6 +27,9 @@ constexpr int32_t kMaxK = 4096;
 // that three CTAs fit an SM.
 constexpr int kResidentMaxSmem = 200 * 1024;
 constexpr int kResidentTarget = 96 * 1024;
+// Sweep row kernel: CTAs per SM of its persistent grid (its launch bounds and
+// at most 96 KiB of stages per CTA let two fit).
+constexpr int kSweepBlocksPerSM = 2;
 
 struct DeviceState {
   bool ready = false;
@@ -146,7 +149,8 @@ specv_status ensure_device(int *sms_out, int64_t *l2_out) {
     if ((e = specv::rows_prepare()) != cudaSuccess ||
         (e = specv::resident_prepare(kResidentMaxSmem)) != cudaSuccess ||
         (e = specv::tile_prepare(kTileSmemBudget)) != cudaSuccess ||
-        (e = specv::tile_tma_prepare(2 * kTmaTileStageBytes + 16 * 1024)) != cudaSuccess) {
+        (e = specv::tile_tma_prepare(2 * kTmaTileStageBytes + 16 * 1024)) != cudaSuccess ||
+        (e = specv::sweep_prepare(specv::sweep_smem_bytes(1024))) != cudaSuccess) {
       note_cuda_error(e);
       return SPECV_ERR_CUDA;
     }
@@ -170,6 +174,9 @@ struct Plan {
   int groups_per_slice, num_groups;
   int seg_tiles, segs_per_slice;  // sampler segments of the streaming row kernel
   int res_smem;          // dynamic shared memory of the resident kernel
+  int chunk_groups, chunks;       // sweep kernel: groups per chunk, chunks per row
+  int sweep_smem;        // dynamic shared memory of the sweep kernel
+  int64_t counters;      // arrival counters in the scratch
 };
 
 int64_t round16(int64_t x) { return (x + 15) / 16 * 16; }
@@ -197,6 +204,7 @@ int variant_from_env() {
   if (std::strcmp(s, "stream") == 0) return 1;
   if (std::strcmp(s, "resident") == 0) return 2;
   if (std::strcmp(s, "spec") == 0) return 4;
+  if (std::strcmp(s, "sweep") == 0) return 5;
   return 0;
 }
 
@@ -251,6 +259,28 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, int6
   const int64_t G = (V + vw - 1) / vw;
   const int env_S = cluster_from_env();
   const int env_var = variant_from_env();
+  if (env_var == 5) {
+    // sweep kernel: persistent CTAs, kSweepBlocksPerSM per SM; chunks of 1024
+    // groups (16 KiB of a row), halved down to 256 while there are fewer than
+    // two items per CTA
+    if (!aligned || row_bytes % 16 != 0) return SPECV_ERR_UNSUPPORTED;
+    const int64_t grid_max = (int64_t)sms * kSweepBlocksPerSM;
+    int cg = 1024;
+    while (cg > specv::kSweepThreads && P * ((G + cg - 1) / cg) < 2 * grid_max) cg /= 2;
+    const int64_t C = (G + cg - 1) / cg;
+    if (P * C > INT64_MAX / 16 || C > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
+    p->kernel = 5;
+    p->cluster = 1;
+    p->chunk_groups = cg;
+    p->chunks = (int)C;
+    p->num_groups = (int)G;
+    specv::segment_geometry(G, specv::kSweepSegGroups, &p->seg_tiles, &p->segs_per_slice);
+    p->sweep_smem = specv::sweep_smem_bytes(cg);
+    p->ctas = P * C < grid_max ? P * C : grid_max;
+    p->counters = P + B;
+    p->ws_bytes = round16(P * C * 16) + round16(P * 16) + round16(p->counters * 4);
+    return SPECV_OK;
+  }
   const bool can_resident = aligned && (row_bytes % 16 == 0) && env_var != 1 && env_var != 4;
   auto slice_smem = [&](int S) { return 2 * ((G + S - 1) / S) * 16; };
   int S = 0;
@@ -300,6 +330,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, int6
   p->ctas = P * S;
   p->num_groups = (int)G;
   p->groups_per_slice = (int)((G + S - 1) / S);
+  p->counters = B;
   if (kernel == 2 || kernel == 4) {
     p->res_smem = kernel == 2 ? (int)slice_smem(S) : 0;
     p->ws_bytes = round16(P * 8) + round16(B * 4);
@@ -368,12 +399,12 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
   (void)cudaGetDevice(&dev);
   // scratch: counters [B] then position data, from the stream's cache or,
   // failing that, stream-ordered memory for this call (counters cleared)
-  const size_t data_bytes = (size_t)(p.ws_bytes - round16(B * 4));
+  const size_t data_bytes = (size_t)(p.ws_bytes - round16(p.counters * 4));
   unsigned *cnt = nullptr;
   void *wdata = nullptr;
   void *ws = nullptr;
   e = cudaSuccess;
-  const bool per_call = !cached_workspace(dev, stream, B, data_bytes, &cnt, &wdata);
+  const bool per_call = !cached_workspace(dev, stream, p.counters, data_bytes, &cnt, &wdata);
   if (per_call) {
     e = cudaMallocAsync(&ws, (size_t)p.ws_bytes, stream);
     if (e != cudaSuccess) {
@@ -382,10 +413,39 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
       return SPECV_ERR_NO_MEMORY;
     }
     cnt = static_cast<unsigned *>(ws);
-    wdata = static_cast<char *>(ws) + round16(B * 4);
-    e = cudaMemsetAsync(cnt, 0, (size_t)B * sizeof(unsigned), stream);
+    wdata = static_cast<char *>(ws) + round16(p.counters * 4);
+    e = cudaMemsetAsync(cnt, 0, (size_t)p.counters * sizeof(unsigned), stream);
   }
-  if (p.kernel == 2 || p.kernel == 4) {
+  if (p.kernel == 5) {
+    const int64_t P = B * (K + 1);
+    specv::SweepArgs w;
+    w.target = target;
+    w.draft = draft;
+    w.tokens = tokens;
+    w.u_accept = ua;
+    w.u_resample = ur;
+    w.lam = lam;
+    w.B = B;
+    w.K = K;
+    w.V = V;
+    w.out_tokens = out_tokens;
+    w.out_n = out_n;
+    w.ws_chunk = static_cast<float4 *>(wdata);
+    w.ws_stats = reinterpret_cast<float4 *>(static_cast<char *>(wdata) +
+                                            round16(P * (int64_t)p.chunks * 16));
+    w.row_count = cnt;
+    w.seq_count = cnt + P;
+    w.dbg_ptilde = dbg_ptilde;
+    w.dbg_q = dbg_q;
+    w.dbg_lse = dbg_lse;
+    w.num_groups = p.num_groups;
+    w.chunk_groups = p.chunk_groups;
+    w.chunks = p.chunks;
+    w.seg_tiles = p.seg_tiles;
+    w.nseg = p.segs_per_slice;
+    w.items = P * (int64_t)p.chunks;
+    if (e == cudaSuccess) e = specv::sweep_launch(w, bf16, mode, p.ctas, p.sweep_smem, stream);
+  } else if (p.kernel == 2 || p.kernel == 4) {
     specv::ResArgs r;
     r.target = target;
     r.draft = draft;

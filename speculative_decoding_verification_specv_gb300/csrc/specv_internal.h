@@ -22,14 +22,54 @@ constexpr int kSegLaneGroups = 4;
 constexpr int kSegGroups = 32 * kSegLaneGroups;
 constexpr int kMaxSegs = 512;
 
-// Segment geometry of a slice of groups_per_slice groups.
-inline void rows_segments(int groups_per_slice, int *seg_tiles, int *segs_per_slice) {
-  const int64_t tiles = ((int64_t)groups_per_slice + kSegGroups - 1) / kSegGroups;
+// Segment geometry of a slice of `groups` groups read in tiles of tile_groups:
+// the fewest whole tiles per segment that keep the count within kMaxSegs.
+inline void segment_geometry(int64_t groups, int tile_groups, int *seg_tiles, int *nseg) {
+  const int64_t tiles = (groups + tile_groups - 1) / tile_groups;
   const int64_t per_seg = (tiles + kMaxSegs - 1) / kMaxSegs;
   *seg_tiles = (int)(per_seg < 1 ? 1 : per_seg);
-  const int64_t seg_groups = (int64_t)*seg_tiles * kSegGroups;
-  *segs_per_slice = (int)(((int64_t)groups_per_slice + seg_groups - 1) / seg_groups);
+  const int64_t seg_groups = (int64_t)*seg_tiles * tile_groups;
+  *nseg = (int)((groups + seg_groups - 1) / seg_groups);
 }
+inline void rows_segments(int groups_per_slice, int *seg_tiles, int *segs_per_slice) {
+  segment_geometry(groups_per_slice, kSegGroups, seg_tiles, segs_per_slice);
+}
+
+// The sweep row kernel: persistent CTAs of kSweepThreads threads stream
+// chunks of rows through a ring of kSweepStages shared-memory stages filled by
+// 1-D bulk copies.  A stage holds one chunk of a target row and the same chunk
+// of its draft row.  The sampler reads tiles of 32 * kSweepLaneGroups groups.
+constexpr int kSweepThreads = 256;
+constexpr int kSweepStages = 3;
+constexpr int kSweepLaneGroups = 4;
+constexpr int kSweepSegGroups = 32 * kSweepLaneGroups;
+
+struct SweepArgs {
+  const void *target;        // [B][K+1][V], 16-byte aligned, V * sizeof(dtype) % 16 == 0
+  const void *draft;         // [B][K][V], same
+  const int32_t *tokens;     // [B][K]
+  const float *u_accept;     // [B][K]
+  const float *u_resample;   // [B]
+  const float *lam;          // [B]
+  int64_t B;
+  int K;
+  int V;
+  int32_t *out_tokens;       // [B][K+1]
+  int32_t *out_n;            // [B]
+  float4 *ws_chunk;          // scratch [B][K+1][chunks]: (mA, sA, mB, sB) of every chunk
+  float4 *ws_stats;          // scratch [B][K+1]: (mA, sA, mB, sB) of every position
+  unsigned *row_count;       // scratch [B][K+1]: chunks published (zero at entry, left zero)
+  unsigned *seq_count;       // scratch [B]: positions published (zero at entry, left zero)
+  float *dbg_ptilde;         // optional [B][K]
+  float *dbg_q;              // optional [B][K]
+  float *dbg_lse;            // optional [B][K+1][2]
+  int num_groups;            // V / elements per 16 bytes
+  int chunk_groups;          // groups per chunk (a multiple of kSweepThreads)
+  int chunks;                // chunks per row
+  int seg_tiles;             // sampler segment = seg_tiles * kSweepSegGroups groups
+  int nseg;                  // sampler segments per row (<= kMaxSegs)
+  int64_t items;             // B * (K+1) * chunks
+};
 
 // Arguments of the cluster row kernel (one cluster per (sequence, position)).
 struct RowArgs {
@@ -109,6 +149,13 @@ cudaError_t resident_prepare(int max_smem);
 // from global memory (the sampler re-reads the slice, from L2 when it fits).
 cudaError_t resident_launch(const ResArgs &a, int dtype_bf16, int mode, bool staged, int S,
                             int64_t grid, int smem, cudaStream_t stream);
+
+// Dynamic shared memory of the sweep kernel for chunks of chunk_groups groups.
+inline int sweep_smem_bytes(int chunk_groups) { return kSweepStages * 2 * chunk_groups * 16; }
+cudaError_t sweep_prepare(int max_smem_bytes);
+int sweep_blocks_per_sm(int dtype_bf16, int mode, int smem_bytes);
+cudaError_t sweep_launch(const SweepArgs &a, int dtype_bf16, int mode, int64_t grid,
+                         int smem_bytes, cudaStream_t stream);
 
 cudaError_t rows_prepare();
 cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,

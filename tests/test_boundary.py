@@ -86,3 +86,24 @@ def test_plan_selects_kernels(lib):
     assert specv.plan(2, 2, 1 << 24, specv.F32)["kernel"] == "rows-stream"
     with pytest.raises(specv.SpecvError):
         specv.plan(0, 4, 32)
+
+
+def test_plan_sweep_variant(lib, monkeypatch):
+    """The sweep row kernel (forced by SPECV_ROWS_VARIANT=sweep): persistent grid
+    of two CTAs per SM at most, scratch = chunk statistics + position statistics
+    + one counter per position and per sequence; rows not on 16-byte boundaries
+    are refused."""
+    monkeypatch.setenv("SPECV_ROWS_VARIANT", "sweep")
+    B, K, V = 256, 8, 128256
+    p = specv.plan(B, K, V, specv.F32)
+    P, G = B * (K + 1), V // 4
+    C = -(-G // 1024)
+    assert p["kernel"] == "rows-sweep" and p["cluster"] == 1
+    assert p["ctas"] <= 2 * 152
+    r16 = lambda x: -(-x // 16) * 16  # noqa: E731
+    assert p["workspace_bytes"] == r16(P * C * 16) + r16(P * 16) + r16((P + B) * 4)
+    # few positions: chunks shrink to 256 groups and the grid to the items
+    p1 = specv.plan(1, 4, 1000, specv.F32)
+    assert p1["kernel"] == "rows-sweep" and p1["ctas"] == 5
+    with pytest.raises(specv.SpecvError):
+        specv.plan(3, 2, 1001, specv.F32)
