@@ -27,6 +27,7 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
 PROB_MIX = 0
 LOGIT_MIX = 1
+GREEDY = 2
 
 FLAG_INVALID = 1
 FLAG_RESIDUAL_ZERO = 2
@@ -76,6 +77,10 @@ def _load():
         lib.oracle_verify.argtypes = [fp, fp, ip, fp, fp, fp, i64, i64, ctypes.c_int32, i64,
                                       ctypes.c_int, ip, ip, dp, dp, dp, dp, dp, dp, ip]
         lib.oracle_verify.restype = ctypes.c_int
+        lib.oracle_greedy_argmax.argtypes = [fp, fp, ctypes.c_float, i64]
+        lib.oracle_greedy_argmax.restype = i64
+        lib.oracle_verify_greedy.argtypes = [fp, fp, ip, fp, i64, i64, ctypes.c_int32, i64, ip, ip]
+        lib.oracle_verify_greedy.restype = None
         _lib = lib
         return lib
 
@@ -221,3 +226,42 @@ def verify(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam,
     res = Result(tokens=out_tok, n_accepted=out_n, threads=nthreads)
     res.update(diag)
     return res
+
+
+def greedy_argmax(zt_row, zq_row, lam: float) -> int:
+    """Argmax of w = z_t + lam (z_q - z_t) over one row, in fp32 as the kernels
+    form it (zq_row None: w = z_t); the first index among equal maxima."""
+    zt = _f32(zt_row).reshape(-1)
+    zq = None if zq_row is None else _f32(zq_row).reshape(-1)
+    return int(_load().oracle_greedy_argmax(_ptr(zt, ctypes.c_float), _ptr(zq, ctypes.c_float),
+                                            float(np.float32(lam)), zt.size))
+
+
+def verify_greedy(target_logits, draft_logits, draft_tokens, lam,
+                  threads: int | None = None) -> Result:
+    """Greedy verification of a batch (same layouts as ``verify``)."""
+    zt = _f32(target_logits)
+    zq = _f32(draft_logits)
+    tok = _i32(draft_tokens)
+    lm = _f32(lam).reshape(-1)
+    B, K1, V = zt.shape
+    K = K1 - 1
+    assert zq.shape == (B, K, V) and tok.shape == (B, K) and lm.shape == (B,)
+    out_tok = np.full((B, K + 1), -2, np.int32)
+    out_n = np.full((B,), -2, np.int32)
+    lib = _load()
+
+    def run(lo, hi):
+        lib.oracle_verify_greedy(_ptr(zt, ctypes.c_float), _ptr(zq, ctypes.c_float),
+                                 _ptr(tok, ctypes.c_int32), _ptr(lm, ctypes.c_float), lo, hi, K,
+                                 V, _ptr(out_tok, ctypes.c_int32), _ptr(out_n, ctypes.c_int32))
+
+    nthreads = threads if threads is not None else (os.cpu_count() or 1)
+    nthreads = max(1, min(nthreads, B))
+    if nthreads == 1:
+        run(0, B)
+    else:
+        edges = np.linspace(0, B, nthreads + 1).astype(np.int64)
+        with ThreadPoolExecutor(max_workers=nthreads) as ex:
+            list(ex.map(lambda j: run(int(edges[j]), int(edges[j + 1])), range(nthreads)))
+    return Result(tokens=out_tok, n_accepted=out_n, threads=nthreads)

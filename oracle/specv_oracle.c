@@ -21,7 +21,10 @@
  *              and discard the rest of the draft.
  *   [EAGLE]  "投机解码（EAGLE）：让小模型猜、大模型验，无损加速 LLM 生成"
  *            - "关键技术点 / 1. 为什么无损": the resample distribution is
- *              max(0, p - q) (normalised), which makes the output exact.
+ *              max(0, p - q) (normalised), which makes the output exact;
+ *            - "核心思路", step 3 (accept/reject): a draft token that is the
+ *              target model's most likely token is accepted outright (the
+ *              greedy clause).
  *
  * Readings taken where the pages are silent or ambiguous (each one is also
  * listed in the design notes):
@@ -42,6 +45,17 @@
  *     rejects.
  *   - Invalid input (a draft token outside [0, V), or lambda outside [0, 1]
  *     or NaN) gives n_accepted = -1 and all output tokens -1.
+ *
+ *   - Greedy verification (the greedy clause of [EAGLE] "核心思路") is read as:
+ *     accept x_i iff x_i is the argmax of the mixed logits
+ *     w = z_t + lambda (z_q - z_t) of row i (the logit-space enhanced target,
+ *     whose softmax is p~ in logit mode; lambda = 0 gives the target's own
+ *     argmax, the clause as printed), emit that argmax at the first mismatch,
+ *     and the argmax of target row K when every draft matches.  Equal maxima
+ *     go to the smallest index.  w is formed in fp32 exactly as the kernels
+ *     form it (one rounded subtraction, one fused multiply-add; -inf where
+ *     z_q = -inf), because an argmax is an integer decided by floating point:
+ *     both sides must decide it in the same precision.
  *
  * Everything is computed in double precision.  fp32 inputs are promoted
  * exactly; bf16 inputs are widened to fp32 (exactly) by the caller first.
@@ -308,4 +322,70 @@ int oracle_verify(const float *zt, const float *zq, const int32_t *tok, const fl
     }
     free(buf);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Greedy verification (reading in the header).                              */
+
+/* w of one entry, in fp32 as the kernels form it. */
+static float greedy_w(float zt, float zq, float lam)
+{
+    if (zq == -INFINITY) return -INFINITY;
+    float d = zq - zt;          /* one rounded fp32 subtraction */
+    return fmaf(lam, d, zt);    /* one fused multiply-add */
+}
+
+/* Argmax over v of w_v (zq == NULL: w = z_t, the bonus position); the first
+ * index among equal maxima. */
+int64_t oracle_greedy_argmax(const float *zt, const float *zq, float lam, int64_t V)
+{
+    int64_t best = 0;
+    float bw = zq ? greedy_w(zt[0], zq[0], lam) : zt[0];
+    for (int64_t v = 1; v < V; ++v) {
+        float w = zq ? greedy_w(zt[v], zq[v], lam) : zt[v];
+        if (w > bw) {
+            bw = w;
+            best = v;
+        }
+    }
+    return best;
+}
+
+/* Greedy verification of sequences [b0, b1); same layouts as oracle_verify.
+ * Invalid input (token outside [0, V), lambda outside [0, 1] or NaN) gives
+ * n_accepted = -1 and all tokens -1. */
+void oracle_verify_greedy(const float *zt, const float *zq, const int32_t *tok, const float *lam,
+                          int64_t b0, int64_t b1, int32_t K, int64_t V, int32_t *out_tok,
+                          int32_t *out_n)
+{
+    for (int64_t b = b0; b < b1; ++b) {
+        const float *zt_b = zt + b * (int64_t)(K + 1) * V;
+        const float *zq_b = zq + b * (int64_t)K * V;
+        const int32_t *tk = tok + b * K;
+        int32_t *ot = out_tok + b * (K + 1);
+        double lambda = (double)lam[b];
+        int invalid = !(lambda >= 0.0 && lambda <= 1.0);
+        for (int32_t i = 0; i < K; ++i)
+            if (tk[i] < 0 || (int64_t)tk[i] >= V) invalid = 1;
+        if (invalid) {
+            for (int32_t i = 0; i <= K; ++i) ot[i] = -1;
+            out_n[b] = -1;
+            continue;
+        }
+        int32_t n = K;
+        int64_t token = -1;
+        for (int32_t i = 0; i < K; ++i) {
+            int64_t a = oracle_greedy_argmax(zt_b + (int64_t)i * V, zq_b + (int64_t)i * V, lam[b], V);
+            if (a != (int64_t)tk[i]) {
+                n = i;
+                token = a;
+                break;
+            }
+            ot[i] = tk[i];
+        }
+        if (n == K) token = oracle_greedy_argmax(zt_b + (int64_t)K * V, NULL, lam[b], V);
+        ot[n] = (int32_t)token;
+        for (int32_t i = n + 1; i <= K; ++i) ot[i] = -1;
+        out_n[b] = n;
+    }
 }

@@ -298,3 +298,102 @@ def test_seq_range_and_threads_do_not_change_results(oracle_mod):
     np.testing.assert_array_equal(a.tokens, b.tokens)
     np.testing.assert_array_equal(a.n_accepted, b.n_accepted)
     np.testing.assert_array_equal(a.ratio, b.ratio)
+
+
+# --------------------------------------------------------------------------- greedy
+# The greedy clause of the EAGLE explainer ("核心思路", step 3): a draft token
+# equal to the target's most likely token is accepted.  Read with RAPID's
+# mixture as: accept x_i iff x_i = argmax_v w_v, w = z_t + lambda (z_q - z_t);
+# emit the argmax at the first mismatch, the argmax of target row K if all match.
+
+def _np_greedy(zt, zq, tok, lam):
+    """Independent restatement for inputs on which every fp32 operation of w is
+    exact (small integers, dyadic lambda): w in float64, numpy's argmax (first
+    index among equal maxima)."""
+    B, K1, V = zt.shape
+    K = K1 - 1
+    out_t = np.full((B, K + 1), -1, np.int32)
+    out_n = np.zeros(B, np.int32)
+    for b in range(B):
+        n = K
+        for i in range(K):
+            w = zt[b, i].astype(np.float64) + lam[b] * (zq[b, i].astype(np.float64) -
+                                                         zt[b, i].astype(np.float64))
+            a = int(np.argmax(w))
+            if a != tok[b, i]:
+                n, t = i, a
+                break
+            out_t[b, i] = tok[b, i]
+        if n == K:
+            t = int(np.argmax(zt[b, K]))
+        out_t[b, n] = t
+        out_n[b] = n
+    return out_t, out_n
+
+
+def test_greedy_lambda_zero_is_the_target_argmax(oracle_mod):
+    rng = np.random.default_rng(7)
+    for V in (1, 2, 17, 1000):
+        zt = rng.normal(0, 3, V).astype(np.float32)
+        zq = rng.normal(0, 3, V).astype(np.float32)
+        assert oracle_mod.greedy_argmax(zt, zq, 0.0) == int(np.argmax(zt))
+        assert oracle_mod.greedy_argmax(zt, None, 0.7) == int(np.argmax(zt))
+
+
+def test_greedy_exact_mixtures_match_an_independent_restatement(oracle_mod):
+    rng = np.random.default_rng(11)
+    for lam in (0.0, 0.25, 0.5, 0.75, 1.0):
+        B, K, V = 40, 4, 9
+        zt = rng.integers(-8, 9, (B, K + 1, V)).astype(np.float32)
+        zq = rng.integers(-8, 9, (B, K, V)).astype(np.float32)
+        lams = np.full(B, lam, np.float32)
+        # half the drafts follow the mixture's argmax, so prefixes get accepted
+        tok = rng.integers(0, V, (B, K)).astype(np.int32)
+        for b in range(0, B, 2):
+            for i in range(K):
+                w = zt[b, i] + lam * (zq[b, i] - zt[b, i])
+                tok[b, i] = int(np.argmax(w))
+        res = oracle_mod.verify_greedy(zt, zq, tok, lams, threads=1)
+        et, en = _np_greedy(zt, zq, tok, lams)
+        np.testing.assert_array_equal(res.n_accepted, en)
+        np.testing.assert_array_equal(res.tokens, et)
+        assert (res.n_accepted[0::2] == K).all()
+
+
+def test_greedy_hand_case(oracle_mod):
+    # K = 3, V = 4, lambda = 0.5.  Rows (w = mean of the two logit rows):
+    #   i=0: zt [0,4,0,0], zq [0,2,0,0] -> w [0,3,0,0], argmax 1 = x_0: accept
+    #   i=1: zt [1,0,0,3], zq [5,0,0,1] -> w [3,0,0,2], argmax 0 = x_1: accept
+    #   i=2: zt [0,0,2,2], zq [0,0,0,2] -> w [0,0,1,2], argmax 3 != x_2 = 2: stop
+    # so n = 2 and the emitted token is 3.
+    zt = np.array([[[0, 4, 0, 0], [1, 0, 0, 3], [0, 0, 2, 2], [9, 0, 0, 0]]], np.float32)
+    zq = np.array([[[0, 2, 0, 0], [5, 0, 0, 1], [0, 0, 0, 2]]], np.float32)
+    tok = np.array([[1, 0, 2]], np.int32)
+    res = oracle_mod.verify_greedy(zt, zq, tok, np.array([0.5], np.float32))
+    assert res.n_accepted.tolist() == [2]
+    assert res.tokens.tolist() == [[1, 0, 3, -1]]
+    # with x_2 = 3 every draft matches: bonus = argmax of target row K = 0
+    res = oracle_mod.verify_greedy(zt, zq, np.array([[1, 0, 3]], np.int32),
+                                   np.array([0.5], np.float32))
+    assert res.n_accepted.tolist() == [3] and res.tokens.tolist() == [[1, 0, 3, 0]]
+
+
+def test_greedy_ties_masked_drafts_and_invalid_inputs(oracle_mod):
+    # equal maxima: the smallest index
+    assert oracle_mod.greedy_argmax(np.array([1, 7, 7, 7], np.float32), None, 0.0) == 1
+    # a draft logit of -inf removes the entry from the mixture
+    zt = np.array([0, 0, 0, 5], np.float32)
+    zq = np.array([0, 1, 0, -np.inf], np.float32)
+    assert oracle_mod.greedy_argmax(zt, zq, 0.25) == 1
+    # invalid token or lambda: everything -1
+    B, K, V = 3, 2, 5
+    zt = np.zeros((B, K + 1, V), np.float32)
+    zq = np.zeros((B, K, V), np.float32)
+    tok = np.zeros((B, K), np.int32)
+    tok[1, 1] = V
+    lam = np.array([0.1, 0.1, 1.5], np.float32)
+    res = oracle_mod.verify_greedy(zt, zq, tok, lam)
+    assert res.n_accepted.tolist() == [2, -1, -1]
+    assert (res.tokens[1:] == -1).all()
+    # all-equal rows: every argmax is 0, so drafts of 0 are all accepted
+    assert res.tokens[0].tolist() == [0, 0, 0]
