@@ -38,7 +38,6 @@ METRIC = "verified draft rows/sec (B·K) and achieved HBM GB/s vs GB300 peak, 1 
 UNIT = "rows/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rows_kernel_batched_v128256_f32.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_specv_gb300", "csrc", f)
                   for f in ("specv_rows.cu", "specv_device.cuh", "specv_block.cuh",
                             "specv_segments.cuh", "specv_internal.h")]
@@ -51,7 +50,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="specv", choices=["specv", "reference"])
     ap.add_argument("--config", type=int, default=4, choices=sorted(workloads.WORKLOADS))
-    ap.add_argument("--mode", default="prob", choices=["prob", "logit"])
+    ap.add_argument("--mode", default="prob", choices=["prob", "logit", "greedy"],
+                    help="sampling rule with the probability or logit mixture, or greedy")
     ap.add_argument("--B", type=int, default=None, help="override the batch size (profiling)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every step from the host instead of replaying a CUDA graph")
@@ -110,26 +110,28 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config_name):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source for this workload; else None."""
-    try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
-        return None
-    vals = {}
-    for line in text.splitlines():
-        if line.startswith("bench-key ") and ":" in line:
-            k, v = line[len("bench-key "):].split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
-        return None
-    if vals.get("workload") != config_name:
-        return None
-    try:
-        return int(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+def profiled_traffic(config_name, mode="prob"):
+    """DRAM bytes per launch from a committed ncu summary under profiles/ taken
+    on the current kernel source for this workload and mode; else None."""
+    import glob
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        try:
+            text = open(path).read()
+        except OSError:
+            continue
+        vals = {}
+        for line in text.splitlines():
+            if line.startswith("bench-key ") and ":" in line:
+                k, v = line[len("bench-key "):].split(":", 1)
+                vals[k.strip()] = v.strip()
+        if (vals.get("kernel_source_sha256_16") != kernel_source_hash()
+                or vals.get("workload") != config_name or vals.get("mode", "prob") != mode):
+            continue
+        try:
+            return int(vals["dram_bytes_per_launch"])
+        except (KeyError, ValueError):
+            continue
+    return None
 
 
 class ClockSampler:
@@ -194,6 +196,19 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
+MODES = {"prob": 0, "logit": 1, "greedy": 2}
+
+
+def oracle_step(xh, mode, threads):
+    """One oracle pass over a host batch (the sampling rule, or greedy)."""
+    import oracle
+    if mode == MODES["greedy"]:
+        oracle.verify_greedy(xh["target_logits"], xh["draft_logits"], xh["draft_tokens"],
+                             xh["lam"], threads=threads)
+    else:
+        oracle_step(xh, mode, threads)
+
+
 def cpu_baseline(w, mode, target_seconds, host_inputs=None):
     """The fp64 oracle, as it stands, on a bounded sample of the workload."""
     import oracle
@@ -208,9 +223,7 @@ def cpu_baseline(w, mode, target_seconds, host_inputs=None):
     passes = 0
     seqs = 0
     while True:
-        oracle.verify(xh["target_logits"], xh["draft_logits"], xh["draft_tokens"],
-                      xh["u_accept"], xh["u_resample"], xh["lam"], mode=mode,
-                      diagnostics=False, threads=threads)
+        oracle_step(xh, mode, threads)
         passes += 1
         seqs += B
         el = time.perf_counter() - t0
@@ -227,7 +240,7 @@ def run_reference(args):
     if rank != 0:
         return
     w = workloads.WORKLOADS[args.config]
-    mode = 0 if args.mode == "prob" else 1
+    mode = MODES[args.mode]
     import oracle
     oracle.build()
     nb = min(w.B, 8)
@@ -235,8 +248,7 @@ def run_reference(args):
     threads = os.cpu_count() or 1
 
     def step():
-        oracle.verify(xh["target_logits"], xh["draft_logits"], xh["draft_tokens"], xh["u_accept"],
-                      xh["u_resample"], xh["lam"], mode=mode, diagnostics=False, threads=threads)
+        oracle_step(xh, mode, threads)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -276,7 +288,7 @@ def main():
     w = workloads.WORKLOADS[args.config]
     if args.B:
         w = w.scaled(B=args.B, name=f"{w.name}-B{args.B}")
-    mode = 0 if args.mode == "prob" else 1
+    mode = MODES[args.mode]
     x = workloads.make_inputs(w, dev, seed_offset=rank)
     stream = torch.cuda.current_stream(dev)
     out_tok = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
@@ -403,13 +415,15 @@ def main():
     alg_bytes = w.roofline_bytes
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
-    traffic = profiled_traffic(w.name)
+    traffic = profiled_traffic(w.name, args.mode)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
                 "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                "kernel": PLAN_KERNEL_FUNCTION.get(plan["kernel"], plan["kernel"]),
+                "kernel": ("rows_greedy_kernel" if args.mode == "greedy" and
+                           plan["kernel"] == "rows-stream" else
+                           PLAN_KERNEL_FUNCTION.get(plan["kernel"], plan["kernel"])),
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "launch_ms_mean": kern_ms, "launch_ms_min": min(per_call_ms),
                 "timing": ("CUDA events around each replay of a CUDA graph holding one "

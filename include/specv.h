@@ -63,7 +63,14 @@ typedef enum {
 
 typedef enum {
     SPECV_PROB_MIX = 0,  /* p~ = (1-l) softmax(z_t) + l softmax(z_q)  (the displayed equation) */
-    SPECV_LOGIT_MIX = 1  /* p~ = softmax((1-l) z_t + l z_q)            (the pseudocode) */
+    SPECV_LOGIT_MIX = 1, /* p~ = softmax((1-l) z_t + l z_q)            (the pseudocode) */
+    SPECV_GREEDY = 2     /* greedy verification: x_i is accepted iff it is the argmax of
+                          * w = z_t + l (z_q - z_t) over row i (w = -inf where z_q = -inf; the
+                          * first maximum in index order); the argmax of row n is emitted at
+                          * the first mismatch n, the argmax of target row K when every draft
+                          * matches.  u_accept and u_resample are not read.  With l = 0 this
+                          * is the greedy clause of the EAGLE explainer ("核心思路", step 3):
+                          * keep a draft token iff it is the target's most likely token. */
 } specv_mode;
 
 typedef enum {
@@ -114,6 +121,7 @@ specv_status specv_verify(const void *target_logits, const void *draft_logits,
  *                                     mode), [.][i][1] of the draft row
  *                                     (undefined at i = K)
  * For a given input, out_tokens and out_n_accepted equal specv_verify's.
+ * SPECV_GREEDY computes no probabilities: it returns SPECV_ERR_UNSUPPORTED.
  */
 specv_status specv_verify_debug(const void *target_logits, const void *draft_logits,
                                 const int32_t *draft_tokens, const float *u_accept,

@@ -28,6 +28,7 @@ __all__ = ["SpecvError", "PROB_MIX", "LOGIT_MIX", "F32", "BF16", "load", "lib_pa
 
 PROB_MIX = 0
 LOGIT_MIX = 1
+GREEDY = 2
 F32 = 0
 BF16 = 1
 
@@ -142,8 +143,8 @@ def _args(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam, 
         out_n_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
     _require(out_tokens, "out_tokens", torch.int32, (B, K + 1), dev)
     _require(out_n_accepted, "out_n_accepted", torch.int32, (B,), dev)
-    if mode not in (PROB_MIX, LOGIT_MIX):
-        raise ValueError("mode must be PROB_MIX (0) or LOGIT_MIX (1)")
+    if mode not in (PROB_MIX, LOGIT_MIX, GREEDY):
+        raise ValueError("mode must be PROB_MIX (0), LOGIT_MIX (1) or GREEDY (2)")
     return B, K, V, dev, out_tokens, out_n_accepted
 
 
@@ -155,6 +156,10 @@ def _stream_ptr(stream, dev):
 def verify(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam,
            mode: int = PROB_MIX, out_tokens=None, out_n_accepted=None, stream=None):
     """One verify/accept step on the GPU.  Returns (out_tokens [B][K+1], out_n [B]).
+
+    mode: PROB_MIX or LOGIT_MIX (the sampling rule with the mixture p~), or
+    GREEDY (accept x_i iff it is the argmax of the mixed logits of row i; the
+    uniforms are not read).
 
     All tensors are CUDA, contiguous: target_logits [B][K+1][V] and
     draft_logits [B][K][V] (float32 or bfloat16), draft_tokens int32 [B][K],

@@ -184,7 +184,7 @@ int64_t round16(int64_t x) { return (x + 15) / 16 * 16; }
 bool sizes_ok(int64_t B, int32_t K, int32_t V, int dtype, int mode) {
   if (B < 1 || K < 1 || K > kMaxK || V < 1) return false;
   if (dtype != SPECV_F32 && dtype != SPECV_BF16) return false;
-  if (mode != SPECV_PROB_MIX && mode != SPECV_LOGIT_MIX) return false;
+  if (mode != SPECV_PROB_MIX && mode != SPECV_LOGIT_MIX && mode != SPECV_GREEDY) return false;
   const int64_t lim = (int64_t)1 << 62;
   if (B > lim / (K + 1) || B * (K + 1) > lim / V) return false;
   return true;
@@ -219,14 +219,18 @@ int variant_from_env() {
 //    96 KiB, doubled while the grid has < 4 CTAs per SM) stays within 2 CTAs
 //    per SM; otherwise the streaming row kernel runs.
 //  SPECV_CLUSTER_SIZE and SPECV_ROWS_VARIANT override the choices.
-specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, int64_t l2, bool aligned,
-                       Plan *p) {
+specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int sms, int64_t l2,
+                       bool aligned, Plan *p) {
   const int elem = dtype == SPECV_BF16 ? 2 : 4;
   std::memset(p, 0, sizeof(*p));
+  const bool greedy = mode == SPECV_GREEDY;
   const int64_t seq_bytes = (int64_t)(2 * K + 1) * V * elem + (int64_t)(K + 1) * 16;
-  if (V <= kTileMaxV && seq_bytes * kTileMinSeqs + 64 <= kTileSmemBudget) {
-    const int64_t data_bytes = (int64_t)(2 * K + 1) * V * elem;
-    const bool tma = aligned && ((int64_t)V * elem) % 16 == 0 && data_bytes <= kTmaTileStageBytes;
+  const int64_t data_bytes0 = (int64_t)(2 * K + 1) * V * elem;
+  const bool tma0 = aligned && ((int64_t)V * elem) % 16 == 0 && data_bytes0 <= kTmaTileStageBytes;
+  // greedy runs in the TMA tile kernel or the streaming row kernel only
+  if (V <= kTileMaxV && seq_bytes * kTileMinSeqs + 64 <= kTileSmemBudget && (!greedy || tma0)) {
+    const int64_t data_bytes = data_bytes0;
+    const bool tma = tma0;
     int ts;
     if (tma) {
       // two alternating tile buffers of <= 40 KiB each; one round of stage-A
@@ -259,6 +263,28 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int sms, int6
   const int64_t G = (V + vw - 1) / vw;
   const int env_S = cluster_from_env();
   const int env_var = variant_from_env();
+  if (greedy) {
+    // greedy needs no sampling pass: the streaming row kernel, one read of every logit
+    if (env_var != 0 && env_var != 1) return SPECV_ERR_UNSUPPORTED;
+    int S = env_S;
+    if (S == 0) {
+      S = 1;
+      while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
+             (P * S < 8LL * sms || 2 * row_bytes / S > 512 * 1024))
+        S *= 2;
+    }
+    while (S > 1 && P * S > INT32_MAX) S /= 2;
+    if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
+    p->kernel = 1;
+    p->cluster = S;
+    p->ctas = P * S;
+    p->num_groups = (int)G;
+    p->groups_per_slice = (int)((G + S - 1) / S);
+    specv::rows_segments(p->groups_per_slice, &p->seg_tiles, &p->segs_per_slice);
+    p->counters = B;
+    p->ws_bytes = round16(P * 16) + round16(B * 4);
+    return SPECV_OK;
+  }
   if (env_var == 5) {
     // sweep kernel: persistent CTAs, kSweepBlocksPerSM per SM; chunks of 1024
     // groups (16 KiB of a row), halved down to 256 while there are fewer than
@@ -358,7 +384,7 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
   const bool aligned = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
                        ((int64_t)V * elem % 16 == 0);
   Plan p;
-  if ((s = make_plan(B, K, V, dtype, sms, l2, aligned, &p)) != SPECV_OK) return s;
+  if ((s = make_plan(B, K, V, dtype, mode, sms, l2, aligned, &p)) != SPECV_OK) return s;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   cudaError_t e;
   if (p.kernel == 0 || p.kernel == 3) {
@@ -490,7 +516,9 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     a.num_groups = p.num_groups;
     a.seg_tiles = p.seg_tiles;
     a.segs_per_slice = p.segs_per_slice;
-    a.ws_seg = reinterpret_cast<float2 *>(static_cast<char *>(wdata) + round16(B * (K + 1) * 16));
+    a.ws_seg = mode == SPECV_GREEDY ? nullptr  // no sampling, no segment statistics
+                                    : reinterpret_cast<float2 *>(static_cast<char *>(wdata) +
+                                                                 round16(B * (K + 1) * 16));
     if (e == cudaSuccess) e = specv::rows_launch(a, bf16, mode, aligned, p.cluster, p.ctas, stream);
   }
   if (per_call) {
@@ -524,6 +552,7 @@ specv_status specv_verify_debug(const void *target_logits, const void *draft_log
                                 int32_t *out_tokens, int32_t *out_n_accepted,
                                 float *out_ptilde_at_x, float *out_q_at_x, float *out_lse,
                                 void *stream) {
+  if (mode == SPECV_GREEDY) return SPECV_ERR_UNSUPPORTED;  // no probabilities to report
   return run(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lambda, B, K, V,
              dtype, mode, out_tokens, out_n_accepted, out_ptilde_at_x, out_q_at_x, out_lse,
              stream);
@@ -546,7 +575,7 @@ specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, spec
     (void)cudaGetLastError();
   }
   Plan p;
-  specv_status s = make_plan(B, K, V, dtype, sms, l2, true, &p);
+  specv_status s = make_plan(B, K, V, dtype, mode, sms, l2, true, &p);
   if (s != SPECV_OK) return s;
   if (kernel) *kernel = p.kernel;
   if (cluster) *cluster = p.cluster;

@@ -15,7 +15,9 @@ namespace specv {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-enum : int { kProbMix = 0, kLogitMix = 1 };
+// Verification modes: the two mixtures of the sampling rule, and greedy
+// verification (accept x_i iff it is the argmax of the mixed logits).
+enum : int { kProbMix = 0, kLogitMix = 1, kGreedy = 2 };
 
 // 2^x and log2(x) on the special-function unit (PTX ex2/lg2, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
@@ -119,6 +121,32 @@ __device__ __forceinline__ void warp_merge_stats(float &m, float &s) {
     float s2 = __shfl_xor_sync(0xffffffffu, s, off);
     merge_stats(m, s, m2, s2);
   }
+}
+
+// Greedy: of two (value, index) candidates keep the larger value, and the
+// smaller index among equal values (the first maximum in index order).  An
+// empty candidate is (-inf, INT_MAX).
+__device__ __forceinline__ void argmax_merge(float &w, int &idx, float w2, int idx2) {
+  if (w2 > w || (w2 == w && idx2 < idx)) {
+    w = w2;
+    idx = idx2;
+  }
+}
+
+// Butterfly argmax across a warp; every lane ends with the result.
+__device__ __forceinline__ void warp_argmax(float &w, int &idx) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float w2 = __shfl_xor_sync(0xffffffffu, w, off);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
+    argmax_merge(w, idx, w2, i2);
+  }
+}
+
+// Greedy score of one entry: the mixed logit z_t + l (z_q - z_t), -inf where
+// the draft logit is -inf (the draft rules the entry out).
+__device__ __forceinline__ float greedy_score(float zt, float zq, float lam) {
+  return zq == -INFINITY ? -INFINITY : mix_logit(zt, zq, lam);
 }
 
 // Statistics of one position: A = source row of p~ (target row in

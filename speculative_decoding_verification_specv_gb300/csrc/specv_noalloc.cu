@@ -96,7 +96,8 @@ extern "C" specv_status specv_verify_noalloc(const void *target_logits, const vo
     return SPECV_ERR_INVALID_ARG;
   if (B < 1 || K < 1 || K > 4096 || V < 1) return SPECV_ERR_INVALID_ARG;
   if (dtype != SPECV_F32 && dtype != SPECV_BF16) return SPECV_ERR_INVALID_ARG;
-  if (mode != SPECV_PROB_MIX && mode != SPECV_LOGIT_MIX) return SPECV_ERR_INVALID_ARG;
+  if (mode != SPECV_PROB_MIX && mode != SPECV_LOGIT_MIX && mode != SPECV_GREEDY)
+    return SPECV_ERR_INVALID_ARG;
   if (B > kNoAllocMaxSequences || B * (K + 1) > kNoAllocMaxPositions) return SPECV_ERR_INVALID_ARG;
   int dev = 0;
   specv_status st = setup(&dev);

@@ -35,6 +35,8 @@
 //
 // No thread ever waits on another cluster: the counter only decides which
 // cluster does phase 2, and the only barriers are hardware cluster barriers.
+#include <climits>
+
 #include <cooperative_groups.h>
 
 #include "specv_block.cuh"
@@ -417,8 +419,135 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   if (lane == 0) a.out_tokens[b * (K + 1) + bc.n] = tok;
 }
 
+// Greedy verification with the same decomposition (one cluster per position,
+// rank r streams slice r): each rank finds the argmax of the mixed logits
+// w = z_t + lambda (z_q - z_t) over its slice (target row K alone at the bonus
+// position), the first maximum in index order; rank 0 merges the S candidates
+// in rank order and publishes (max, index).  The last cluster of the sequence
+// accepts x_i iff it is the argmax of row i, stops at the first mismatch and
+// emits that argmax there, or the argmax of target row K when every draft
+// matches.  There is no sampling pass: each logit is read once.
+template <typename T, bool ALIGNED>
+__global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
+  constexpr int VW = Elem<T>::kPerVec;
+  __shared__ RowsShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int S = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int64_t p = (int64_t)blockIdx.x / S;
+  const int K = a.K, V = a.V;
+  const int64_t b = p / (K + 1);
+  const int i = (int)(p - b * (K + 1));
+  const bool pair = i < K;
+  const T *tgt = static_cast<const T *>(a.target);
+  const T *dft = static_cast<const T *>(a.draft);
+  const T *rowA = tgt + (b * (K + 1) + i) * (int64_t)V;
+  const T *rowB = dft + (b * K + (pair ? i : 0)) * (int64_t)V;
+  const int g_lo = rank * a.groups_per_slice;
+  const int g_hi = min(a.num_groups, g_lo + a.groups_per_slice);
+  const float lam = a.lam[b];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  float best = -INFINITY;
+  int bidx = INT_MAX;
+  for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += kNT * kUnroll) {
+    uint4 za[kUnroll], zb[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int g = g0 + u * kNT;
+      if (g < g_hi) {
+        za[u] = load_group<T, ALIGNED>(rowA, g, V);
+        if (pair) zb[u] = load_group<T, ALIGNED>(rowB, g, V);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int g = g0 + u * kNT;
+      if (g < g_hi) {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          const int idx = g * VW + e;
+          if (ALIGNED || idx < V) {
+            const float zt = Elem<T>::get(za[u], e);
+            const float w = pair ? greedy_score(zt, Elem<T>::get(zb[u], e), lam) : zt;
+            argmax_merge(best, bidx, w, idx);
+          }
+        }
+      }
+    }
+  }
+  warp_argmax(best, bidx);
+  if (lane == 0) {
+    sh.bs.red[warp][0] = best;
+    sh.bs.red[warp][1] = __int_as_float(bidx);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = -INFINITY;
+    int ix = INT_MAX;
+    for (int w = 0; w < kNW; ++w) argmax_merge(m, ix, sh.bs.red[w][0], __float_as_int(sh.bs.red[w][1]));
+    sh.part[0] = m;
+    sh.part[1] = __int_as_float(ix);
+  }
+  cluster.sync();  // candidates of every rank are visible
+  if (rank == 0 && threadIdx.x == 0) {
+    float m = -INFINITY;
+    int ix = INT_MAX;
+    for (int r = 0; r < S; ++r) {
+      const float *pr = cluster.map_shared_rank(sh.part, r);
+      argmax_merge(m, ix, pr[0], __float_as_int(pr[1]));
+    }
+    a.ws_stats[p] = make_float4(m, __int_as_float(ix), 0.0f, 0.0f);
+    __threadfence();
+    const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
+    const int last = prev == (unsigned)K;
+    if (last) {
+      __threadfence();
+      a.ws_count[b] = 0;
+    }
+    for (int r = 0; r < S; ++r) *cluster.map_shared_rank(&sh.last, r) = last;
+  }
+  cluster.sync();  // sh.last is set in every rank; rank 0 is done reading candidates
+  if (!sh.last || rank != 0 || warp != 0) return;
+
+  // the sequence: accept while x_i is the argmax of row i
+  __threadfence();
+  const bool lam_ok = lambda_valid(lam);
+  bool lane_ok = true;
+  int n = K;
+  for (int i0 = 0; i0 < K; i0 += 32) {
+    const int j = i0 + lane;
+    bool rejected = false;
+    if (j < K) {
+      const int x = a.tokens[b * K + j];
+      const bool tok_ok = x >= 0 && x < V;
+      lane_ok = lane_ok && tok_ok;
+      if (tok_ok && lam_ok) rejected = __float_as_int(__ldcg(&a.ws_stats[b * (K + 1) + j]).y) != x;
+    }
+    const unsigned rej = __ballot_sync(0xffffffffu, rejected);
+    if (rej != 0u && n == K) n = i0 + __ffs(rej) - 1;
+  }
+  const bool valid = lam_ok && __all_sync(0xffffffffu, lane_ok);  // every lane votes
+  for (int j = lane; j <= K; j += 32) {
+    int out = -1;
+    if (valid && j < n) out = a.tokens[b * K + j];
+    if (valid && j == n) out = __float_as_int(__ldcg(&a.ws_stats[b * (K + 1) + n]).y);
+    a.out_tokens[b * (K + 1) + j] = out;
+  }
+  if (lane == 0) a.out_n[b] = valid ? n : -1;
+}
+
+template <typename T, int MODE, bool ALIGNED>
+constexpr void (*row_kernel_of())(RowArgs) {
+  if constexpr (MODE == kGreedy)
+    return rows_greedy_kernel<T, ALIGNED>;
+  else
+    return rows_kernel<T, MODE, ALIGNED>;
+}
+
 template <typename T, int MODE, bool ALIGNED>
 cudaError_t launch_one(const RowArgs &a, int S, int64_t grid, cudaStream_t stream) {
+  void (*kern)(RowArgs) = row_kernel_of<T, MODE, ALIGNED>();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kNT, 1, 1);
@@ -431,12 +560,12 @@ cudaError_t launch_one(const RowArgs &a, int S, int64_t grid, cudaStream_t strea
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, rows_kernel<T, MODE, ALIGNED>, a);
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <typename T, int MODE, bool ALIGNED>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(rows_kernel<T, MODE, ALIGNED>,
+  return cudaFuncSetAttribute(row_kernel_of<T, MODE, ALIGNED>(),
                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
@@ -455,12 +584,23 @@ cudaError_t rows_prepare() {
   SPECV_PREP(uint16_t, kProbMix, false)
   SPECV_PREP(uint16_t, kLogitMix, true)
   SPECV_PREP(uint16_t, kLogitMix, false)
+  SPECV_PREP(float, kGreedy, true)
+  SPECV_PREP(float, kGreedy, false)
+  SPECV_PREP(uint16_t, kGreedy, true)
+  SPECV_PREP(uint16_t, kGreedy, false)
 #undef SPECV_PREP
   return e;
 }
 
 cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
                         int64_t grid, cudaStream_t stream) {
+  if (mode == kGreedy) {
+    if (dtype_bf16)
+      return aligned ? launch_one<uint16_t, kGreedy, true>(a, S, grid, stream)
+                     : launch_one<uint16_t, kGreedy, false>(a, S, grid, stream);
+    return aligned ? launch_one<float, kGreedy, true>(a, S, grid, stream)
+                   : launch_one<float, kGreedy, false>(a, S, grid, stream);
+  }
   if (dtype_bf16) {
     if (mode == kProbMix)
       return aligned ? launch_one<uint16_t, kProbMix, true>(a, S, grid, stream)

@@ -18,6 +18,8 @@
 //            owning a contiguous run of 16-byte groups of the row.
 // The per-sequence scalars (tokens, uniforms, lambda) are loaded into
 // registers before stage A so their latency overlaps it.  No scratch memory.
+#include <climits>
+
 #include "specv_block.cuh"
 #include "specv_device.cuh"
 #include "specv_internal.h"
@@ -77,8 +79,33 @@ __device__ __forceinline__ float2 row_stats(const uint4 *ra, const uint4 *rb, in
   return make_float2(m, s);
 }
 
+// Greedy: (max, index) of the mixed logits w of one staged row (target row
+// alone at the bonus position), the first maximum in index order; the index
+// is returned in the bits of the second component.
+template <typename T>
+__device__ __forceinline__ float2 row_argmax(const uint4 *ra, const uint4 *rb, int G, int rot,
+                                             bool mixed, float lam) {
+  constexpr int VW = Elem<T>::kPerVec;
+  float best = -INFINITY;
+  int bidx = INT_MAX;
+  int g = rot;
+  for (int k = 0; k < G; ++k) {
+    const uint4 va = ra[g];
+    const uint4 vb = mixed ? rb[g] : va;
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      const float zt = Elem<T>::get(va, e);
+      const float w = mixed ? greedy_score(zt, Elem<T>::get(vb, e), lam) : zt;
+      argmax_merge(best, bidx, w, g * VW + e);
+    }
+    g = (g + 1 == G) ? 0 : g + 1;
+  }
+  return make_float2(best, __int_as_float(bidx));
+}
+
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
+  constexpr bool GREEDY = MODE == kGreedy;  // argmax per row; no draft-row tasks, no sampling
   constexpr int VW = Elem<T>::kPerVec;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
@@ -120,7 +147,7 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
 
   // This thread's first stage-A task of a full tile (the same in every full
   // tile): computed once, so full tiles need no integer division per row.
-  const int fA = TS * (K + 1), fB = TS * K;
+  const int fA = TS * (K + 1), fB = GREEDY ? 0 : TS * K;
   const bool has_task = (int)threadIdx.x < fA + fB;
   int t_pos = 0, t_rd = 0, t_rot = 0, t_s = 0;
   bool t_isA = false, t_mixed = false;
@@ -172,13 +199,15 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
 
     // stage A: one thread per row; A-rows (p~ source) of all positions first,
     // then the draft rows
-    const int nA = ok ? nseq * (K + 1) : 0, nB = ok ? nseq * K : 0;
+    const int nA = ok ? nseq * (K + 1) : 0, nB = (ok && !GREEDY) ? nseq * K : 0;
     const bool full = nseq == TS;
     if (ok && full && has_task) {
       const uint4 *rt = reinterpret_cast<const uint4 *>(st_t + (int64_t)t_pos * V);
       const uint4 *rd = reinterpret_cast<const uint4 *>(st_d + t_rd);
       float2 r;
-      if (t_isA)
+      if constexpr (GREEDY)
+        r = row_argmax<T>(rt, rd, G, t_rot, t_mixed, a.lam[b0 + t_s]);
+      else if (t_isA)
         r = row_stats<T, MODE>(rt, rd, G, t_rot, t_mixed, a.lam[b0 + t_s]);
       else
         r = row_stats<T, kProbMix>(rd, rd, G, t_rot, false, 0.0f);
@@ -203,7 +232,9 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
       const uint4 *rt = reinterpret_cast<const uint4 *>(st_t + (int64_t)pos * V);
       const uint4 *rd = reinterpret_cast<const uint4 *>(st_d + ((int64_t)s * K + (i < K ? i : 0)) * V);
       float2 r;
-      if (isA)
+      if constexpr (GREEDY)
+        r = row_argmax<T>(rt, rd, G, rot, i < K, a.lam[b0 + s]);
+      else if (isA)
         r = row_stats<T, MODE>(rt, rd, G, rot, i < K, a.lam[b0 + s]);
       else
         r = row_stats<T, kProbMix>(rd, rd, G, rot, false, 0.0f);
@@ -221,6 +252,36 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
       if (mine) {
         for (int j = gl; j <= K; j += kLanes) a.out_tokens[b * (K + 1) + j] = -1;
         if (gl == 0) a.out_n[b] = -2;
+      }
+    } else if constexpr (GREEDY) {
+      // accept while x_j is the argmax of row j; emit the argmax at the first
+      // mismatch (or of row K when every draft matches)
+      const int sl = mine ? sq : 0;
+      const bool lam_ok = lambda_valid(p_lam);
+      bool lane_ok = true;
+      int n = K;
+      for (int i0 = 0; i0 < K; i0 += kLanes) {
+        const int j = i0 + gl;
+        bool rejected = false;
+        if (j < K) {
+          const int x = i0 == 0 ? p_tok : a.tokens[b * K + j];
+          const bool tok_ok = x >= 0 && x < V;
+          lane_ok = lane_ok && tok_ok;
+          if (tok_ok && lam_ok) rejected = __float_as_int(st_s[(sl * (K + 1) + j) * 4 + 1]) != x;
+        }
+        const unsigned rej = (__ballot_sync(0xffffffffu, rejected) & gmask) >> gsh;
+        if (rej != 0u && n == K) n = i0 + __ffs(rej) - 1;
+      }
+      const unsigned bad_tok = __ballot_sync(0xffffffffu, !lane_ok) & gmask;
+      const bool valid = lam_ok && bad_tok == 0u;
+      if (mine) {
+        for (int j = gl; j <= K; j += kLanes) {
+          int out = -1;
+          if (valid && j < n) out = j == gl ? p_tok : a.tokens[b * K + j];
+          if (valid && j == n) out = __float_as_int(st_s[(sl * (K + 1) + n) * 4 + 1]);
+          a.out_tokens[b * (K + 1) + j] = out;
+        }
+        if (gl == 0) a.out_n[b] = valid ? n : -1;
       }
     } else {
       const int sl = mine ? sq : 0;  // staged sequence slot (a valid one for idle groups)
@@ -380,10 +441,14 @@ cudaError_t tile_tma_prepare(int max_smem_bytes) {
   if ((r = prep<float, kLogitMix>(max_smem_bytes)) != cudaSuccess) e = r;
   if ((r = prep<uint16_t, kProbMix>(max_smem_bytes)) != cudaSuccess) e = r;
   if ((r = prep<uint16_t, kLogitMix>(max_smem_bytes)) != cudaSuccess) e = r;
+  if ((r = prep<float, kGreedy>(max_smem_bytes)) != cudaSuccess) e = r;
+  if ((r = prep<uint16_t, kGreedy>(max_smem_bytes)) != cudaSuccess) e = r;
   return e;
 }
 
 int tile_tma_blocks_per_sm(int dtype_bf16, int mode, int smem_bytes) {
+  if (mode == kGreedy)
+    return dtype_bf16 ? occ<uint16_t, kGreedy>(smem_bytes) : occ<float, kGreedy>(smem_bytes);
   if (dtype_bf16) return mode == kProbMix ? occ<uint16_t, kProbMix>(smem_bytes)
                                           : occ<uint16_t, kLogitMix>(smem_bytes);
   return mode == kProbMix ? occ<float, kProbMix>(smem_bytes) : occ<float, kLogitMix>(smem_bytes);
@@ -392,6 +457,13 @@ int tile_tma_blocks_per_sm(int dtype_bf16, int mode, int smem_bytes) {
 cudaError_t tile_tma_launch(const TileArgs &a, int dtype_bf16, int mode, int64_t grid,
                             int smem_bytes, cudaStream_t stream) {
   const dim3 g((unsigned)grid), blk(kNT);
+  if (mode == kGreedy) {
+    if (dtype_bf16)
+      tile_tma_kernel<uint16_t, kGreedy><<<g, blk, smem_bytes, stream>>>(a);
+    else
+      tile_tma_kernel<float, kGreedy><<<g, blk, smem_bytes, stream>>>(a);
+    return cudaGetLastError();
+  }
   if (dtype_bf16) {
     if (mode == kProbMix)
       tile_tma_kernel<uint16_t, kProbMix><<<g, blk, smem_bytes, stream>>>(a);

@@ -62,7 +62,7 @@ def test_null_pointers_are_rejected(lib, null):
 
 @pytest.mark.parametrize("kw", [dict(B=0), dict(B=-5), dict(K=0), dict(K=-1), dict(K=4097),
                                 dict(V=0), dict(V=-7), dict(dtype=2), dict(dtype=-1),
-                                dict(mode=2), dict(B=1 << 40, K=4000, V=1 << 30)])
+                                dict(mode=3), dict(mode=-1), dict(B=1 << 40, K=4000, V=1 << 30)])
 def test_bad_sizes_and_enums_are_rejected(lib, kw):
     assert _call(**kw) == 1
 
@@ -107,3 +107,23 @@ def test_plan_sweep_variant(lib, monkeypatch):
     assert p1["kernel"] == "rows-sweep" and p1["ctas"] == 5
     with pytest.raises(specv.SpecvError):
         specv.plan(3, 2, 1001, specv.F32)
+
+
+def test_plan_greedy_mode(lib, monkeypatch):
+    """Greedy verification (mode 2) never samples: short aligned rows use the
+    TMA tile kernel, everything else the streaming row kernel with the position
+    statistics and counters only; the variants that exist for the sampler are
+    refused; the debug entry point (probabilities) is refused too."""
+    assert specv.plan(1_000_000, 4, 32, specv.F32, specv.GREEDY)["kernel"] == "tile-tma"
+    p4 = specv.plan(256, 8, 128256, specv.F32, specv.GREEDY)
+    assert p4["kernel"] == "rows-stream" and p4["workspace_bytes"] == 256 * 9 * 16 + 256 * 4
+    # short rows off 16-byte boundaries: the streaming row kernel, not the generic tile
+    assert specv.plan(5, 3, 33, specv.F32, specv.GREEDY)["kernel"] == "rows-stream"
+    for v in ("resident", "spec", "sweep"):
+        monkeypatch.setenv("SPECV_ROWS_VARIANT", v)
+        with pytest.raises(specv.SpecvError):
+            specv.plan(256, 8, 128256, specv.F32, specv.GREEDY)
+    monkeypatch.delenv("SPECV_ROWS_VARIANT")
+    st = specv.raw_call("specv_verify_debug", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 0, 2,
+                        FAKE, FAKE, None, None, None, None)
+    assert st == 2
