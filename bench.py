@@ -57,6 +57,9 @@ def parse():
                     help="launch every step from the host instead of replaying a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stats", action="store_true",
+                    help="time specv_acceptance_rates (exact acceptance probabilities of every "
+                         "drafted position) instead of the verify step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args()
@@ -271,8 +274,72 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_stats(args):
+    """One line for the acceptance-probability kernel: drafted positions per
+    second, and its HBM bandwidth with the algorithmic bytes 2K*B*V*s (every
+    drafted row pair read once; the second pass is meant to hit L2)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import speculative_decoding_verification_specv_gb300 as specv
+    specv.load(build_if_missing=True)
+    w = workloads.WORKLOADS[args.config]
+    if args.B:
+        w = w.scaled(B=args.B, name=f"{w.name}-B{args.B}")
+    mode = MODES[args.mode]
+    x = workloads.make_inputs(w, dev)
+    out = torch.empty((w.B, w.K), dtype=torch.float32, device=dev)
+
+    def launch():
+        specv.acceptance_rates(x["target_logits"], x["draft_logits"], x["lam"], mode=mode,
+                               out=out, stream=torch.cuda.current_stream(dev))
+    launch()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        launch()
+    stream = torch.cuda.current_stream(dev)
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    elem = 2 if w.dtype == "bf16" else 4
+    alg = 2 * w.K * w.B * w.V * elem
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev) if alg < 2 * l2 else None
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(0) as clk:
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(float(i))
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    peak, kind = measured_peak()
+    achieved = alg / (ms / 1e3) / 1e9
+    line = {
+        "metric": "drafted positions/s with exact acceptance probability (specv_acceptance_rates)",
+        "value": w.B * w.K / (ms / 1e3), "unit": "positions/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "f32" if w.dtype == "f32" else "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "mode": args.mode,
+                   "l2": "flushed before every step" if flush is not None else "inputs > L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": alg, "kernel": "alpha_kernel",
+                     "peak_source": kind},
+        "clocks": clk.summary(), "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.stats:
+        run_stats(args)
+        return
     if args.impl == "reference":
         run_reference(args)
         return

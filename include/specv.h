@@ -159,6 +159,46 @@ specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, spec
                         int64_t *workspace_bytes);
 
 /*
+ * specv_acceptance_rates -- the exact acceptance probability of every drafted
+ * position, for host policies such as specv_choose_k.  A draft token x ~ q is
+ * accepted with probability min(1, p~(x)/q(x)) (the RAPID explainer's
+ * "3) 候选验证机制" loop), so position i of sequence b is accepted with
+ *   alpha[b][i] = sum_v min(p~_v, q_v)  (1 minus the total variation distance),
+ * the per-position rate on which the speculative-decoding explainer builds
+ * its expected-token count ("加速效果分析").
+ *   target_logits [B][K+1][V], draft_logits [B][K][V], lambda [B]: as for
+ *   specv_verify (rows K of the target are not read); mode PROB_MIX or
+ *   LOGIT_MIX (SPECV_GREEDY: SPECV_ERR_UNSUPPORTED);
+ *   out_alpha [B][K] fp32, device; NaN where lambda is outside [0, 1].
+ * Two passes over every drafted row pair (statistics, then the overlap sum),
+ * the second mostly from L2; no scratch, no allocation; asynchronous on
+ * `stream`.  Host argument errors as for specv_verify.
+ */
+specv_status specv_acceptance_rates(const void *target_logits, const void *draft_logits,
+                                    const float *lambda, int64_t B, int32_t K, int32_t V,
+                                    specv_dtype dtype, specv_mode mode, float *out_alpha,
+                                    void *stream);
+
+/*
+ * specv_choose_k -- host-only draft-length policy (no device work): the K in
+ * [k_min, k_max] that maximises the expected tokens of one step per unit of
+ * step cost,
+ *   tokens(K) = 1 + alpha + ... + alpha^K   (accepted prefix + the final token,
+ *                                             positions accepted independently
+ *                                             with probability alpha),
+ *   cost(K)   = cost_verify_fixed + K * (cost_draft + cost_verify_per_token),
+ * the smallest such K on ties.  This is the adaptive draft length of the EAGLE
+ * explainer ("4. 草稿长度和接受率的权衡": lengthen the draft when recent
+ * acceptance is high, shorten it when low) made concrete with the expected
+ * token count of the speculative-decoding explainer ("加速效果分析").
+ * alpha would typically be a running mean of specv_acceptance_rates.
+ * Returns -1 for alpha outside [0, 1] or NaN, k_min < 1, k_max < k_min or
+ * > 4096, a negative cost, or a step cost of zero.
+ */
+int32_t specv_choose_k(double alpha, double cost_draft, double cost_verify_fixed,
+                       double cost_verify_per_token, int32_t k_min, int32_t k_max);
+
+/*
  * specv_verify_noalloc -- specv_verify for callers that cannot let a library
  * allocate device memory while they run: an engine that hands all of HBM to
  * its own pools up front, a decode loop where an allocation could stall or

@@ -33,7 +33,8 @@ F32 = 0
 BF16 = 1
 
 EXPORTED_SYMBOLS = ("specv_verify", "specv_verify_debug", "specv_plan", "specv_status_string",
-                    "specv_last_cuda_error", "specv_version")
+                    "specv_last_cuda_error", "specv_version", "specv_verify_noalloc",
+                    "specv_acceptance_rates", "specv_choose_k")
 
 _STATUS = {0: "SPECV_OK", 1: "SPECV_ERR_INVALID_ARG", 2: "SPECV_ERR_UNSUPPORTED",
            3: "SPECV_ERR_CUDA", 4: "SPECV_ERR_NO_MEMORY"}
@@ -85,6 +86,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.specv_last_cuda_error.restype = ctypes.c_char_p
         lib.specv_version.argtypes = []
         lib.specv_version.restype = ctypes.c_int32
+        lib.specv_acceptance_rates.argtypes = [vp, vp, vp, i64, i32, i32, ctypes.c_int,
+                                               ctypes.c_int, vp, vp]
+        lib.specv_acceptance_rates.restype = ctypes.c_int
+        dbl = ctypes.c_double
+        lib.specv_choose_k.argtypes = [dbl, dbl, dbl, dbl, i32, i32]
+        lib.specv_choose_k.restype = ctypes.c_int32
         _ = f32p
         _lib = lib
         return lib
@@ -192,6 +199,79 @@ def verify_debug(target_logits, draft_logits, draft_tokens, u_accept, u_resample
         px.data_ptr(), qx.data_ptr(), lse.data_ptr(), _stream_ptr(stream, dev))
     _check(st, "specv_verify_debug")
     return dict(tokens=out_tokens, n_accepted=out_n, ptilde_x=px, q_x=qx, lse=lse)
+
+
+def acceptance_rates(target_logits, draft_logits, lam, mode: int = PROB_MIX, out=None,
+                     stream=None):
+    """Exact acceptance probability alpha [B][K] = sum_v min(p~_v, q_v) of every
+    drafted position (float32, on the logits' device; NaN where lam is outside
+    [0, 1]).  Same tensor rules as verify(); mode PROB_MIX or LOGIT_MIX."""
+    zt, zq = target_logits, draft_logits
+    if zt.dim() != 3:
+        raise ValueError("target_logits must be [B][K+1][V]")
+    B, K1, V = zt.shape
+    K = K1 - 1
+    dev = zt.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors (the kernels run only on the GPU)")
+    _require(zt, "target_logits", None, (B, K + 1, V), dev)
+    _require(zq, "draft_logits", zt.dtype, (B, K, V), dev)
+    _require(lam, "lam", torch.float32, (B,), dev)
+    if mode not in (PROB_MIX, LOGIT_MIX):
+        raise ValueError("mode must be PROB_MIX (0) or LOGIT_MIX (1)")
+    if out is None:
+        out = torch.empty((B, K), dtype=torch.float32, device=dev)
+    _require(out, "out", torch.float32, (B, K), dev)
+    st = load().specv_acceptance_rates(zt.data_ptr(), zq.data_ptr(), lam.data_ptr(), B, K, V,
+                                       _dtype_code(zt), int(mode), out.data_ptr(),
+                                       _stream_ptr(stream, dev))
+    _check(st, "specv_acceptance_rates")
+    return out
+
+
+def choose_k(alpha: float, cost_draft: float, cost_verify_fixed: float,
+             cost_verify_per_token: float = 0.0, k_min: int = 1, k_max: int = 16) -> int:
+    """Draft length maximising (1 + a + ... + a^K) / (fixed + K (draft + per-token))."""
+    k = load().specv_choose_k(float(alpha), float(cost_draft), float(cost_verify_fixed),
+                              float(cost_verify_per_token), int(k_min), int(k_max))
+    if k < 0:
+        raise ValueError("specv_choose_k: alpha must be in [0, 1], costs >= 0 with a positive "
+                         "step cost, and 1 <= k_min <= k_max <= 4096")
+    return int(k)
+
+
+class AdaptiveK:
+    """Host-side draft-length controller: a running mean of the acceptance
+    probabilities of recent steps (from acceptance_rates, or any estimate)
+    and the K that specv_choose_k picks for it."""
+
+    def __init__(self, cost_draft: float, cost_verify_fixed: float,
+                 cost_verify_per_token: float = 0.0, k_min: int = 1, k_max: int = 16,
+                 k_init: int = 4, decay: float = 0.9):
+        if not 0.0 <= decay < 1.0:
+            raise ValueError("decay must be in [0, 1)")
+        self.costs = (cost_draft, cost_verify_fixed, cost_verify_per_token)
+        self.k_min, self.k_max, self.decay = k_min, k_max, decay
+        self.alpha = None
+        self.k = int(min(max(k_init, k_min), k_max))
+
+    def update(self, alpha) -> int:
+        """Fold in one step's acceptance probabilities (a tensor, array or
+        float; NaN entries ignored) and return the draft length to use next."""
+        if isinstance(alpha, torch.Tensor):
+            a = alpha.detach().float()
+            a = a[~torch.isnan(a)]
+            if a.numel() == 0:
+                return self.k
+            mean = float(a.mean())
+        else:
+            mean = float(alpha)
+            if mean != mean:
+                return self.k
+        mean = min(max(mean, 0.0), 1.0)
+        self.alpha = mean if self.alpha is None else self.decay * self.alpha + (1 - self.decay) * mean
+        self.k = choose_k(self.alpha, *self.costs, k_min=self.k_min, k_max=self.k_max)
+        return self.k
 
 
 # specv_plan's kernel codes

@@ -150,7 +150,8 @@ specv_status ensure_device(int *sms_out, int64_t *l2_out) {
         (e = specv::resident_prepare(kResidentMaxSmem)) != cudaSuccess ||
         (e = specv::tile_prepare(kTileSmemBudget)) != cudaSuccess ||
         (e = specv::tile_tma_prepare(2 * kTmaTileStageBytes + 16 * 1024)) != cudaSuccess ||
-        (e = specv::sweep_prepare(specv::sweep_smem_bytes(1024))) != cudaSuccess) {
+        (e = specv::sweep_prepare(specv::sweep_smem_bytes(1024))) != cudaSuccess ||
+        (e = specv::alpha_prepare()) != cudaSuccess) {
       note_cuda_error(e);
       return SPECV_ERR_CUDA;
     }
@@ -582,6 +583,83 @@ specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, spec
   if (ctas) *ctas = p.ctas;
   if (workspace_bytes) *workspace_bytes = p.ws_bytes;
   return SPECV_OK;
+}
+
+specv_status specv_acceptance_rates(const void *target_logits, const void *draft_logits,
+                                    const float *lambda, int64_t B, int32_t K, int32_t V,
+                                    specv_dtype dtype, specv_mode mode, float *out_alpha,
+                                    void *stream) {
+  if (!target_logits || !draft_logits || !lambda || !out_alpha) return SPECV_ERR_INVALID_ARG;
+  if (!sizes_ok(B, K, V, dtype, mode)) return SPECV_ERR_INVALID_ARG;
+  if (mode == SPECV_GREEDY) return SPECV_ERR_UNSUPPORTED;  // greedy has no p~ to overlap with q
+  int sms = kDefaultSMs;
+  int64_t l2 = kDefaultL2;
+  specv_status s = ensure_device(&sms, &l2);
+  if (s != SPECV_OK) return s;
+  const int bf16 = dtype == SPECV_BF16;
+  const int elem = bf16 ? 2 : 4;
+  const int vw = 16 / elem;
+  const int64_t row_bytes = (int64_t)V * elem;
+  const int64_t G = (V + vw - 1) / vw;
+  const int64_t Q = B * K;  // drafted positions
+  const bool aligned = ((uintptr_t)target_logits % 16 == 0) && ((uintptr_t)draft_logits % 16 == 0) &&
+                       (row_bytes % 16 == 0);
+  // Cluster size: the smallest power of two (<= 16) that keeps one CTA's
+  // slice of the pair within 128 KiB (so the second pass finds it in L2) and
+  // gives >= 8 CTAs per SM, without going under 4 KiB of a row per CTA.
+  int S = cluster_from_env();
+  if (S == 0) {
+    S = 1;
+    while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
+           (Q * S < 8LL * sms || 2 * row_bytes / S > 128 * 1024))
+      S *= 2;
+  }
+  while (S > 1 && Q * S > INT32_MAX) S /= 2;
+  if (Q * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
+  specv::AlphaArgs a;
+  a.target = target_logits;
+  a.draft = draft_logits;
+  a.lam = lambda;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.out_alpha = out_alpha;
+  a.num_groups = (int)G;
+  a.groups_per_slice = (int)((G + S - 1) / S);
+  const cudaError_t e = specv::alpha_launch(a, bf16, mode, aligned, S, Q * S,
+                                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    return SPECV_ERR_CUDA;
+  }
+  return SPECV_OK;
+}
+
+int32_t specv_choose_k(double alpha, double cost_draft, double cost_verify_fixed,
+                       double cost_verify_per_token, int32_t k_min, int32_t k_max) {
+  if (!(alpha >= 0.0 && alpha <= 1.0)) return -1;
+  if (k_min < 1 || k_max < k_min || k_max > kMaxK) return -1;
+  if (!(cost_draft >= 0.0) || !(cost_verify_fixed >= 0.0) || !(cost_verify_per_token >= 0.0))
+    return -1;
+  int32_t best_k = k_min;
+  double best = -1.0;
+  for (int32_t k = k_min; k <= k_max; ++k) {
+    // expected tokens of one step: 1 + a + ... + a^k (the accepted prefix and
+    // the token drawn at its end), over the step's cost
+    double tokens = 0.0, ak = 1.0;
+    for (int32_t j = 0; j <= k; ++j) {
+      tokens += ak;
+      ak *= alpha;
+    }
+    const double cost = cost_verify_fixed + (double)k * (cost_draft + cost_verify_per_token);
+    if (!(cost > 0.0)) return -1;
+    const double rate = tokens / cost;
+    if (rate > best) {
+      best = rate;
+      best_k = k;
+    }
+  }
+  return best_k;
 }
 
 const char *specv_status_string(specv_status status) {

@@ -150,6 +150,23 @@ cudaError_t resident_prepare(int max_smem);
 cudaError_t resident_launch(const ResArgs &a, int dtype_bf16, int mode, bool staged, int S,
                             int64_t grid, int smem, cudaStream_t stream);
 
+// Arguments of the acceptance-probability kernel (one cluster per drafted
+// position b*K + i).
+struct AlphaArgs {
+  const void *target;        // [B][K+1][V]
+  const void *draft;         // [B][K][V]
+  const float *lam;          // [B]
+  int64_t B;
+  int K;
+  int V;
+  float *out_alpha;          // [B][K]
+  int groups_per_slice;      // 16-byte groups of a row handled by one CTA
+  int num_groups;            // ceil(V / elements per 16 bytes)
+};
+cudaError_t alpha_prepare();
+cudaError_t alpha_launch(const AlphaArgs &a, int dtype_bf16, int mode, bool aligned, int S,
+                         int64_t grid, cudaStream_t stream);
+
 // Dynamic shared memory of the sweep kernel for chunks of chunk_groups groups.
 inline int sweep_smem_bytes(int chunk_groups) { return kSweepStages * 2 * chunk_groups * 16; }
 cudaError_t sweep_prepare(int max_smem_bytes);
