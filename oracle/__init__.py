@@ -81,6 +81,10 @@ def _load():
         lib.oracle_greedy_argmax.restype = i64
         lib.oracle_verify_greedy.argtypes = [fp, fp, ip, fp, i64, i64, ctypes.c_int32, i64, ip, ip]
         lib.oracle_verify_greedy.restype = None
+        lib.oracle_verify_tree.argtypes = [fp, fp, ip, ip, ip, fp, fp, fp, i64, i64,
+                                           ctypes.c_int32, ctypes.c_int32, i64, ctypes.c_int, ip,
+                                           ip, ip, dp, dp]
+        lib.oracle_verify_tree.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -265,3 +269,54 @@ def verify_greedy(target_logits, draft_logits, draft_tokens, lam,
         with ThreadPoolExecutor(max_workers=nthreads) as ex:
             list(ex.map(lambda j: run(int(edges[j]), int(edges[j + 1])), range(nthreads)))
     return Result(tokens=out_tok, n_accepted=out_n, threads=nthreads)
+
+
+def verify_tree(target_logits, draft_logits, parent, draft_row, tokens, u_accept, u_resample,
+                lam, mode: int = PROB_MIX, threads: int | None = None) -> Result:
+    """Tree verification (the reading in specv_oracle.c).  target_logits
+    [B][N+1][V], draft_logits [B][M][V], parent/draft_row/tokens int32 [B][N+1],
+    u_accept fp32 [B][N+1], u_resample and lam fp32 [B].  Returns tokens and
+    path [B][N+1], n_accepted [B], accept_margin and cdf_margin [B]."""
+    zt = _f32(target_logits)
+    zq = _f32(draft_logits)
+    par, drow, tok = _i32(parent), _i32(draft_row), _i32(tokens)
+    ua = _f32(u_accept)
+    ur = _f32(u_resample).reshape(-1)
+    lm = _f32(lam).reshape(-1)
+    B, N1, V = zt.shape
+    N = N1 - 1
+    if zq.ndim != 3 or zq.shape[0] != B or (zq.shape[1] > 0 and zq.shape[2] != V):
+        raise ValueError("draft_logits must be [B][M][V]")
+    M = zq.shape[1]
+    if M == 0:
+        zq = np.zeros((B, 1, V), np.float32)
+    for a in (par, drow, tok, ua):
+        assert a.shape == (B, N + 1)
+    out_tok = np.full((B, N + 1), -2, np.int32)
+    out_path = np.full((B, N + 1), -2, np.int32)
+    out_n = np.full((B,), -2, np.int32)
+    am = np.full((B,), np.nan, np.float64)
+    cm = np.full((B,), np.nan, np.float64)
+    lib = _load()
+    dp_ = ctypes.c_double
+
+    def run(lo, hi):
+        rc = lib.oracle_verify_tree(
+            _ptr(zt, ctypes.c_float), _ptr(zq, ctypes.c_float), _ptr(par, ctypes.c_int32),
+            _ptr(drow, ctypes.c_int32), _ptr(tok, ctypes.c_int32), _ptr(ua, ctypes.c_float),
+            _ptr(ur, ctypes.c_float), _ptr(lm, ctypes.c_float), lo, hi, N, M, V, int(mode),
+            _ptr(out_tok, ctypes.c_int32), _ptr(out_path, ctypes.c_int32),
+            _ptr(out_n, ctypes.c_int32), _ptr(am, dp_), _ptr(cm, dp_))
+        if rc != 0:
+            raise MemoryError("oracle_verify_tree could not allocate its row buffers")
+
+    nthreads = threads if threads is not None else (os.cpu_count() or 1)
+    nthreads = max(1, min(nthreads, B))
+    if nthreads == 1:
+        run(0, B)
+    else:
+        edges = np.linspace(0, B, nthreads + 1).astype(np.int64)
+        with ThreadPoolExecutor(max_workers=nthreads) as ex:
+            list(ex.map(lambda j: run(int(edges[j]), int(edges[j + 1])), range(nthreads)))
+    return Result(tokens=out_tok, path=out_path, n_accepted=out_n, accept_margin=am,
+                  cdf_margin=cm, threads=nthreads)

@@ -389,3 +389,150 @@ void oracle_verify_greedy(const float *zt, const float *zq, const int32_t *tok, 
         out_n[b] = n;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Tree verification.
+ *
+ * Reading (the pages describe draft trees -- the speculative-decoding
+ * explainer's "Tree Speculation" section: several candidate branches per
+ * position, verified at once, so that another branch can be accepted when one
+ * is rejected; the EAGLE explainer's "3. 验证阶段树形attention" and EAGLE-2's
+ * dynamic draft tree -- but give no multi-branch acceptance rule).  A sequence's tree has nodes 0..N; node 0 is the root (the
+ * last accepted position), node j >= 1 has parent[j] in [0, j) and token x_j.
+ * Every node u has a target row z_t[u] (the target's next-token logits after
+ * the path root..u) and, when draft_row[u] >= 0, the draft row
+ * z_q[draft_row[u]] from which u's children were drawn, independently.  The
+ * enhanced target at u is p~_u = mix(p_t[u], q_u) (the chosen mixture mode),
+ * or p_t[u] when u has no draft row.  The walk, from u = 0:
+ *   - p = p~_u; for each child c of u in index order: accept x_c iff
+ *     u_accept[c] < min(1, p(x_c) / q_u(x_c)); on acceptance emit x_c and
+ *     continue the walk at c; on rejection p = normalize(max(0, p - q_u));
+ *   - if every child is rejected, draw the token from p (inverse CDF with
+ *     u_resample); if u has no children, draw the bonus token from p~_u;
+ *   - if a residual has zero mass (round-off only), draw from p~_u instead.
+ * With one child per node (parent[j] = j - 1) this is the chain loop of
+ * oracle_verify.  Invalid input: parent[0] != -1, parent[j] outside [0, j),
+ * draft_row outside [-1, M), a node with children but no draft row, a token
+ * outside [0, V), lambda outside [0, 1] -> n = -1, all outputs -1.
+ */
+static int tree_valid(const int32_t *par, const int32_t *drow, const int32_t *tok, int32_t N,
+                      int32_t M, int64_t V, double lambda)
+{
+    if (!(lambda >= 0.0 && lambda <= 1.0)) return 0;
+    if (par[0] != -1) return 0;
+    for (int32_t j = 0; j <= N; ++j) {
+        if (drow[j] < -1 || drow[j] >= M) return 0;
+        if (j == 0) continue;
+        if (par[j] < 0 || par[j] >= j) return 0;
+        if (tok[j] < 0 || (int64_t)tok[j] >= V) return 0;
+        if (drow[par[j]] < 0) return 0;
+    }
+    return 1;
+}
+
+/* p~ and q of node u (q left untouched when u has no draft row). */
+static void tree_rows(const float *zt_seq, const float *zq_seq, const int32_t *drow, int64_t V,
+                      int32_t u, double lambda, int mode, double *zt, double *zq, double *pt,
+                      double *pq, double *ptilde)
+{
+    const float *rt = zt_seq + (int64_t)u * V;
+    for (int64_t v = 0; v < V; ++v) zt[v] = (double)rt[v];
+    if (drow[u] < 0) {
+        oracle_softmax(zt, V, ptilde);
+        return;
+    }
+    const float *rq = zq_seq + (int64_t)drow[u] * V;
+    for (int64_t v = 0; v < V; ++v) zq[v] = (double)rq[v];
+    oracle_softmax(zq, V, pq);
+    if (mode == 0) {
+        oracle_softmax(zt, V, pt);
+        oracle_mix_prob(pt, pq, lambda, V, ptilde);
+    } else {
+        oracle_mix_logit(zt, zq, lambda, V, ptilde);
+    }
+}
+
+/* Tree verification of sequences [b0, b1).
+ *   zt  [B][N+1][V]   zq [B][M][V]   parent, draft_row, tok, ua: [B][N+1]
+ *   ur, lam: [B]; out_tok, out_path: [B][N+1]; out_n: [B]
+ *   accept_margin, cdf_margin: [B] or NULL (as for oracle_verify).
+ * Returns 0, or -1 on allocation failure. */
+int oracle_verify_tree(const float *zt, const float *zq, const int32_t *parent,
+                       const int32_t *draft_row, const int32_t *tok, const float *ua,
+                       const float *ur, const float *lam, int64_t b0, int64_t b1, int32_t N,
+                       int32_t M, int64_t V, int mode, int32_t *out_tok, int32_t *out_path,
+                       int32_t *out_n, double *accept_margin, double *cdf_margin)
+{
+    double *buf = (double *)malloc((size_t)6 * (size_t)V * sizeof(double));
+    if (!buf) return -1;
+    double *zt_d = buf, *zq_d = buf + V, *pt = buf + 2 * V, *pq = buf + 3 * V;
+    double *ptilde = buf + 4 * V, *p = buf + 5 * V;
+    for (int64_t b = b0; b < b1; ++b) {
+        const float *zt_b = zt + b * (int64_t)(N + 1) * V;
+        const float *zq_b = zq + b * (int64_t)M * V;
+        const int32_t *par = parent + b * (N + 1), *drow = draft_row + b * (N + 1);
+        const int32_t *tk = tok + b * (N + 1);
+        const float *u_b = ua + b * (N + 1);
+        int32_t *ot = out_tok + b * (N + 1), *op = out_path + b * (N + 1);
+        for (int32_t j = 0; j <= N; ++j) ot[j] = op[j] = -1;
+        double am = INFINITY, cm = INFINITY;
+        double lambda = (double)lam[b];
+        if (!tree_valid(par, drow, tk, N, M, V, lambda)) {
+            out_n[b] = -1;
+            if (accept_margin) accept_margin[b] = am;
+            if (cdf_margin) cdf_margin[b] = cm;
+            continue;
+        }
+        int32_t u = 0, n = 0;
+        int64_t token = -1;
+        for (;;) {
+            tree_rows(zt_b, zq_b, drow, V, u, lambda, mode, zt_d, zq_d, pt, pq, ptilde);
+            for (int64_t v = 0; v < V; ++v) p[v] = ptilde[v];
+            int32_t next = -1, any_child = 0, exhausted = 0;
+            for (int32_t c = u + 1; c <= N; ++c) {
+                if (par[c] != u) continue;
+                any_child = 1;
+                double px = p[tk[c]], qx = pq[tk[c]];
+                double accept_prob = qx > 0.0 ? (px / qx < 1.0 ? px / qx : 1.0)
+                                              : (px > 0.0 ? 1.0 : 0.0);
+                double dm = fabs((double)u_b[c] - accept_prob);
+                if (dm < am) am = dm;
+                if ((double)u_b[c] < accept_prob) {
+                    next = c;
+                    break;
+                }
+                /* rejected: p = normalize(max(0, p - q_u)) */
+                double z = 0.0;
+                for (int64_t v = 0; v < V; ++v) {
+                    double r = p[v] - pq[v];
+                    p[v] = r > 0.0 ? r : 0.0;
+                    z += p[v];
+                }
+                if (!(z > 0.0)) {
+                    exhausted = 1;
+                    break;
+                }
+                for (int64_t v = 0; v < V; ++v) p[v] /= z;
+            }
+            if (next >= 0) {
+                ot[n] = tk[next];
+                op[n] = next;
+                ++n;
+                u = next;
+                continue;
+            }
+            int fb = 0;
+            /* no child: bonus from p~_u; every child rejected: the residual p;
+             * a residual of zero mass: p~_u */
+            const double *w = (!any_child || exhausted) ? ptilde : p;
+            token = oracle_sample_inverse_cdf(w, V, (double)ur[b], &fb, &cm);
+            break;
+        }
+        ot[n] = (int32_t)token;
+        out_n[b] = n;
+        if (accept_margin) accept_margin[b] = am;
+        if (cdf_margin) cdf_margin[b] = cm;
+    }
+    free(buf);
+    return 0;
+}
