@@ -40,7 +40,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_specv_gb300", "csrc", f)
                   for f in ("specv_rows.cu", "specv_device.cuh", "specv_block.cuh",
-                            "specv_segments.cuh", "specv_internal.h")]
+                            "specv_segments.cuh", "specv_stream.cuh", "specv_internal.h")]
 
 
 def parse():

@@ -159,6 +159,51 @@ specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, spec
                         int64_t *workspace_bytes);
 
 /*
+ * specv_verify_tree -- the verify/accept step for a tree of drafted tokens per
+ * sequence (the speculative-decoding explainer's "Tree Speculation": several
+ * candidate branches per position verified at once, so that another branch can
+ * be accepted when one is rejected).  Rule (a reading; the pages give none for
+ * several branches): node 0 is the root; the children of node u were drawn
+ * independently from the draft distribution q_u; starting at the root with
+ * p = p~_u, u's children are tested in index order, x_c accepted iff
+ * u_accept[c] < min(1, p(x_c)/q_u(x_c)); a rejection replaces p by
+ * normalize(max(0, p - q_u)); an acceptance moves on to c.  When every child is
+ * rejected the token is drawn from p (inverse CDF with u_resample[b]); at a
+ * node without children, the bonus token from p~_u.  p~_u mixes the target row
+ * of u with q_u by `mode`, or is the target softmax when u has no draft row.
+ * A chain (parent[j] = j - 1) is specv_verify.
+ *   target_logits [B][N+1][V]  target row of every node (row 0: the root)
+ *   draft_logits  [B][M][V]    draft rows (may be NULL when M == 0)
+ *   parent        [B][N+1]     int32: -1 at node 0, parent[j] in [0, j) else
+ *   draft_row     [B][N+1]     int32: the draft row (in [0, M)) u's children
+ *                              were drawn from, -1 for a node without children
+ *   tokens        [B][N+1]     int32: token of node j (entry 0 unused)
+ *   u_accept      [B][N+1]     fp32: uniform of node j's test (entry 0 unused)
+ *   u_resample [B], lambda [B] fp32
+ *   mode          SPECV_PROB_MIX or SPECV_LOGIT_MIX
+ *   out_tokens    [B][N+1]     accepted tokens along the path, then the drawn
+ *                              token, then -1
+ *   out_path      [B][N+1]     the accepted nodes in order, then -1
+ *   out_n         [B]          number of accepted nodes; -1 for an invalid
+ *                              sequence (bad parent, draft_row or token, a node
+ *                              with children but no draft row, lambda outside
+ *                              [0, 1]): then every output entry is -1
+ * Every node's rows are read once for their statistics; the walk reads the
+ * rows of the nodes it visits again (one pass per rejection, one for the final
+ * draw).  Scratch as specv_verify's streaming kernel (16 bytes per node + one
+ * counter per sequence).  Host argument errors (null pointers, B < 1, N < 0 or
+ * > 4096, M < 0, V < 1, overflowing sizes, unknown enums) return
+ * SPECV_ERR_INVALID_ARG and launch nothing.
+ */
+specv_status specv_verify_tree(const void *target_logits, const void *draft_logits,
+                               const int32_t *parent, const int32_t *draft_row,
+                               const int32_t *tokens, const float *u_accept,
+                               const float *u_resample, const float *lambda, int64_t B, int32_t N,
+                               int32_t M, int32_t V, specv_dtype dtype, specv_mode mode,
+                               int32_t *out_tokens, int32_t *out_path, int32_t *out_n,
+                               void *stream);
+
+/*
  * specv_acceptance_rates -- the exact acceptance probability of every drafted
  * position, for host policies such as specv_choose_k.  A draft token x ~ q is
  * accepted with probability min(1, p~(x)/q(x)) (the RAPID explainer's

@@ -34,7 +34,7 @@ BF16 = 1
 
 EXPORTED_SYMBOLS = ("specv_verify", "specv_verify_debug", "specv_plan", "specv_status_string",
                     "specv_last_cuda_error", "specv_version", "specv_verify_noalloc",
-                    "specv_acceptance_rates", "specv_choose_k")
+                    "specv_acceptance_rates", "specv_choose_k", "specv_verify_tree")
 
 _STATUS = {0: "SPECV_OK", 1: "SPECV_ERR_INVALID_ARG", 2: "SPECV_ERR_UNSUPPORTED",
            3: "SPECV_ERR_CUDA", 4: "SPECV_ERR_NO_MEMORY"}
@@ -89,6 +89,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.specv_acceptance_rates.argtypes = [vp, vp, vp, i64, i32, i32, ctypes.c_int,
                                                ctypes.c_int, vp, vp]
         lib.specv_acceptance_rates.restype = ctypes.c_int
+        lib.specv_verify_tree.argtypes = [vp] * 8 + [i64, i32, i32, i32, ctypes.c_int,
+                                                     ctypes.c_int, vp, vp, vp, vp]
+        lib.specv_verify_tree.restype = ctypes.c_int
         dbl = ctypes.c_double
         lib.specv_choose_k.argtypes = [dbl, dbl, dbl, dbl, i32, i32]
         lib.specv_choose_k.restype = ctypes.c_int32
@@ -199,6 +202,41 @@ def verify_debug(target_logits, draft_logits, draft_tokens, u_accept, u_resample
         px.data_ptr(), qx.data_ptr(), lse.data_ptr(), _stream_ptr(stream, dev))
     _check(st, "specv_verify_debug")
     return dict(tokens=out_tokens, n_accepted=out_n, ptilde_x=px, q_x=qx, lse=lse)
+
+
+def verify_tree(target_logits, draft_logits, parent, draft_row, tokens, u_accept, u_resample,
+                lam, mode: int = PROB_MIX, stream=None):
+    """Tree verification on the GPU.  target_logits [B][N+1][V], draft_logits
+    [B][M][V] (same dtype; M may be 0), parent/draft_row/tokens int32 [B][N+1],
+    u_accept float32 [B][N+1], u_resample and lam float32 [B].  Returns
+    (out_tokens [B][N+1], out_path [B][N+1], out_n [B])."""
+    zt, zq = target_logits, draft_logits
+    if zt.dim() != 3 or zq.dim() != 3:
+        raise ValueError("target_logits must be [B][N+1][V] and draft_logits [B][M][V]")
+    B, N1, V = zt.shape
+    M = zq.shape[1]
+    dev = zt.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors (the verify step runs only on the GPU)")
+    _require(zt, "target_logits", None, (B, N1, V), dev)
+    _require(zq, "draft_logits", zt.dtype, (B, M, V), dev)
+    for name, t in (("parent", parent), ("draft_row", draft_row), ("tokens", tokens)):
+        _require(t, name, torch.int32, (B, N1), dev)
+    _require(u_accept, "u_accept", torch.float32, (B, N1), dev)
+    _require(u_resample, "u_resample", torch.float32, (B,), dev)
+    _require(lam, "lam", torch.float32, (B,), dev)
+    if mode not in (PROB_MIX, LOGIT_MIX):
+        raise ValueError("mode must be PROB_MIX (0) or LOGIT_MIX (1)")
+    out_tokens = torch.empty((B, N1), dtype=torch.int32, device=dev)
+    out_path = torch.empty((B, N1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    st = load().specv_verify_tree(
+        zt.data_ptr(), zq.data_ptr() if M > 0 else None, parent.data_ptr(), draft_row.data_ptr(),
+        tokens.data_ptr(), u_accept.data_ptr(), u_resample.data_ptr(), lam.data_ptr(), B, N1 - 1,
+        M, V, _dtype_code(zt), int(mode), out_tokens.data_ptr(), out_path.data_ptr(),
+        out_n.data_ptr(), _stream_ptr(stream, dev))
+    _check(st, "specv_verify_tree")
+    return out_tokens, out_path, out_n
 
 
 def acceptance_rates(target_logits, draft_logits, lam, mode: int = PROB_MIX, out=None,

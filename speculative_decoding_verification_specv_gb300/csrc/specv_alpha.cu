@@ -23,6 +23,7 @@
 #include "specv_device.cuh"
 #include "specv_internal.h"
 #include "specv_segments.cuh"
+#include "specv_stream.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -68,54 +69,7 @@ __global__ void __launch_bounds__(kNT, 4) alpha_kernel(AlphaArgs a) {
 
   // ------------------------------------------------ pass 1: row statistics
   float mA = -INFINITY, sA = 0.0f, mB = -INFINITY, sB = 0.0f;
-  for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += kNT * kUnroll) {
-    uint4 za[kUnroll], zb[kUnroll];
-    bool ok[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int g = g0 + u * kNT;
-      ok[u] = g < g_hi;
-      if (ok[u]) {
-        za[u] = load_group<T, ALIGNED>(rowA, g, V);
-        zb[u] = load_group<T, ALIGNED>(rowB, g, V);
-      }
-    }
-    auto a_val = [&](int u, int e) -> float {
-      const float zt = Elem<T>::get(za[u], e);
-      if (MODE == kLogitMix) {
-        const float zq = Elem<T>::get(zb[u], e);
-        return zq == -INFINITY ? -INFINITY : mix_logit(zt, zq, lam);
-      }
-      return zt;
-    };
-    float bmA = -INFINITY, bmB = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (ok[u]) {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) {
-          bmA = fmaxf(bmA, a_val(u, e));
-          bmB = fmaxf(bmB, Elem<T>::get(zb[u], e));
-        }
-      }
-    if (bmA > mA) {
-      sA = __fmul_rn(sA, exp_shifted(mA, bmA));
-      mA = bmA;
-    }
-    if (bmB > mB) {
-      sB = __fmul_rn(sB, exp_shifted(mB, bmB));
-      mB = bmB;
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (ok[u]) {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) {
-          sA = __fadd_rn(sA, exp_shifted(a_val(u, e), mA));
-          sB = __fadd_rn(sB, exp_shifted(Elem<T>::get(zb[u], e), mB));
-        }
-      }
-  }
+  slice_stats<T, MODE, ALIGNED, kNT, kUnroll>(rowA, rowB, true, lam, V, g_lo, g_hi, mA, sA, mB, sB);
   block_merge_stats<kNT>(sh.bs, mA, sA, mB, sB);
   if (threadIdx.x == 0) {
     sh.part[0] = mA;

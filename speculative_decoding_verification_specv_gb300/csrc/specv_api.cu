@@ -151,7 +151,8 @@ specv_status ensure_device(int *sms_out, int64_t *l2_out) {
         (e = specv::tile_prepare(kTileSmemBudget)) != cudaSuccess ||
         (e = specv::tile_tma_prepare(2 * kTmaTileStageBytes + 16 * 1024)) != cudaSuccess ||
         (e = specv::sweep_prepare(specv::sweep_smem_bytes(1024))) != cudaSuccess ||
-        (e = specv::alpha_prepare()) != cudaSuccess) {
+        (e = specv::alpha_prepare()) != cudaSuccess ||
+        (e = specv::tree_prepare()) != cudaSuccess) {
       note_cuda_error(e);
       return SPECV_ERR_CUDA;
     }
@@ -582,6 +583,97 @@ specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, spec
   if (cluster) *cluster = p.cluster;
   if (ctas) *ctas = p.ctas;
   if (workspace_bytes) *workspace_bytes = p.ws_bytes;
+  return SPECV_OK;
+}
+
+specv_status specv_verify_tree(const void *target_logits, const void *draft_logits,
+                               const int32_t *parent, const int32_t *draft_row,
+                               const int32_t *tokens, const float *u_accept,
+                               const float *u_resample, const float *lambda, int64_t B, int32_t N,
+                               int32_t M, int32_t V, specv_dtype dtype, specv_mode mode,
+                               int32_t *out_tokens, int32_t *out_path, int32_t *out_n,
+                               void *stream) {
+  if (!target_logits || !parent || !draft_row || !tokens || !u_accept || !u_resample || !lambda ||
+      !out_tokens || !out_path || !out_n || (M > 0 && !draft_logits))
+    return SPECV_ERR_INVALID_ARG;
+  if (B < 1 || N < 0 || N > kMaxK || M < 0 || V < 1) return SPECV_ERR_INVALID_ARG;
+  if (dtype != SPECV_F32 && dtype != SPECV_BF16) return SPECV_ERR_INVALID_ARG;
+  if (mode != SPECV_PROB_MIX && mode != SPECV_LOGIT_MIX) return SPECV_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t)1 << 62;
+  if (B > lim / (N + 1) || B * (N + 1) > lim / V || (M > 0 && B * (int64_t)M > lim / V))
+    return SPECV_ERR_INVALID_ARG;
+  int sms = kDefaultSMs;
+  int64_t l2 = kDefaultL2;
+  specv_status st = ensure_device(&sms, &l2);
+  if (st != SPECV_OK) return st;
+  const int bf16 = dtype == SPECV_BF16;
+  const int elem = bf16 ? 2 : 4;
+  const int vw = 16 / elem;
+  const int64_t row_bytes = (int64_t)V * elem;
+  const int64_t G = (V + vw - 1) / vw;
+  const int64_t P = B * (N + 1);
+  const bool aligned = ((uintptr_t)target_logits % 16 == 0) &&
+                       (M == 0 || (uintptr_t)draft_logits % 16 == 0) && (row_bytes % 16 == 0);
+  // cluster size: the streaming row kernel's rule
+  int S = cluster_from_env();
+  if (S == 0) {
+    S = 1;
+    while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
+           (P * S < 8LL * sms || 2 * row_bytes / S > 512 * 1024))
+      S *= 2;
+  }
+  while (S > 1 && P * S > INT32_MAX) S /= 2;
+  if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  (void)cudaGetDevice(&dev);
+  const size_t data_bytes = (size_t)round16(P * 16);
+  unsigned *cnt = nullptr;
+  void *wdata = nullptr;
+  void *ws = nullptr;
+  cudaError_t e = cudaSuccess;
+  const bool per_call = !cached_workspace(dev, s, B, data_bytes, &cnt, &wdata);
+  if (per_call) {
+    e = cudaMallocAsync(&ws, data_bytes + (size_t)round16(B * 4), s);
+    if (e != cudaSuccess) {
+      note_cuda_error(e);
+      (void)cudaGetLastError();
+      return SPECV_ERR_NO_MEMORY;
+    }
+    cnt = static_cast<unsigned *>(ws);
+    wdata = static_cast<char *>(ws) + round16(B * 4);
+    e = cudaMemsetAsync(cnt, 0, (size_t)B * sizeof(unsigned), s);
+  }
+  specv::TreeArgs a;
+  a.target = target_logits;
+  a.draft = draft_logits ? draft_logits : target_logits;  // M == 0: never read
+  a.parent = parent;
+  a.draft_row = draft_row;
+  a.tokens = tokens;
+  a.u_accept = u_accept;
+  a.u_resample = u_resample;
+  a.lam = lambda;
+  a.B = B;
+  a.N = N;
+  a.M = M;
+  a.V = V;
+  a.out_tokens = out_tokens;
+  a.out_path = out_path;
+  a.out_n = out_n;
+  a.ws_stats = static_cast<float4 *>(wdata);
+  a.ws_count = cnt;
+  a.num_groups = (int)G;
+  a.groups_per_slice = (int)((G + S - 1) / S);
+  specv::rows_segments(a.groups_per_slice, &a.seg_tiles, &a.segs_per_slice);
+  if (e == cudaSuccess) e = specv::tree_launch(a, bf16, mode, aligned, S, P * S, s);
+  if (per_call) {
+    const cudaError_t ef = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = ef;
+  }
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    return SPECV_ERR_CUDA;
+  }
   return SPECV_OK;
 }
 

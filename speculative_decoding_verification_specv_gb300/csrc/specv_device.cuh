@@ -192,11 +192,15 @@ __device__ __forceinline__ bool lambda_valid(float lam) { return lam >= 0.0f && 
 //                probability mode (p~ - q = (1 - l)(p_t - q) there), exactly
 //                in logit mode;
 //   kWBonus    : p~_v at the bonus position = target softmax of row K;
-//   kWMixture  : p~_v itself (fallback when the residual has zero mass).
-enum : int { kWResidual = 0, kWBonus = 1, kWMixture = 2 };
+//   kWMixture  : p~_v itself (fallback when the residual has zero mass);
+//   kWResidualC: max(0, p~_v - c q_v), the residual after rejections of
+//                several independent drafts of one node (tree verification;
+//                c = 1 is the residual of the first rejection).
+enum : int { kWResidual = 0, kWBonus = 1, kWMixture = 2, kWResidualC = 3 };
 
 struct SampleParams {
   float mA, invSA, mB, invSB, lam;
+  float c;  // threshold of kWResidualC
 };
 
 // Sampler parameters of a position from its statistics.  The reciprocals are
@@ -210,6 +214,7 @@ __device__ __forceinline__ SampleParams make_sample_params(float mA, float sA, f
   p.mB = mB;
   p.invSB = __fdividef(1.0f, sB);
   p.lam = lam;
+  p.c = 1.0f;
   return p;
 }
 
@@ -220,9 +225,10 @@ __device__ __forceinline__ float sample_weight(int mode, int kind, const SampleP
   float pa = __fmul_rn(exp_shifted(a, p.mA), p.invSA);
   float pq = __fmul_rn(exp_shifted(zq, p.mB), p.invSB);
   if (kind == kWResidual) return fmaxf(0.0f, __fsub_rn(pa, pq));
-  // kWMixture
-  if (mode == kProbMix) return __fmaf_rn(p.lam, pq, __fmul_rn(__fsub_rn(1.0f, p.lam), pa));
-  return pa;
+  const float pt = (mode == kProbMix) ? __fmaf_rn(p.lam, pq, __fmul_rn(__fsub_rn(1.0f, p.lam), pa))
+                                      : pa;
+  if (kind == kWResidualC) return fmaxf(0.0f, __fsub_rn(pt, __fmul_rn(p.c, pq)));
+  return pt;  // kWMixture
 }
 
 // sample_weight without branches on `kind`: every candidate is computed and

@@ -167,6 +167,34 @@ cudaError_t alpha_prepare();
 cudaError_t alpha_launch(const AlphaArgs &a, int dtype_bf16, int mode, bool aligned, int S,
                          int64_t grid, cudaStream_t stream);
 
+// Arguments of the tree-verification kernel (one cluster per tree node b*(N+1) + u).
+struct TreeArgs {
+  const void *target;        // [B][N+1][V]: target row of every node
+  const void *draft;         // [B][M][V]: draft rows
+  const int32_t *parent;     // [B][N+1]: parent node (-1 at the root)
+  const int32_t *draft_row;  // [B][N+1]: draft row a node's children were drawn from, or -1
+  const int32_t *tokens;     // [B][N+1]: token of every node (entry 0 unused)
+  const float *u_accept;     // [B][N+1]: uniform of every node's test (entry 0 unused)
+  const float *u_resample;   // [B]
+  const float *lam;          // [B]
+  int64_t B;
+  int N;
+  int M;
+  int V;
+  int32_t *out_tokens;       // [B][N+1]
+  int32_t *out_path;         // [B][N+1]
+  int32_t *out_n;            // [B]
+  float4 *ws_stats;          // scratch [B][N+1]: (mA, sA, mB, sB) of every node
+  unsigned *ws_count;        // scratch [B]: nodes published so far (zero at entry, left zero)
+  int groups_per_slice;
+  int num_groups;
+  int seg_tiles;
+  int segs_per_slice;
+};
+cudaError_t tree_prepare();
+cudaError_t tree_launch(const TreeArgs &a, int dtype_bf16, int mode, bool aligned, int S,
+                        int64_t grid, cudaStream_t stream);
+
 // Dynamic shared memory of the sweep kernel for chunks of chunk_groups groups.
 inline int sweep_smem_bytes(int chunk_groups) { return kSweepStages * 2 * chunk_groups * 16; }
 cudaError_t sweep_prepare(int max_smem_bytes);

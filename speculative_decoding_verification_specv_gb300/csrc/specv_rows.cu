@@ -43,6 +43,7 @@
 #include "specv_device.cuh"
 #include "specv_internal.h"
 #include "specv_segments.cuh"
+#include "specv_stream.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -210,56 +211,8 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
     bonus_segment_stats<T, ALIGNED>(rowA, V, g_lo, g_hi, seg_groups, nseg,
                                     a.ws_seg + (b * S + rank) * (int64_t)nseg, mA, sA);
   else
-  for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += kNT * kUnroll) {
-    uint4 za[kUnroll], zb[kUnroll];
-    bool ok[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int g = g0 + u * kNT;
-      ok[u] = g < g_hi;
-      if (ok[u]) {
-        za[u] = load_group<T, ALIGNED>(rowA, g, V);
-        if (pair) zb[u] = load_group<T, ALIGNED>(rowB, g, V);
-      }
-    }
-    // A-row value of element e of group u: the target logit, or in logit mode
-    // the mixed logit (entries past V stay -inf).
-    auto a_val = [&](int u, int e) -> float {
-      const float zt = Elem<T>::get(za[u], e);
-      if (MODE == kLogitMix && pair) {
-        const float zq = Elem<T>::get(zb[u], e);
-        return zq == -INFINITY ? -INFINITY : mix_logit(zt, zq, lam_seq);
-      }
-      return zt;
-    };
-    float bmA = -INFINITY, bmB = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (ok[u]) {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) {
-          bmA = fmaxf(bmA, a_val(u, e));
-          if (pair) bmB = fmaxf(bmB, Elem<T>::get(zb[u], e));
-        }
-      }
-    if (bmA > mA) {
-      sA = __fmul_rn(sA, exp_shifted(mA, bmA));
-      mA = bmA;
-    }
-    if (pair && bmB > mB) {
-      sB = __fmul_rn(sB, exp_shifted(mB, bmB));
-      mB = bmB;
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (ok[u]) {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) {
-          sA = __fadd_rn(sA, exp_shifted(a_val(u, e), mA));
-          if (pair) sB = __fadd_rn(sB, exp_shifted(Elem<T>::get(zb[u], e), mB));
-        }
-      }
-  }
+    slice_stats<T, MODE, ALIGNED, kNT, kUnroll>(rowA, rowB, pair, lam_seq, V, g_lo, g_hi, mA, sA,
+                                                 mB, sB);
   block_merge_stats<kNT>(sh.bs, mA, sA, mB, sB);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -343,6 +296,7 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
       bc.sp.mB = st4.z;
       bc.sp.invSB = __fdiv_rn(1.0f, st4.w);
       bc.sp.lam = lam_seq;
+      bc.sp.c = 1.0f;
       if (n == K)
         bc.kind = kWBonus;
       else if (MODE == kProbMix && !(lam_seq < 1.0f))

@@ -1,0 +1,78 @@
+// specv_stream.cuh -- the streaming row-statistics loop shared by the cluster
+// row kernels (verify, tree verify, acceptance probabilities).
+//
+// A CTA of NT threads streams groups [g_lo, g_hi) of an A row (the p~ source:
+// the target row, or the mixed row z_t + lambda (z_q - z_t) in logit mode when
+// a draft row is present) and, if `pair`, of the B row (the draft row), with
+// U 16-byte loads per thread and row in flight.  Each thread keeps running
+// (max, sum-exp) statistics with a per-batch max: one exp per element and a
+// rescale only when the max grows.  The A and B rows go through the same
+// instruction sequence, so identical rows give bitwise identical statistics.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "specv_device.cuh"
+#include "specv_segments.cuh"
+
+namespace specv {
+
+template <typename T, int MODE, bool ALIGNED, int NT, int U>
+__device__ __forceinline__ void slice_stats(const T *rowA, const T *rowB, bool pair, float lam,
+                                            int V, int g_lo, int g_hi, float &mA, float &sA,
+                                            float &mB, float &sB) {
+  constexpr int VW = Elem<T>::kPerVec;
+  for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += NT * U) {
+    uint4 za[U], zb[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int g = g0 + u * NT;
+      ok[u] = g < g_hi;
+      if (ok[u]) {
+        za[u] = load_group<T, ALIGNED>(rowA, g, V);
+        if (pair) zb[u] = load_group<T, ALIGNED>(rowB, g, V);
+      }
+    }
+    // A-row value of element e of group u: the target logit, or in logit mode
+    // the mixed logit (entries past V stay -inf).
+    auto a_val = [&](int u, int e) -> float {
+      const float zt = Elem<T>::get(za[u], e);
+      if (MODE == kLogitMix && pair) {
+        const float zq = Elem<T>::get(zb[u], e);
+        return zq == -INFINITY ? -INFINITY : mix_logit(zt, zq, lam);
+      }
+      return zt;
+    };
+    float bmA = -INFINITY, bmB = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (ok[u]) {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          bmA = fmaxf(bmA, a_val(u, e));
+          if (pair) bmB = fmaxf(bmB, Elem<T>::get(zb[u], e));
+        }
+      }
+    if (bmA > mA) {
+      sA = __fmul_rn(sA, exp_shifted(mA, bmA));
+      mA = bmA;
+    }
+    if (pair && bmB > mB) {
+      sB = __fmul_rn(sB, exp_shifted(mB, bmB));
+      mB = bmB;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (ok[u]) {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          sA = __fadd_rn(sA, exp_shifted(a_val(u, e), mA));
+          if (pair) sB = __fadd_rn(sB, exp_shifted(Elem<T>::get(zb[u], e), mB));
+        }
+      }
+  }
+}
+
+}  // namespace specv

@@ -292,6 +292,7 @@ __device__ void finish_sequence(SweepShared &sh, const SweepArgs &a, int64_t b) 
       bc.sp.mB = st4.z;
       bc.sp.invSB = __fdiv_rn(1.0f, st4.w);
       bc.sp.lam = lam;
+      bc.sp.c = 1.0f;
       if (n == K)
         bc.kind = kWBonus;
       else if (MODE == kProbMix && !(lam < 1.0f))

@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kNT) tile_kernel(TileArgs a) {
       sp.mB = st4.z;
       sp.invSB = __fdiv_rn(1.0f, st4.w);
       sp.lam = lam;
+      sp.c = 1.0f;
       int kind = (n == K) ? kWBonus
                           : ((MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual);
       const T *ra = st_t + ((int64_t)s * (K + 1) + n) * V;

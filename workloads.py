@@ -148,6 +148,80 @@ def make_inputs(w: Workload, device="cpu", seed_offset: int = 0, lam=None):
                 u_resample=u_resample, lam=lam_t.to(torch.float32).contiguous())
 
 
+def tree_shape(kind: str, N: int, seed: int = 0):
+    """Parent list [N+1] (-1 at the root, parent[j] < j) of a draft tree.
+      chain      parent[j] = j - 1
+      kary:k     breadth-first k-ary tree (each node's children contiguous)
+      star       every node a child of the root
+      random:f   parent[j] uniform in [max(0, j - f), j)
+    """
+    name, *rest = kind.split(":")
+    par = [-1]
+    if name == "chain":
+        par += [j - 1 for j in range(1, N + 1)]
+    elif name == "kary":
+        k = int(rest[0])
+        par += [(j - 1) // k for j in range(1, N + 1)]
+    elif name == "star":
+        par += [0] * N
+    elif name == "random":
+        f = int(rest[0])
+        g = torch.Generator().manual_seed(SEED_BASE * 7 + seed)
+        for j in range(1, N + 1):
+            lo = max(0, j - f)
+            par.append(lo + int(torch.randint(0, j - lo, (1,), generator=g)))
+    else:
+        raise ValueError(f"unknown tree shape {kind}")
+    return par
+
+
+def make_tree_inputs(B: int, N: int, V: int, dtype: str = "f32", shape: str = "kary:2",
+                     s: float = 3.0, a: float = 0.8, e: float = 1.0, lam: float = 0.3,
+                     seed: int = 0, device="cpu"):
+    """Seeded inputs of tree verification: the same tree for every sequence.
+
+    Every node u has a target row z_t[u] ~ N(0, s^2); every node with children
+    has a draft row z_q = a * z_t[u] + N(0, e^2), numbered in node order; the
+    children of u are drawn independently from softmax(z_q) by the Gumbel-max
+    trick (the tree verification reading: siblings are i.i.d. draft samples).
+    Returns target_logits [B][N+1][V], draft_logits [B][M][V], parent,
+    draft_row, tokens (int32 [B][N+1]), u_accept [B][N+1], u_resample [B], lam
+    [B].
+    """
+    device = torch.device(device)
+    par = tree_shape(shape, N, seed)
+    has_child = [False] * (N + 1)
+    for j in range(1, N + 1):
+        has_child[par[j]] = True
+    drow = []
+    M = 0
+    for u in range(N + 1):
+        drow.append(M if has_child[u] else -1)
+        M += 1 if has_child[u] else 0
+    base = (SEED_BASE + 50 + seed) * 100
+    g_t, g_q, g_tok, g_u = (_gen(device, base + k) for k in range(4))
+    torch_dtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+    zt = _randn((B, N + 1, V), g_t, device).mul_(s)
+    rows_of = [u for u in range(N + 1) if has_child[u]]
+    zq = torch.empty((B, M, V), dtype=torch.float32, device=device)
+    if M:
+        zq.copy_(zt[:, rows_of].mul(a).add_(_randn((B, M, V), g_q, device).mul_(e)))
+    zt = zt.to(torch_dtype).contiguous()
+    zq = zq.to(torch_dtype).contiguous()
+    tokens = torch.zeros((B, N + 1), dtype=torch.int32, device=device)
+    if N:
+        child_rows = torch.tensor([drow[par[j]] for j in range(1, N + 1)], device=device)
+        zq_children = zq.float().index_select(1, child_rows)  # [B][N][V]: parent's draft row
+        tokens[:, 1:] = _gumbel_max_tokens(zq_children, g_tok, device)
+    u_accept = torch.rand((B, N + 1), generator=g_u, device=device, dtype=torch.float32)
+    u_resample = torch.rand((B,), generator=g_u, device=device, dtype=torch.float32)
+    parent_t = torch.tensor(par, dtype=torch.int32, device=device).repeat(B, 1).contiguous()
+    drow_t = torch.tensor(drow, dtype=torch.int32, device=device).repeat(B, 1).contiguous()
+    return dict(target_logits=zt, draft_logits=zq, parent=parent_t, draft_row=drow_t,
+                tokens=tokens, u_accept=u_accept, u_resample=u_resample,
+                lam=torch.full((B,), float(lam), dtype=torch.float32, device=device))
+
+
 def expected_bytes(w: Workload) -> int:
     return w.roofline_bytes
 
