@@ -57,6 +57,10 @@ def parse():
                     help="launch every step from the host instead of replaying a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tree", default=None, metavar="SHAPE",
+                    help="time specv_verify_tree on a draft tree of this shape (chain, kary:k, "
+                         "star, random:f) with --tree-nodes nodes besides the root")
+    ap.add_argument("--tree-nodes", type=int, default=14)
     ap.add_argument("--stats", action="store_true",
                     help="time specv_acceptance_rates (exact acceptance probabilities of every "
                          "drafted position) instead of the verify step")
@@ -209,7 +213,9 @@ def oracle_step(xh, mode, threads):
         oracle.verify_greedy(xh["target_logits"], xh["draft_logits"], xh["draft_tokens"],
                              xh["lam"], threads=threads)
     else:
-        oracle_step(xh, mode, threads)
+        oracle.verify(xh["target_logits"], xh["draft_logits"], xh["draft_tokens"],
+                      xh["u_accept"], xh["u_resample"], xh["lam"], mode=mode,
+                      diagnostics=False, threads=threads)
 
 
 def cpu_baseline(w, mode, target_seconds, host_inputs=None):
@@ -335,8 +341,75 @@ def run_stats(args):
     print(json.dumps(line), flush=True)
 
 
+def run_tree(args):
+    """One line for tree verification: tree nodes verified per second, and the
+    HBM bandwidth of the call with the bytes of one read of every node's rows
+    (target rows of all nodes, draft rows of the nodes with children); the walk
+    reads the rows of the nodes it visits again, which this figure leaves out."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import speculative_decoding_verification_specv_gb300 as specv
+    specv.load(build_if_missing=True)
+    w = workloads.WORKLOADS[args.config]
+    B = args.B or w.B
+    N = args.tree_nodes
+    mode = MODES[args.mode]
+    if mode == MODES["greedy"]:
+        raise SystemExit("tree verification takes prob or logit mode")
+    x = workloads.make_tree_inputs(B, N, w.V, w.dtype, args.tree, lam=float(w.lam[0])
+                                   if w.lam[0] != "uniform" else 0.25, device=dev)
+    M = x["draft_logits"].shape[1]
+    elem = 2 if w.dtype == "bf16" else 4
+    alg = (N + 1 + M) * B * w.V * elem
+    args_t = (x["target_logits"], x["draft_logits"], x["parent"], x["draft_row"], x["tokens"],
+              x["u_accept"], x["u_resample"], x["lam"])
+    specv.verify_tree(*args_t, mode=mode)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out = specv.verify_tree(*args_t, mode=mode)
+    stream = torch.cuda.current_stream(dev)
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev) if alg < 2 * l2 else None
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(0) as clk:
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(float(i))
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    peak, kind = measured_peak()
+    achieved = alg / (ms / 1e3) / 1e9
+    line = {
+        "metric": "draft-tree nodes verified/s (specv_verify_tree)",
+        "value": B * N / (ms / 1e3), "unit": "nodes/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "f32" if w.dtype == "f32" else "bf16", "data": "synthetic",
+        "config": {"workload": f"tree-{args.tree}-n{N}-v{w.V}-{w.dtype}-b{B}", "B": B, "N": N,
+                   "M": M, "V": w.V, "mode": args.mode,
+                   "mean_accepted": float(out[2].float().mean().item()),
+                   "l2": "flushed before every step" if flush is not None else "inputs > L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": alg, "kernel": "tree_kernel",
+                     "peak_source": kind},
+        "clocks": clk.summary(), "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.tree:
+        run_tree(args)
+        return
     if args.stats:
         run_stats(args)
         return

@@ -88,3 +88,13 @@ def test_plan_kernel_names_map_to_kernel_functions():
         pytest.skip("binding exposes no kernel-name table")
     for name in names.values():
         assert name in bench.PLAN_KERNEL_FUNCTION
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_oracle_step_runs_every_mode(mode):
+    """The oracle leg of the benchmark (cpu_baseline and the reference arm)."""
+    w = workloads.WORKLOADS[1]
+    xh = workloads.make_inputs(w, "cpu")
+    bench.oracle_step(xh, mode, 2)
+    out = bench.cpu_baseline(w, mode, 0.05, host_inputs=xh)
+    assert out["kind"] == "oracle" and out["value"] > 0
