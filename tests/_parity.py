@@ -5,7 +5,9 @@ decision boundary: |u_i - min(1, ratio_i)| for a decided position, or the
 distance of u_resample to the nearest boundary of the CDF it was drawn
 through.  Those sequences are counted, and their GPU output must still be a
 valid outcome: an accepted prefix of the draft, then one token that has
-positive probability under the distribution of that step, then -1.
+positive probability under the distribution of that step, then -1; when the
+GPU took the oracle's acceptance decisions, that token must also lie in the
+oracle's inverse-CDF interval of u_resample to within the band.
 """
 from __future__ import annotations
 
@@ -32,8 +34,11 @@ def run_oracle(xh, mode, seqs=None):
                          xh["u_accept"], xh["u_resample"], xh["lam"], mode=mode)
 
 
-def _valid_outcome(xh_b, mode, n, toks):
-    """Is (n, toks) a possible output for this sequence (any uniforms)?"""
+def _valid_outcome(xh_b, mode, n, toks, same_n=False, band=BAND):
+    """Is (n, toks) a possible output for this sequence?  With same_n (the GPU
+    took the oracle's decisions), the drawn token must also lie in the oracle's
+    fp64 inverse-CDF interval of u_resample for that step's distribution, to
+    within the band: C_{t-1} - band <= u <= C_t + band."""
     K = xh_b["draft_tokens"].shape[0]
     if not (0 <= n <= K):
         return False
@@ -47,9 +52,19 @@ def _valid_outcome(xh_b, mode, n, toks):
     lam = float(xh_b["lam"])
     pt, q = oracle.rows(xh_b["target_logits"], xh_b["draft_logits"], lam, mode)
     if n == K:
-        return pt[K, t] > 0
-    resid = np.maximum(0.0, pt[n] - q[n])
-    return resid[t] > 0 or (resid.sum() < 1e-12 and pt[n, t] > 0)
+        w = pt[K]
+    else:
+        w = np.maximum(0.0, pt[n] - q[n])
+        if w.sum() < 1e-12:
+            w = pt[n]
+    if not w[t] > 0:
+        return False
+    if not same_n:
+        return True
+    c = np.cumsum(w) / w.sum()
+    lo = c[t - 1] if t > 0 else 0.0
+    u = float(xh_b["u_resample"])
+    return lo - band <= u <= c[t] + band
 
 
 def compare(xh, mode, gpu_tokens, gpu_n, orc, seqs=None, band=BAND):
@@ -75,7 +90,7 @@ def compare(xh, mode, gpu_tokens, gpu_n, orc, seqs=None, band=BAND):
                 near_same += 1
                 continue
             xb = {k: v[b] for k, v in xh.items()}
-            if not _valid_outcome(xb, mode, int(gn[b]), gt[b]):
+            if not _valid_outcome(xb, mode, int(gn[b]), gt[b], same_n=int(gn[b]) == on):
                 mism.append((b, "invalid-outcome-near-band", on, int(gn[b]), ot.tolist(),
                              gt[b].tolist()))
             continue

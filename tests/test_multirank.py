@@ -98,3 +98,10 @@ def test_oracle_step_runs_every_mode(mode):
     bench.oracle_step(xh, mode, 2)
     out = bench.cpu_baseline(w, mode, 0.05, host_inputs=xh)
     assert out["kind"] == "oracle" and out["value"] > 0
+
+
+def test_l2_flush_runs_on_any_device():
+    """The between-steps L2 flush (write a 2x-L2 buffer, then read another)."""
+    f = bench.L2Flush("cpu", 1 << 16)
+    f(3)
+    assert float(f.w[0]) == 3.0 and float(f.sink) == 0.0
