@@ -213,7 +213,7 @@ int variant_from_env() {
 // The launch plan.
 //  - Short rows whose whole sequences fit a shared-memory tile: tile kernel.
 //  - Row kernels: the streaming cluster size is the smallest power of two
-//    (<= 16) that gives the grid >= 8 CTAs per SM and each CTA <= 512 KiB of
+//    (<= 16) that gives the grid >= 4 CTAs per SM and each CTA <= 512 KiB of
 //    (target + draft) slice, without going under 4 KiB of a row per CTA.
 //  - The resident row kernel (16-byte aligned rows, slice in shared memory)
 //    pays a fixed latency per CTA that only a single wave of clusters hides,
@@ -272,7 +272,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     if (S == 0) {
       S = 1;
       while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
-             (P * S < 8LL * sms || 2 * row_bytes / S > 512 * 1024))
+             (P * S < 4LL * sms || 2 * row_bytes / S > 512 * 1024))
         S *= 2;
     }
     while (S > 1 && P * S > INT32_MAX) S /= 2;
@@ -347,7 +347,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     if (S == 0) {
       S = 1;
       while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
-             (P * S < 8LL * sms || 2 * row_bytes / S > 512 * 1024))
+             (P * S < 4LL * sms || 2 * row_bytes / S > 512 * 1024))
         S *= 2;
     }
     while (S > 1 && P * S > INT32_MAX) S /= 2;
@@ -619,7 +619,7 @@ specv_status specv_verify_tree(const void *target_logits, const void *draft_logi
   if (S == 0) {
     S = 1;
     while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
-           (P * S < 8LL * sms || 2 * row_bytes / S > 512 * 1024))
+           (P * S < 4LL * sms || 2 * row_bytes / S > 512 * 1024))
       S *= 2;
   }
   while (S > 1 && P * S > INT32_MAX) S /= 2;

@@ -109,11 +109,11 @@ extern "C" specv_status specv_verify_noalloc(const void *target_logits, const vo
   const int64_t P = B * (K + 1);
   const int64_t G = (V + vw - 1) / vw;
   const int64_t row_bytes = (int64_t)V * elem;
-  // cluster size: the streaming kernel's rule (>= 8 CTAs per SM, <= 512 KiB
+  // cluster size: the streaming kernel's rule (>= 4 CTAs per SM, <= 512 KiB
   // of slice per CTA, >= 4 KiB of a row per CTA)
   int S = 1;
   while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
-         (P * S < 8LL * g_sms[dev] || 2 * row_bytes / S > 512 * 1024))
+         (P * S < 4LL * g_sms[dev] || 2 * row_bytes / S > 512 * 1024))
     S *= 2;
 
   unsigned char *scratch = static_cast<unsigned char *>(g_scratch_ptr[dev]);
