@@ -143,7 +143,7 @@ specv_status specv_verify_debug(const void *target_logits, const void *draft_log
  *            4 = resident cluster row kernel that samples the rejected row
  *            speculatively in place (only when the environment variable
  *            SPECV_ROWS_VARIANT=spec asks for it; =stream and =resident force
- *            kernels 1 and 2, and SPECV_CLUSTER_SIZE=1..16 (a power of two)
+ *            kernels 1 and 2, and SPECV_CLUSTER_SIZE=1..16
  *            forces the cluster size of the row kernels),
  *            5 = sweep row kernel: persistent CTAs stream fixed-size chunks of
  *            the rows through shared memory by bulk copies (only when

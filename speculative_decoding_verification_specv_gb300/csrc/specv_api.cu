@@ -195,8 +195,8 @@ bool sizes_ok(int64_t B, int32_t K, int32_t V, int dtype, int mode) {
 int cluster_from_env() {
   const char *s = std::getenv("SPECV_CLUSTER_SIZE");
   if (!s || !*s) return 0;
-  int v = std::atoi(s);
-  return (v == 1 || v == 2 || v == 4 || v == 8 || v == 16) ? v : 0;
+  const int v = std::atoi(s);
+  return (v >= 1 && v <= specv::kMaxCluster) ? v : 0;
 }
 
 // "stream", "resident" or "spec" forces a row-kernel variant (tuning and tests).
@@ -270,10 +270,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     if (env_var != 0 && env_var != 1) return SPECV_ERR_UNSUPPORTED;
     int S = env_S;
     if (S == 0) {
-      S = 1;
-      while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
-             (P * S < 4LL * sms || 2 * row_bytes / S > 512 * 1024))
-        S *= 2;
+      S = specv::stream_cluster_size(P, row_bytes, G, sms);
     }
     while (S > 1 && P * S > INT32_MAX) S /= 2;
     if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
@@ -345,10 +342,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
   if (kernel == 1 || kernel == 4) {
     S = env_S;
     if (S == 0) {
-      S = 1;
-      while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
-             (P * S < 4LL * sms || 2 * row_bytes / S > 512 * 1024))
-        S *= 2;
+      S = specv::stream_cluster_size(P, row_bytes, G, sms);
     }
     while (S > 1 && P * S > INT32_MAX) S /= 2;
     if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
@@ -617,10 +611,7 @@ specv_status specv_verify_tree(const void *target_logits, const void *draft_logi
   // cluster size: the streaming row kernel's rule
   int S = cluster_from_env();
   if (S == 0) {
-    S = 1;
-    while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
-           (P * S < 4LL * sms || 2 * row_bytes / S > 512 * 1024))
-      S *= 2;
+    S = specv::stream_cluster_size(P, row_bytes, G, sms);
   }
   while (S > 1 && P * S > INT32_MAX) S /= 2;
   if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;

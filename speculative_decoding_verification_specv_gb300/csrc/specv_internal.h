@@ -71,6 +71,35 @@ struct SweepArgs {
   int64_t items;             // B * (K+1) * chunks
 };
 
+// Cluster size of the streaming row kernels (verify, greedy, tree) for P
+// positions of rows of row_bytes bytes (groups 16-byte groups) on `sms` SMs.
+// The smallest power of two (<= kMaxCluster) that gives the grid >= 4 CTAs per
+// SM and each CTA <= 512 KiB of (target + draft) slice, without going under
+// 4 KiB of a row per CTA.  When that grid is at most two waves of 4 CTAs per
+// SM, the size (any 1..kMaxCluster within the same slice limits) that
+// minimises waves x (slice length + a fixed cost per CTA of kCtaFixedGroups
+// groups) instead: a badly quantised wave costs a whole extra slice time (at
+// 192 positions S = 3 fills one wave where S = 4 needs two).
+constexpr int64_t kCtaFixedGroups = 2048;
+inline int stream_cluster_size(int64_t P, int64_t row_bytes, int64_t groups, int sms) {
+  int S = 1;
+  while (S < kMaxCluster && row_bytes / (2 * S) >= 4096 &&
+         (P * S < 4LL * sms || 2 * row_bytes / S > 512 * 1024))
+    S *= 2;
+  const int64_t slots = 4LL * sms;
+  if (P * S > 2 * slots) return S;
+  auto cost = [&](int s) {
+    return ((P * s + slots - 1) / slots) * ((groups + s - 1) / s + kCtaFixedGroups);
+  };
+  int best = S;
+  for (int s = 1; s <= kMaxCluster; ++s) {
+    if (s > 1 && row_bytes / (2 * s) < 4096) continue;
+    if (2 * row_bytes / s > 512 * 1024) continue;
+    if (cost(s) < cost(best)) best = s;
+  }
+  return best;
+}
+
 // Arguments of the cluster row kernel (one cluster per (sequence, position)).
 struct RowArgs {
   const void *target;        // [B][K+1][V]

@@ -109,12 +109,8 @@ extern "C" specv_status specv_verify_noalloc(const void *target_logits, const vo
   const int64_t P = B * (K + 1);
   const int64_t G = (V + vw - 1) / vw;
   const int64_t row_bytes = (int64_t)V * elem;
-  // cluster size: the streaming kernel's rule (>= 4 CTAs per SM, <= 512 KiB
-  // of slice per CTA, >= 4 KiB of a row per CTA)
-  int S = 1;
-  while (S < specv::kMaxCluster && row_bytes / (2 * S) >= 4096 &&
-         (P * S < 4LL * g_sms[dev] || 2 * row_bytes / S > 512 * 1024))
-    S *= 2;
+  // cluster size: the streaming kernel's rule
+  const int S = specv::stream_cluster_size(P, row_bytes, G, g_sms[dev]);
 
   unsigned char *scratch = static_cast<unsigned char *>(g_scratch_ptr[dev]);
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -127,3 +127,16 @@ def test_plan_greedy_mode(lib, monkeypatch):
     st = specv.raw_call("specv_verify_debug", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 0, 2,
                         FAKE, FAKE, None, None, None, None)
     assert st == 2
+
+
+def test_plan_cluster_size_model(lib):
+    """Streaming cluster size: the power-of-two rule for many waves (the batched
+    workload keeps S = 2), waves x (slice + fixed cost) near one wave (192
+    positions: S = 3 fills one wave where S = 4 needs two)."""
+    assert specv.plan(256, 8, 128256, specv.F32)["cluster"] == 2
+    p3 = specv.plan(32, 5, 152064, specv.BF16)
+    assert p3["kernel"] == "rows-stream" and p3["cluster"] == 3 and p3["ctas"] == 192 * 3
+    assert specv.plan(32, 5, 152064, specv.BF16, specv.GREEDY)["cluster"] == 3
+    for B, K, V, dt in [(16, 8, 128256, 0), (64, 4, 32000, 1), (8, 4, 128256, 1), (3, 2, 9000, 0)]:
+        S = specv.plan(B, K, V, dt)["cluster"]
+        assert 1 <= S <= 16

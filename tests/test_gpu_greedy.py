@@ -131,7 +131,7 @@ def test_greedy_ragged_shapes(specv, shape, lam):
     _check(specv, x)
 
 
-@pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 7, 8, 16])
 def test_greedy_every_cluster_size_with_ties(specv, env_guard, S):
     """Integer logits in a small range: every row has many equal maxima, spread
     over all ranks of the cluster; the first one in index order must win."""

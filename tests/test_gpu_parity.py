@@ -104,7 +104,7 @@ def test_parity_full_size_exactness_workload(specv, mode):
     print(f"full-size exactness workload mode={mode}: {rep}")
 
 
-@pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 6, 8, 15, 16])
 @pytest.mark.parametrize("variant", ["stream", "resident", "spec"])
 def test_every_cluster_size(specv, cluster_env, variant, S):
     os.environ["SPECV_CLUSTER_SIZE"] = str(S)

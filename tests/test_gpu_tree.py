@@ -109,7 +109,7 @@ def test_tree_many_siblings_rejected(specv):
     assert (n <= 1).all()
 
 
-@pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 8, 13, 16])
 def test_tree_every_cluster_size(specv, env_guard, S):
     os.environ["SPECV_CLUSTER_SIZE"] = str(S)
     x = workloads.make_tree_inputs(4, 7, 50000, "bf16", "kary:2", lam=0.25, seed=7, device=DEV)
