@@ -176,6 +176,9 @@ struct Plan {
   int groups_per_slice, num_groups;
   int seg_tiles, segs_per_slice;  // sampler segments of the streaming row kernel
   int res_smem;          // dynamic shared memory of the resident kernel
+  int split;             // streaming kernel: 1 = token draws in a second launch (rows_sample)
+  int sample_cluster;    // its cluster size
+  int sample_gps, sample_seg_tiles, sample_segs;  // its slice and segment geometry
   int chunk_groups, chunks;       // sweep kernel: groups per chunk, chunks per row
   int sweep_smem;        // dynamic shared memory of the sweep kernel
   int64_t counters;      // arrival counters in the scratch
@@ -197,6 +200,14 @@ int cluster_from_env() {
   if (!s || !*s) return 0;
   const int v = std::atoi(s);
   return (v >= 1 && v <= specv::kMaxCluster) ? v : 0;
+}
+
+// SPECV_SAMPLE_SPLIT=0/1 forces the streaming kernel's token draws into the
+// statistics launch or into a second launch (tuning and tests); -1: the plan.
+int split_from_env() {
+  const char *s = std::getenv("SPECV_SAMPLE_SPLIT");
+  if (!s || !*s) return -1;
+  return s[0] == '1' ? 1 : (s[0] == '0' ? 0 : -1);
 }
 
 // "stream", "resident" or "spec" forces a row-kernel variant (tuning and tests).
@@ -360,6 +371,23 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     // position statistics, then the bonus rows' segment statistics
     specv::rows_segments(p->groups_per_slice, &p->seg_tiles, &p->segs_per_slice);
     p->ws_bytes = round16(P * 16) + round16(B * S * (int64_t)p->segs_per_slice * 8) + round16(B * 4);
+    // A grid of about one wave finishes every sequence at about the same time,
+    // so the last clusters' token draws form a tail on a few CTAs each; then
+    // the draws run as a second launch with a wider cluster per sequence
+    // (about 48 KiB of the row pair per CTA, mostly still in L2).  Several
+    // waves keep the draws in the statistics launch, overlapped with streaming.
+    const int env_split = split_from_env();
+    const bool one_wave = P * S <= 2 * 4LL * sms;
+    p->split = env_split >= 0 ? env_split : (one_wave ? 1 : 0);
+    if (p->split) {
+      int64_t s2 = (2 * row_bytes + 48 * 1024 - 1) / (48 * 1024);
+      if (s2 < 1) s2 = 1;
+      if (s2 > specv::kMaxCluster) s2 = specv::kMaxCluster;
+      while (s2 > 1 && B * s2 > INT32_MAX) --s2;
+      p->sample_cluster = (int)s2;
+      p->sample_gps = (int)((G + s2 - 1) / s2);
+      specv::rows_segments(p->sample_gps, &p->sample_seg_tiles, &p->sample_segs);
+    }
   }
   return SPECV_OK;
 }
@@ -515,7 +543,20 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     a.ws_seg = mode == SPECV_GREEDY ? nullptr  // no sampling, no segment statistics
                                     : reinterpret_cast<float2 *>(static_cast<char *>(wdata) +
                                                                  round16(B * (K + 1) * 16));
+    a.defer_sampling = mode != SPECV_GREEDY && p.split;
+    a.stats_cluster = p.cluster;
+    a.stats_groups_per_slice = p.groups_per_slice;
+    a.stats_seg_tiles = p.seg_tiles;
+    a.stats_segs_per_slice = p.segs_per_slice;
     if (e == cudaSuccess) e = specv::rows_launch(a, bf16, mode, aligned, p.cluster, p.ctas, stream);
+    if (e == cudaSuccess && a.defer_sampling) {
+      specv::RowArgs a2 = a;
+      a2.groups_per_slice = p.sample_gps;
+      a2.seg_tiles = p.sample_seg_tiles;
+      a2.segs_per_slice = p.sample_segs;
+      e = specv::rows_sample_launch(a2, bf16, mode, aligned, p.sample_cluster,
+                                    B * (int64_t)p.sample_cluster, stream);
+    }
   }
   if (per_call) {
     const cudaError_t ef = cudaFreeAsync(ws, stream);

@@ -125,6 +125,13 @@ struct RowArgs {
   float2 *ws_seg;            // optional scratch [B][S][segs_per_slice]: (max, sum-exp) of the
                              // bonus row's segments, written in phase 1 (null: the sampler
                              // reads the bonus row again)
+  int defer_sampling;        // 1: the last cluster stops after the decisions; rows_sample
+                             // draws the tokens in a second launch
+  // rows_sample only: the statistics launch's geometry (for the bonus segments)
+  int stats_cluster;
+  int stats_groups_per_slice;
+  int stats_seg_tiles;
+  int stats_segs_per_slice;
 };
 
 // Arguments of the small-vocabulary tile kernel (a CTA holds whole sequences).
@@ -234,6 +241,10 @@ cudaError_t sweep_launch(const SweepArgs &a, int dtype_bf16, int mode, int64_t g
 cudaError_t rows_prepare();
 cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
                         int64_t grid, cudaStream_t stream);
+// The deferred token draws: one cluster of S CTAs per sequence (grid B * S),
+// after a rows_launch with defer_sampling = 1 on the same stream.
+cudaError_t rows_sample_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
+                               int64_t grid, cudaStream_t stream);
 
 cudaError_t tile_tma_prepare(int max_smem_bytes);
 int tile_tma_blocks_per_sm(int dtype_bf16, int mode, int smem_bytes);

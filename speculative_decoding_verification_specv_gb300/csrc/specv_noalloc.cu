@@ -136,6 +136,11 @@ extern "C" specv_status specv_verify_noalloc(const void *target_logits, const vo
   // no room for the bonus rows' segment statistics: the sampler reads the bonus row again
   specv::rows_segments(a.groups_per_slice, &a.seg_tiles, &a.segs_per_slice);
   a.ws_seg = nullptr;
+  a.defer_sampling = 0;  // one launch: the token draws stay in the statistics launch
+  a.stats_cluster = S;
+  a.stats_groups_per_slice = a.groups_per_slice;
+  a.stats_seg_tiles = a.seg_tiles;
+  a.stats_segs_per_slice = a.segs_per_slice;
   const bool aligned = ((uintptr_t)target_logits % 16 == 0) && ((uintptr_t)draft_logits % 16 == 0) &&
                        (row_bytes % 16 == 0);
   // the arrival counters must start at zero on every call (no allocation: a memset)

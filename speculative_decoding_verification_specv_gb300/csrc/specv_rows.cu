@@ -183,6 +183,71 @@ __device__ int bonus_from_stats(RowsShared &sh, const RowArgs &a, const T *row, 
                                                         lo, t);
 }
 
+// The token at one index of a sequence, by inverse CDF over the sampler
+// weights of `kind` of the row(s), split over the S CTAs of the cluster (this
+// CTA: groups [g_lo, g_hi) in nseg segments): segment masses, the S slice
+// masses over DSMEM, the rank holding u * total routes it to a segment, one
+// warp walks it; a residual of zero mass (round-off only) falls back to p~.
+// Writes *out.  Every rank of the cluster calls it (cluster barriers inside).
+template <typename T, int MODE, bool ALIGNED>
+__device__ void draw_token(RowsShared &sh, cg::cluster_group &cluster, int S, int rank,
+                           const T *sA_row, const T *sB_row, int V, int g_lo, int g_hi,
+                           int seg_groups, int nseg, int kind, const SampleParams &sp, float u,
+                           int32_t *out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float R = 0.0f;
+  int attempt = 0;
+  for (;; ++attempt) {
+    const float mass = segment_masses<T, MODE, ALIGNED, kSegLaneGroups, kNT>(
+        sh, sA_row, sB_row, V, g_lo, g_hi, seg_groups, nseg, kind, sp);
+    if (threadIdx.x == 0)
+      for (int r = 0; r < S; ++r) cluster.map_shared_rank(sh.masses[attempt], r)[rank] = mass;
+    cluster.sync();  // all slice masses exchanged
+    R = 0.0f;
+    for (int r = 0; r < S; ++r) R = __fadd_rn(R, sh.masses[attempt][r]);
+    if (R > 0.0f || kind != kWResidual || attempt == 1) break;
+    kind = kWMixture;  // zero residual mass (round-off only): draw from p~ instead
+  }
+  if (!(R > 0.0f)) {
+    if (rank == 0 && threadIdx.x == 0) *out = -1;
+    return;
+  }
+  const float t = __fmul_rn(u, R);
+  int rstar = -1;
+  float tloc = INFINITY;
+  float c = 0.0f;
+  for (int r = 0; r < S; ++r) {
+    const float cn = __fadd_rn(c, sh.masses[attempt][r]);
+    if (cn > t) {
+      rstar = r;
+      tloc = __fsub_rn(t, c);
+      break;
+    }
+    c = cn;
+  }
+  if (rstar < 0) {  // u*R not below the total (u >= 1 or round-off): last slice with mass
+    for (int r = S - 1; r >= 0; --r)
+      if (sh.masses[attempt][r] > 0.0f) {
+        rstar = r;
+        break;
+      }
+    tloc = INFINITY;
+  }
+  if (rank != rstar) return;
+  float lo = 0.0f;
+  const int s = find_segment<kNT>(sh, nseg, tloc, &lo);
+  if (warp != 0) return;
+  if (s < 0) {  // no entry of positive weight in the routed slice (not reached: its mass is > 0)
+    if (lane == 0) *out = -1;
+    return;
+  }
+  const int sg_lo = g_lo + s * seg_groups;
+  const int sg_hi = min(g_hi, sg_lo + seg_groups);
+  const int tok = segment_walk<T, MODE, ALIGNED, kSegLaneGroups>(sA_row, sB_row, V, sg_lo, sg_hi,
+                                                                  kind, sp, lo, tloc);
+  if (lane == 0) *out = tok;
+}
+
 template <typename T, int MODE, bool ALIGNED>
 __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   constexpr int VW = Elem<T>::kPerVec;
@@ -303,9 +368,11 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
         bc.kind = kWMixture;  // p~ = q: the residual is identically zero
       else
         bc.kind = kWResidual;
-      for (int r = 0; r < S; ++r) *cluster.map_shared_rank(&sh.bc, r) = bc;
+      if (!a.defer_sampling)
+        for (int r = 0; r < S; ++r) *cluster.map_shared_rank(&sh.bc, r) = bc;
     }
   }
+  if (a.defer_sampling) return;  // rows_sample draws the tokens (no DSMEM traffic above)
   cluster.sync();  // broadcast visible everywhere
   const Broadcast bc = sh.bc;
   if (bc.n < 0) return;
@@ -319,58 +386,56 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
     if (threadIdx.x == 0) a.out_tokens[b * (K + 1) + bc.n] = tok;
     return;
   }
-  int kind = bc.kind;
-  float R = 0.0f;
-  int attempt = 0;
-  for (;; ++attempt) {
-    const float mass = segment_masses<T, MODE, ALIGNED, kSegLaneGroups, kNT>(
-        sh, sA_row, sB_row, V, g_lo, g_hi, seg_groups, nseg, kind, bc.sp);
-    if (threadIdx.x == 0)
-      for (int r = 0; r < S; ++r) cluster.map_shared_rank(sh.masses[attempt], r)[rank] = mass;
-    cluster.sync();  // all slice masses exchanged
-    R = 0.0f;
-    for (int r = 0; r < S; ++r) R = __fadd_rn(R, sh.masses[attempt][r]);
-    if (R > 0.0f || kind != kWResidual || attempt == 1) break;
-    kind = kWMixture;  // zero residual mass (round-off only): draw from p~ instead
-  }
-  if (!(R > 0.0f)) {
-    if (rank == 0 && threadIdx.x == 0) a.out_tokens[b * (K + 1) + bc.n] = -1;
+  draw_token<T, MODE, ALIGNED>(sh, cluster, S, rank, sA_row, sB_row, V, g_lo, g_hi, seg_groups,
+                               nseg, bc.kind, bc.sp, bc.u, a.out_tokens + b * (K + 1) + bc.n);
+}
+
+// The deferred token draws: one cluster of S CTAs per sequence (a wider
+// cluster than the statistics launch's, so that each CTA's share of the
+// second read is small), after the statistics launch has written out_n and
+// the position statistics.  The sampler's weight kind and parameters follow
+// from out_n[b] exactly as the statistics launch's last cluster derives them.
+template <typename T, int MODE, bool ALIGNED>
+__global__ void __launch_bounds__(kNT, 4) rows_sample_kernel(RowArgs a) {
+  __shared__ RowsShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int S = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int64_t b = (int64_t)blockIdx.x / S;
+  const int K = a.K, V = a.V;
+  const int n = a.out_n[b];
+  if (n < 0) return;  // invalid sequence (or a timed-out copy): nothing to draw
+  const float lam = a.lam[b];
+  const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + n]);
+  SampleParams sp;
+  sp.mA = st4.x;
+  sp.invSA = __fdiv_rn(1.0f, st4.y);
+  sp.mB = st4.z;
+  sp.invSB = __fdiv_rn(1.0f, st4.w);
+  sp.lam = lam;
+  sp.c = 1.0f;
+  const int kind = n == K ? kWBonus
+                          : ((MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual);
+  const float u = a.u_resample[b];
+  const T *tgt = static_cast<const T *>(a.target);
+  const T *dft = static_cast<const T *>(a.draft);
+  const T *sA_row = tgt + (b * (K + 1) + n) * (int64_t)V;
+  const T *sB_row = dft + (b * K + (n < K ? n : 0)) * (int64_t)V;
+  int32_t *out = a.out_tokens + b * (K + 1) + n;
+  if (kind == kWBonus && a.ws_seg != nullptr) {
+    if (rank != 0) return;
+    RowArgs a1 = a;  // the statistics launch's geometry of the segment statistics
+    a1.groups_per_slice = a.stats_groups_per_slice;
+    a1.seg_tiles = a.stats_seg_tiles;
+    a1.segs_per_slice = a.stats_segs_per_slice;
+    const int tok = bonus_from_stats<T, MODE, ALIGNED>(sh, a1, sA_row, a.stats_cluster, b, sp, u);
+    if (threadIdx.x == 0) *out = tok;
     return;
   }
-  const float t = __fmul_rn(bc.u, R);
-  int rstar = -1;
-  float tloc = INFINITY;
-  float c = 0.0f;
-  for (int r = 0; r < S; ++r) {
-    const float cn = __fadd_rn(c, sh.masses[attempt][r]);
-    if (cn > t) {
-      rstar = r;
-      tloc = __fsub_rn(t, c);
-      break;
-    }
-    c = cn;
-  }
-  if (rstar < 0) {  // u*R not below the total (u >= 1 or round-off): last slice with mass
-    for (int r = S - 1; r >= 0; --r)
-      if (sh.masses[attempt][r] > 0.0f) {
-        rstar = r;
-        break;
-      }
-    tloc = INFINITY;
-  }
-  if (rank != rstar) return;
-  float lo = 0.0f;
-  const int s = find_segment<kNT>(sh, nseg, tloc, &lo);
-  if (warp != 0) return;
-  if (s < 0) {  // no entry of positive weight in the routed slice (not reached: its mass is > 0)
-    if (lane == 0) a.out_tokens[b * (K + 1) + bc.n] = -1;
-    return;
-  }
-  const int sg_lo = g_lo + s * seg_groups;
-  const int sg_hi = min(g_hi, sg_lo + seg_groups);
-  const int tok = segment_walk<T, MODE, ALIGNED, kSegLaneGroups>(sA_row, sB_row, V, sg_lo, sg_hi,
-                                                                  kind, bc.sp, lo, tloc);
-  if (lane == 0) a.out_tokens[b * (K + 1) + bc.n] = tok;
+  const int g_lo = rank * a.groups_per_slice;
+  const int g_hi = min(a.num_groups, g_lo + a.groups_per_slice);
+  draw_token<T, MODE, ALIGNED>(sh, cluster, S, rank, sA_row, sB_row, V, g_lo, g_hi,
+                               a.seg_tiles * kSegGroups, a.segs_per_slice, kind, sp, u, out);
 }
 
 // Greedy verification with the same decomposition (one cluster per position,
@@ -518,9 +583,32 @@ cudaError_t launch_one(const RowArgs &a, int S, int64_t grid, cudaStream_t strea
 }
 
 template <typename T, int MODE, bool ALIGNED>
+cudaError_t launch_sample_one(const RowArgs &a, int S, int64_t grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kNT, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rows_sample_kernel<T, MODE, ALIGNED>, a);
+}
+
+template <typename T, int MODE, bool ALIGNED>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(row_kernel_of<T, MODE, ALIGNED>(),
-                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = cudaFuncSetAttribute(row_kernel_of<T, MODE, ALIGNED>(),
+                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if constexpr (MODE != kGreedy) {
+    const cudaError_t e2 = cudaFuncSetAttribute(rows_sample_kernel<T, MODE, ALIGNED>,
+                                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e;
 }
 
 }  // namespace
@@ -567,6 +655,26 @@ cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned
                    : launch_one<float, kProbMix, false>(a, S, grid, stream);
   return aligned ? launch_one<float, kLogitMix, true>(a, S, grid, stream)
                  : launch_one<float, kLogitMix, false>(a, S, grid, stream);
+}
+
+}  // namespace specv
+
+namespace specv {
+
+cudaError_t rows_sample_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
+                               int64_t grid, cudaStream_t stream) {
+  if (dtype_bf16) {
+    if (mode == kProbMix)
+      return aligned ? launch_sample_one<uint16_t, kProbMix, true>(a, S, grid, stream)
+                     : launch_sample_one<uint16_t, kProbMix, false>(a, S, grid, stream);
+    return aligned ? launch_sample_one<uint16_t, kLogitMix, true>(a, S, grid, stream)
+                   : launch_sample_one<uint16_t, kLogitMix, false>(a, S, grid, stream);
+  }
+  if (mode == kProbMix)
+    return aligned ? launch_sample_one<float, kProbMix, true>(a, S, grid, stream)
+                   : launch_sample_one<float, kProbMix, false>(a, S, grid, stream);
+  return aligned ? launch_sample_one<float, kLogitMix, true>(a, S, grid, stream)
+                 : launch_sample_one<float, kLogitMix, false>(a, S, grid, stream);
 }
 
 }  // namespace specv

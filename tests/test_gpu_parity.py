@@ -31,7 +31,7 @@ def specv():
 
 @pytest.fixture
 def cluster_env():
-    keys = ("SPECV_CLUSTER_SIZE", "SPECV_ROWS_VARIANT")
+    keys = ("SPECV_CLUSTER_SIZE", "SPECV_ROWS_VARIANT", "SPECV_SAMPLE_SPLIT")
     old = {k: os.environ.get(k) for k in keys}
     yield
     for k, v in old.items():
@@ -155,6 +155,27 @@ def test_long_slices_multi_tile_segments(specv, cluster_env, V, dt, mode):
     rep, _, n = _check(specv, x, mode)
     assert (n == w.K).any() and (n < w.K).any()
     print(f"V={V} {dt} mode={mode}: {rep}")
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+@pytest.mark.parametrize("split", ["0", "1"], ids=["fused", "split"])
+@pytest.mark.parametrize("shape", [(8, 5, 152064, "bf16", "rho:3.0:0.5:0.95"),
+                                   (16, 8, 128256, "f32", "half_equal:3.0:0.85:1.0"),
+                                   (5, 3, 1001, "f32", "corr:2.0:0.8:1.0"),
+                                   (3, 33, 515, "bf16", "corr:3.0:0.9:0.7"),
+                                   (6, 4, 300001, "f32", "half_equal:3.0:0.85:1.0")],
+                         ids=lambda s: f"B{s[0]}K{s[1]}V{s[2]}{s[3]}")
+def test_token_draws_in_one_or_two_launches(specv, cluster_env, shape, split, mode):
+    """The streaming kernel's token draws in the statistics launch (fused) or in
+    a second launch with a wider cluster per sequence (split): both give the
+    oracle's decisions, bonus rows included."""
+    os.environ["SPECV_ROWS_VARIANT"] = "stream"
+    os.environ["SPECV_SAMPLE_SPLIT"] = split
+    B, K, V, dt, st = shape
+    w = workloads.Workload("split", B, K, V, dt, st, (0.3,), 17)
+    x = workloads.make_inputs(w, DEV)
+    rep, _, n = _check(specv, x, mode)
+    print(f"{shape} split={split} mode={mode}: {rep}")
 
 
 RAGGED = [
