@@ -5,7 +5,11 @@
 // the target row, or the mixed row z_t + lambda (z_q - z_t) in logit mode when
 // a draft row is present) and, if `pair`, of the B row (the draft row), with
 // U 16-byte loads per thread and row in flight.  Each thread keeps running
-// (max, sum-exp) statistics with a per-batch max: one exp per element and a
+// (max, sum-exp) statistics with a per-batch max: one exp per element,
+// 2^(z log2e - m log2e) as one fused multiply-add and the SFU's 2^x, with
+// m log2e rounded once per batch (which scales the batch's terms by a common
+// factor within half an ulp of m log2e of 1: a relative error below 1e-6 of
+// the sum for |m| < 64, the order of the fp32 accumulation itself), and a
 // rescale only when the max grows.  The A and B rows go through the same
 // instruction sequence, so identical rows give bitwise identical statistics.
 #pragma once
@@ -63,13 +67,14 @@ __device__ __forceinline__ void slice_stats(const T *rowA, const T *rowB, bool p
       sB = __fmul_rn(sB, exp_shifted(mB, bmB));
       mB = bmB;
     }
+    const float nA = -__fmul_rn(mA, kLog2e), nB = -__fmul_rn(mB, kLog2e);
 #pragma unroll
     for (int u = 0; u < U; ++u)
       if (ok[u]) {
 #pragma unroll
         for (int e = 0; e < VW; ++e) {
-          sA = __fadd_rn(sA, exp_shifted(a_val(u, e), mA));
-          if (pair) sB = __fadd_rn(sB, exp_shifted(Elem<T>::get(zb[u], e), mB));
+          sA = __fadd_rn(sA, ex2(__fmaf_rn(a_val(u, e), kLog2e, nA)));
+          if (pair) sB = __fadd_rn(sB, ex2(__fmaf_rn(Elem<T>::get(zb[u], e), kLog2e, nB)));
         }
       }
   }
