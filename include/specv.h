@@ -110,6 +110,45 @@ specv_status specv_verify(const void *target_logits, const void *draft_logits,
                           int32_t *out_n_accepted, void *stream);
 
 /*
+ * specv_verify_host -- specv_verify on inputs and outputs in host memory.
+ *
+ *   Arguments, layouts and results as specv_verify, except that every array
+ *   (the six inputs, out_tokens and out_n_accepted) is a HOST pointer.
+ *   chunks         0 = the library's choice (about 64 MiB of logits per
+ *                  chunk, at most 16), else 1..64; capped at B.
+ *
+ * The call copies the inputs into device staging memory that the library
+ * owns (one buffer per (device, stream), grown on demand, kept until the
+ * process exits), runs the verify step there and copies out_tokens and
+ * out_n_accepted back, all asynchronously: the batch is cut into `chunks`
+ * runs of whole sequences, each chunk's logits are copied on a copy stream of
+ * the library, and each chunk's verify step runs on `stream` as soon as its
+ * copy has landed, so the host link and the kernels overlap.  On return
+ * nothing has completed yet: the host inputs must stay unchanged, and the
+ * outputs unread, until `stream` has completed (cudaStreamSynchronize or an
+ * event recorded on it).  The copies are asynchronous only from page-locked
+ * host memory; pageable memory gives the same results, with copies that
+ * the CUDA runtime may serialise against the host.  Calls on one stream must
+ * come from one host thread at a time.
+ *
+ * The result equals specv_verify's on the same inputs with chunks = 1; with
+ * more chunks every sequence is verified by the same kernels on a smaller
+ * batch, which may change the launch plan and so the rounding order of the
+ * row sums: decisions can then differ only where a uniform lies within
+ * rounding error of a decision or CDF boundary.
+ *
+ * Errors: SPECV_ERR_INVALID_ARG as specv_verify, or chunks outside 0..64;
+ * SPECV_ERR_UNSUPPORTED while `stream` is being captured into a CUDA graph
+ * (staging may have to grow; capture specv_verify on device buffers
+ * instead); SPECV_ERR_NO_MEMORY if the staging memory cannot be allocated.
+ */
+specv_status specv_verify_host(const void *target_logits, const void *draft_logits,
+                               const int32_t *draft_tokens, const float *u_accept,
+                               const float *u_resample, const float *lambda, int64_t B, int32_t K,
+                               int32_t V, specv_dtype dtype, specv_mode mode, int32_t *out_tokens,
+                               int32_t *out_n_accepted, int32_t chunks, void *stream);
+
+/*
  * specv_verify_debug -- specv_verify plus the intermediate probabilities, for
  * tests.  Same kernels and the same arithmetic as specv_verify; the extra
  * outputs (device pointers, each may be NULL) are:

@@ -23,8 +23,9 @@ import torch
 
 from . import build as _build
 
-__all__ = ["SpecvError", "PROB_MIX", "LOGIT_MIX", "F32", "BF16", "load", "lib_path", "verify",
-           "verify_debug", "plan", "status_string", "EXPORTED_SYMBOLS"]
+__all__ = ["SpecvError", "PROB_MIX", "LOGIT_MIX", "GREEDY", "F32", "BF16", "load", "lib_path",
+           "verify", "verify_host", "verify_debug", "verify_tree", "acceptance_rates", "choose_k",
+           "AdaptiveK", "plan", "status_string", "EXPORTED_SYMBOLS"]
 
 PROB_MIX = 0
 LOGIT_MIX = 1
@@ -34,7 +35,8 @@ BF16 = 1
 
 EXPORTED_SYMBOLS = ("specv_verify", "specv_verify_debug", "specv_plan", "specv_status_string",
                     "specv_last_cuda_error", "specv_version", "specv_verify_noalloc",
-                    "specv_acceptance_rates", "specv_choose_k", "specv_verify_tree")
+                    "specv_acceptance_rates", "specv_choose_k", "specv_verify_tree",
+                    "specv_verify_host")
 
 _STATUS = {0: "SPECV_OK", 1: "SPECV_ERR_INVALID_ARG", 2: "SPECV_ERR_UNSUPPORTED",
            3: "SPECV_ERR_CUDA", 4: "SPECV_ERR_NO_MEMORY"}
@@ -75,6 +77,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         common = [vp, vp, vp, vp, vp, vp, i64, i32, i32, ctypes.c_int, ctypes.c_int, vp, vp]
         lib.specv_verify.argtypes = common + [vp]
         lib.specv_verify.restype = ctypes.c_int
+        lib.specv_verify_host.argtypes = common + [i32, vp]
+        lib.specv_verify_host.restype = ctypes.c_int
         lib.specv_verify_debug.argtypes = common + [vp, vp, vp, vp]
         lib.specv_verify_debug.restype = ctypes.c_int
         lib.specv_plan.argtypes = [i64, i32, i32, ctypes.c_int, ctypes.c_int, i32p, i32p,
@@ -132,14 +136,16 @@ def _require(t: torch.Tensor, name: str, dtype, shape, device):
 
 
 def _args(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam, mode, out_tokens,
-          out_n_accepted):
+          out_n_accepted, host=False):
     zt, zq = target_logits, draft_logits
     if zt.dim() != 3:
         raise ValueError("target_logits must be [B][K+1][V]")
     B, K1, V = zt.shape
     K = K1 - 1
     dev = zt.device
-    if dev.type != "cuda":
+    if host and dev.type != "cpu":
+        raise ValueError("verify_host takes tensors in host memory (use verify for CUDA tensors)")
+    if not host and dev.type != "cuda":
         raise ValueError("inputs must be CUDA tensors (the verify step runs only on the GPU)")
     _require(zt, "target_logits", None, (B, K + 1, V), dev)
     _require(zq, "draft_logits", zt.dtype, (B, K, V), dev)
@@ -148,9 +154,9 @@ def _args(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam, 
     _require(u_resample, "u_resample", torch.float32, (B,), dev)
     _require(lam, "lam", torch.float32, (B,), dev)
     if out_tokens is None:
-        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev, pin_memory=host)
     if out_n_accepted is None:
-        out_n_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+        out_n_accepted = torch.empty((B,), dtype=torch.int32, device=dev, pin_memory=host)
     _require(out_tokens, "out_tokens", torch.int32, (B, K + 1), dev)
     _require(out_n_accepted, "out_n_accepted", torch.int32, (B,), dev)
     if mode not in (PROB_MIX, LOGIT_MIX, GREEDY):
@@ -184,6 +190,33 @@ def verify(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam,
         _dtype_code(target_logits), int(mode), out_tokens.data_ptr(), out_n.data_ptr(),
         _stream_ptr(stream, dev))
     _check(st, "specv_verify")
+    return out_tokens, out_n
+
+
+def verify_host(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam,
+                mode: int = PROB_MIX, out_tokens=None, out_n_accepted=None, chunks: int = 0,
+                stream=None):
+    """verify() on tensors in host memory (page-locked for asynchronous copies):
+    the library copies the inputs to the GPU in chunks of whole sequences,
+    overlapping each chunk's copy with the verify step of the previous one, and
+    copies the results back into out_tokens / out_n_accepted (host tensors,
+    page-locked ones allocated if not given).  Asynchronous on ``stream``
+    (default: the current stream of the current device): synchronise it before
+    reading the outputs or changing the inputs.  chunks: 0 = the library's
+    choice, else 1..64."""
+    B, K, V, _, out_tokens, out_n = _args(target_logits, draft_logits, draft_tokens, u_accept,
+                                          u_resample, lam, mode, out_tokens, out_n_accepted,
+                                          host=True)
+    if not 0 <= int(chunks) <= 64:
+        raise ValueError("chunks must be in 0..64")
+    dev = stream.device if stream is not None else torch.device("cuda",
+                                                                torch.cuda.current_device())
+    st = load().specv_verify_host(
+        target_logits.data_ptr(), draft_logits.data_ptr(), draft_tokens.data_ptr(),
+        u_accept.data_ptr(), u_resample.data_ptr(), lam.data_ptr(), B, K, V,
+        _dtype_code(target_logits), int(mode), out_tokens.data_ptr(), out_n.data_ptr(),
+        int(chunks), _stream_ptr(stream, dev))
+    _check(st, "specv_verify_host")
     return out_tokens, out_n
 
 

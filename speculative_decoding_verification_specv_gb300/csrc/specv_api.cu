@@ -569,6 +569,183 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
   return SPECV_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Verify on host buffers.  Per (device, stream) the library keeps a copy
+// stream, one event per chunk, and device staging memory for the inputs and
+// outputs of one call.  The inputs of chunk c (whole sequences) are copied on
+// the copy stream while the verify step of chunk c-1 runs on the caller's
+// stream, so the host link and the kernels overlap; the link (not HBM) bounds
+// such a call.  Staging grows by replacement after both streams have drained;
+// a call never runs under stream capture, so no graph can hold staging memory.
+constexpr int kHostMaxChunks = 64;
+constexpr int kHostAutoMaxChunks = 16;
+constexpr int64_t kHostChunkBytes = 64LL << 20;  // logit bytes per chunk (automatic choice)
+
+struct HostPipe {
+  int dev;
+  cudaStream_t stream;
+  cudaStream_t copy;
+  cudaEvent_t start;
+  cudaEvent_t ready[kHostMaxChunks];
+  void *stage;
+  size_t stage_bytes;
+};
+std::vector<HostPipe *> g_pipes;  // never freed while the process runs
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// The pipe of (dev, stream) with at least `need` bytes of staging memory.
+specv_status host_pipe(int dev, cudaStream_t stream, size_t need, HostPipe **out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  HostPipe *hp = nullptr;
+  for (HostPipe *x : g_pipes)
+    if (x->dev == dev && x->stream == stream) hp = x;
+  cudaError_t e = cudaSuccess;
+  if (hp == nullptr) {
+    hp = new HostPipe{};
+    hp->dev = dev;
+    hp->stream = stream;
+    e = cudaStreamCreateWithFlags(&hp->copy, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->start, cudaEventDisableTiming);
+    for (int c = 0; c < kHostMaxChunks && e == cudaSuccess; ++c)
+      e = cudaEventCreateWithFlags(&hp->ready[c], cudaEventDisableTiming);
+    if (e != cudaSuccess) {  // a partly built pipe is leaked, not reused
+      note_cuda_error(e);
+      (void)cudaGetLastError();
+      return SPECV_ERR_CUDA;
+    }
+    g_pipes.push_back(hp);
+  }
+  if (hp->stage_bytes < need) {
+    // earlier calls on this pipe may still read or write the old staging
+    e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(hp->copy);
+    if (e == cudaSuccess && hp->stage != nullptr) e = cudaFree(hp->stage);
+    if (e != cudaSuccess) {
+      note_cuda_error(e);
+      (void)cudaGetLastError();
+      return SPECV_ERR_CUDA;
+    }
+    hp->stage = nullptr;
+    hp->stage_bytes = 0;
+    const size_t sz = grow_to(need);
+    if (cudaMalloc(&hp->stage, sz) != cudaSuccess) {
+      (void)cudaGetLastError();
+      hp->stage = nullptr;
+      return SPECV_ERR_NO_MEMORY;
+    }
+    hp->stage_bytes = sz;
+  }
+  *out = hp;
+  return SPECV_OK;
+}
+
+specv_status verify_host(const void *target, const void *draft, const int32_t *tokens,
+                         const float *ua, const float *ur, const float *lam, int64_t B, int32_t K,
+                         int32_t V, specv_dtype dtype, specv_mode mode, int32_t *out_tokens,
+                         int32_t *out_n, int32_t chunks, void *stream_ptr) {
+  if (!target || !draft || !tokens || !ua || !ur || !lam || !out_tokens || !out_n)
+    return SPECV_ERR_INVALID_ARG;
+  if (!sizes_ok(B, K, V, dtype, mode) || chunks < 0 || chunks > kHostMaxChunks)
+    return SPECV_ERR_INVALID_ARG;
+  const size_t elem = dtype == SPECV_BF16 ? 2 : 4;
+  // staging larger than any device's memory is refused before the products overflow
+  if ((uint64_t)B * (uint64_t)(2 * K + 1) > ((uint64_t)1 << 50) / elem / (uint64_t)V)
+    return SPECV_ERR_NO_MEMORY;
+  int sms = kDefaultSMs;
+  int64_t l2 = kDefaultL2;
+  specv_status s = ensure_device(&sms, &l2);
+  if (s != SPECV_OK) return s;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return SPECV_ERR_UNSUPPORTED;
+  int dev = 0;
+  (void)cudaGetDevice(&dev);
+
+  // staging layout: target, draft, tokens, u_accept, u_resample, lambda,
+  // out_tokens, out_n (each region 256-byte aligned)
+  const size_t row_bytes = (size_t)V * elem;
+  const size_t t_bytes = (size_t)B * (K + 1) * row_bytes, d_bytes = (size_t)B * K * row_bytes;
+  const size_t bk4 = (size_t)B * K * 4, b4 = (size_t)B * 4, bk14 = (size_t)B * (K + 1) * 4;
+  const size_t o_d = round256(t_bytes), o_tok = o_d + round256(d_bytes);
+  const size_t o_ua = o_tok + round256(bk4), o_ur = o_ua + round256(bk4);
+  const size_t o_lam = o_ur + round256(b4), o_ot = o_lam + round256(b4);
+  const size_t o_on = o_ot + round256(bk14), need = o_on + round256(b4);
+  HostPipe *hp = nullptr;
+  if ((s = host_pipe(dev, stream, need, &hp)) != SPECV_OK) return s;
+  char *st = static_cast<char *>(hp->stage);
+
+  int64_t nc = chunks;
+  if (nc == 0) {
+    nc = (int64_t)((t_bytes + d_bytes + kHostChunkBytes - 1) / kHostChunkBytes);
+    nc = nc < 1 ? 1 : (nc > kHostAutoMaxChunks ? kHostAutoMaxChunks : nc);
+  }
+  if (nc > B) nc = B;
+  auto chunk_lo = [&](int64_t c) { return c * (B / nc) + (c < B % nc ? c : B % nc); };
+
+  // copies: after the caller's earlier work on `stream` (which may still read
+  // the staging), the per-sequence arrays first, then the logits chunk by chunk
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+  e = cudaEventRecord(hp->start, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->copy, hp->start, 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st + o_tok, tokens, bk4, h2d, hp->copy);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st + o_ua, ua, bk4, h2d, hp->copy);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st + o_ur, ur, b4, h2d, hp->copy);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st + o_lam, lam, b4, h2d, hp->copy);
+  for (int64_t c = 0; c < nc && e == cudaSuccess; ++c) {
+    const int64_t b0 = chunk_lo(c), b1 = chunk_lo(c + 1);
+    const size_t ot = (size_t)b0 * (K + 1) * row_bytes, od = (size_t)b0 * K * row_bytes;
+    e = cudaMemcpyAsync(st + ot, static_cast<const char *>(target) + ot,
+                        (size_t)(b1 - b0) * (K + 1) * row_bytes, h2d, hp->copy);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(st + o_d + od, static_cast<const char *>(draft) + od,
+                          (size_t)(b1 - b0) * K * row_bytes, h2d, hp->copy);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->ready[c], hp->copy);
+  }
+  if (e != cudaSuccess) {  // nothing of this call has been launched on `stream`
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  // the verify step of each chunk, once its inputs are in
+  for (int64_t c = 0; c < nc && s == SPECV_OK; ++c) {
+    const int64_t b0 = chunk_lo(c), b1 = chunk_lo(c + 1);
+    e = cudaStreamWaitEvent(stream, hp->ready[c], 0);
+    if (e != cudaSuccess) {
+      note_cuda_error(e);
+      s = SPECV_ERR_CUDA;
+      break;
+    }
+    s = run(st + (size_t)b0 * (K + 1) * row_bytes, st + o_d + (size_t)b0 * K * row_bytes,
+            reinterpret_cast<const int32_t *>(st + o_tok) + b0 * K,
+            reinterpret_cast<const float *>(st + o_ua) + b0 * K,
+            reinterpret_cast<const float *>(st + o_ur) + b0,
+            reinterpret_cast<const float *>(st + o_lam) + b0, b1 - b0, K, V, dtype, mode,
+            reinterpret_cast<int32_t *>(st + o_ot) + b0 * (K + 1),
+            reinterpret_cast<int32_t *>(st + o_on) + b0, nullptr, nullptr, nullptr, stream);
+  }
+  if (s != SPECV_OK) {
+    // join the copy stream so that the caller's stream covers every copy issued
+    (void)cudaStreamWaitEvent(stream, hp->ready[nc - 1], 0);
+    (void)cudaGetLastError();
+    return s;
+  }
+  e = cudaMemcpyAsync(out_tokens, st + o_ot, bk14, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out_n, st + o_on, b4, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  return SPECV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -580,6 +757,15 @@ specv_status specv_verify(const void *target_logits, const void *draft_logits,
                           int32_t *out_n_accepted, void *stream) {
   return run(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lambda, B, K, V,
              dtype, mode, out_tokens, out_n_accepted, nullptr, nullptr, nullptr, stream);
+}
+
+specv_status specv_verify_host(const void *target_logits, const void *draft_logits,
+                               const int32_t *draft_tokens, const float *u_accept,
+                               const float *u_resample, const float *lambda, int64_t B, int32_t K,
+                               int32_t V, specv_dtype dtype, specv_mode mode, int32_t *out_tokens,
+                               int32_t *out_n_accepted, int32_t chunks, void *stream) {
+  return verify_host(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lambda, B,
+                     K, V, dtype, mode, out_tokens, out_n_accepted, chunks, stream);
 }
 
 specv_status specv_verify_debug(const void *target_logits, const void *draft_logits,

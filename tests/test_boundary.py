@@ -140,3 +140,42 @@ def test_plan_cluster_size_model(lib):
     for B, K, V, dt in [(16, 8, 128256, 0), (64, 4, 32000, 1), (8, 4, 128256, 1), (3, 2, 9000, 0)]:
         S = specv.plan(B, K, V, dt)["cluster"]
         assert 1 <= S <= 16
+
+
+def _host_call(B=2, K=3, V=100, dtype=0, mode=0, chunks=0, null=None):
+    ptrs = [FAKE] * 8
+    if null is not None:
+        ptrs[null] = None
+    t, d, tok, ua, ur, lam, ot, on = ptrs
+    return specv.raw_call("specv_verify_host", t, d, tok, ua, ur, lam, B, K, V, dtype, mode, ot,
+                          on, chunks, None)
+
+
+@pytest.mark.parametrize("kw", [dict(null=0), dict(null=5), dict(null=7), dict(B=0), dict(K=4097),
+                                dict(V=-1), dict(dtype=3), dict(mode=3), dict(chunks=-1),
+                                dict(chunks=65)])
+def test_host_entry_point_validates(lib, kw):
+    assert _host_call(**kw) == 1
+
+
+def test_host_entry_point_refuses_staging_beyond_any_device(lib):
+    # 2^20 x 2049 rows of 2^20 fp32 logits: sizes the verify step accepts, but
+    # petabytes of staging, refused before anything is allocated or launched
+    assert _host_call(B=1 << 20, K=1024, V=1 << 20) == 4
+
+
+def test_host_binding_checks_tensors():
+    import torch
+    B, K, V = 3, 2, 50
+    x = dict(target_logits=torch.zeros(B, K + 1, V), draft_logits=torch.zeros(B, K, V),
+             draft_tokens=torch.zeros(B, K, dtype=torch.int32),
+             u_accept=torch.zeros(B, K), u_resample=torch.zeros(B), lam=torch.zeros(B))
+    outs = dict(out_tokens=torch.empty(B, K + 1, dtype=torch.int32),
+                out_n_accepted=torch.empty(B, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        specv.verify_host(*x.values(), chunks=65, **outs)
+    bad = dict(x, draft_tokens=torch.zeros(B, K, dtype=torch.int64))
+    with pytest.raises(TypeError):
+        specv.verify_host(*bad.values(), **outs)
+    with pytest.raises(ValueError):  # CUDA-side entry point on host tensors
+        specv.verify(*x.values())
