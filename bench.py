@@ -40,7 +40,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_specv_gb300", "csrc", f)
                   for f in ("specv_rows.cu", "specv_device.cuh", "specv_block.cuh",
-                            "specv_segments.cuh", "specv_stream.cuh", "specv_internal.h")]
+                            "specv_segments.cuh", "specv_stream.cuh", "specv_ring.cuh",
+                            "specv_internal.h")]
 
 
 def parse():
@@ -96,7 +97,7 @@ def job_throughput(rows_per_step, steps, ws, slowest_ms):
 
 
 # kernel function timed for the roofline, by the planner's kernel name
-PLAN_KERNEL_FUNCTION = {"tile": "tile_kernel", "rows-stream": "rows_kernel",
+PLAN_KERNEL_FUNCTION = {"tile": "tile_kernel", "rows-stream": "rows_kernel", "rows-ring": "rows_kernel",
                         "rows-resident": "resident_kernel", "tile-tma": "tile_tma_kernel",
                         "rows-spec": "resident_kernel", "rows-sweep": "sweep_kernel"}
 
@@ -109,6 +110,24 @@ def measured_peak():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def capture_graph(launch, dev):
+    """A CUDA graph of one launch() call, captured on a side stream after one
+    plain call on that same stream: the library keeps its scratch per stream
+    and creates it on the first call, so the captured graph holds the verify
+    launches only (no allocation or clearing nodes), as it would for a user
+    who calls once before capturing."""
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        launch()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        launch()
+    torch.cuda.synchronize(dev)
+    return graph
 
 
 def kernel_source_hash():
@@ -317,11 +336,7 @@ def run_stats(args):
     def launch():
         specv.acceptance_rates(x["target_logits"], x["draft_logits"], x["lam"], mode=mode,
                                out=out, stream=torch.cuda.current_stream(dev))
-    launch()
-    torch.cuda.synchronize(dev)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        launch()
+    graph = capture_graph(launch, dev)
     stream = torch.cuda.current_stream(dev)
     l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
     elem = 2 if w.dtype == "bf16" else 4
@@ -382,11 +397,12 @@ def run_tree(args):
     alg = (N + 1 + M) * B * w.V * elem
     args_t = (x["target_logits"], x["draft_logits"], x["parent"], x["draft_row"], x["tokens"],
               x["u_accept"], x["u_resample"], x["lam"])
-    specv.verify_tree(*args_t, mode=mode)
-    torch.cuda.synchronize(dev)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        out = specv.verify_tree(*args_t, mode=mode)
+    res = {}
+
+    def launch():
+        res["out"] = specv.verify_tree(*args_t, mode=mode)
+    graph = capture_graph(launch, dev)
+    out = res["out"]
     stream = torch.cuda.current_stream(dev)
     l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
     flush = L2Flush(dev, l2) if alg < 2 * l2 else None
@@ -460,16 +476,12 @@ def main():
                      stream=torch.cuda.current_stream(dev))
 
     # One step = one specv_verify call.  By default it is captured once in a
-    # CUDA graph (kernel, workspace alloc/memset/free nodes) and replayed, so
-    # the device time is not hidden behind host launch overhead.
+    # CUDA graph (the verify launches only: the stream's scratch exists before
+    # the capture) and replayed, so the device time is not hidden behind host
+    # launch overhead.
     graph = None
     if not args.no_graph:
-        launch()
-        torch.cuda.synchronize(dev)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            launch()
-        torch.cuda.synchronize(dev)
+        graph = capture_graph(launch, dev)
 
     def step():
         if graph is not None:
@@ -582,14 +594,14 @@ def main():
                 else "fallback 6.8 TB/s",
                 "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                 "kernel": ("rows_greedy_kernel" if args.mode == "greedy" and
-                           plan["kernel"] == "rows-stream" else
+                           plan["kernel"] in ("rows-stream", "rows-ring") else
                            PLAN_KERNEL_FUNCTION.get(plan["kernel"], plan["kernel"])),
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "launch_ms_mean": kern_ms, "launch_ms_min": min(per_call_ms),
                 "timing": ("CUDA events around each replay of a CUDA graph holding one "
                            "specv_verify call" if graph is not None else
                            "CUDA events around each specv_verify call") +
-                          " on its stream (the kernel plus a B*4-byte workspace memset)"}
+                          " on its stream (the verify launches only)"}
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
         cpu = cpu_baseline(w, mode, args.cpu_seconds)

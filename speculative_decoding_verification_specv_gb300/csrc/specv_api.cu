@@ -167,7 +167,8 @@ specv_status ensure_device(int *sms_out, int64_t *l2_out) {
 
 struct Plan {
   int kernel;            // 0 tile, 1 streaming row kernel, 2 resident row kernel, 3 TMA tile,
-                         // 4 resident row kernel reading in place (speculative sampling)
+                         // 4 resident row kernel reading in place (speculative sampling),
+                         // 5 sweep kernel, 6 streaming row kernel fed by the bulk-copy ring
   int cluster;           // CTAs per cluster (row kernels)
   int64_t ctas;          // CTAs of the row kernels (tile kernel: tiles)
   int64_t ws_bytes;      // scratch bytes
@@ -208,6 +209,30 @@ int split_from_env() {
   const char *s = std::getenv("SPECV_SAMPLE_SPLIT");
   if (!s || !*s) return -1;
   return s[0] == '1' ? 1 : (s[0] == '0' ? 0 : -1);
+}
+
+// SPECV_ROWS_RING=0/1 forces the streaming row kernel's register loads or its
+// bulk-copy ring (16-byte aligned rows); -1: the plan.
+int ring_from_env() {
+  const char *s = std::getenv("SPECV_ROWS_RING");
+  if (!s || !*s) return -1;
+  return s[0] == '1' ? 1 : (s[0] == '0' ? 0 : -1);
+}
+
+// Whether the streaming row kernel (grid of `ctas` CTAs) takes the bulk-copy
+// ring: rows on 16-byte boundaries, a grid of at most two waves of 4 CTAs per
+// SM (where CTAs that load in step leave HBM idle while they fold), and the
+// greedy or logit-mixture mode.  Measured on the Qwen-shaped batch (B = 32,
+// K = 5, V = 152064 bf16, one wave): greedy 32.7 vs 34.9 us, logit 59.7 vs
+// 61.3 us, but probability mode 46.9 vs 45.0 us (the ring folds two groups per
+// thread per chunk instead of four, and that mode's folds are the heaviest
+// part of its step).  Grids of many waves desynchronise by themselves and
+// stream at the copy peak with register loads.
+bool ring_choice(bool aligned, int64_t ctas, int sms, int mode) {
+  if (!aligned) return false;
+  const int env = ring_from_env();
+  if (env >= 0) return env == 1;
+  return mode != SPECV_PROB_MIX && ctas <= 2 * 4LL * sms;
 }
 
 // "stream", "resident" or "spec" forces a row-kernel variant (tuning and tests).
@@ -285,7 +310,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     }
     while (S > 1 && P * S > INT32_MAX) S /= 2;
     if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
-    p->kernel = 1;
+    p->kernel = ring_choice(aligned && row_bytes % 16 == 0, P * S, sms, mode) ? 6 : 1;
     p->cluster = S;
     p->ctas = P * S;
     p->num_groups = (int)G;
@@ -358,6 +383,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     while (S > 1 && P * S > INT32_MAX) S /= 2;
     if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
   }
+  if (kernel == 1 && ring_choice(aligned && row_bytes % 16 == 0, P * S, sms, mode)) kernel = 6;
   p->kernel = kernel;
   p->cluster = S;
   p->ctas = P * S;
@@ -548,7 +574,8 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     a.stats_groups_per_slice = p.groups_per_slice;
     a.stats_seg_tiles = p.seg_tiles;
     a.stats_segs_per_slice = p.segs_per_slice;
-    if (e == cudaSuccess) e = specv::rows_launch(a, bf16, mode, aligned, p.cluster, p.ctas, stream);
+    if (e == cudaSuccess)
+      e = specv::rows_launch(a, bf16, mode, aligned, p.cluster, p.ctas, stream, p.kernel == 6);
     if (e == cudaSuccess && a.defer_sampling) {
       specv::RowArgs a2 = a;
       a2.groups_per_slice = p.sample_gps;

@@ -239,8 +239,10 @@ cudaError_t sweep_launch(const SweepArgs &a, int dtype_bf16, int mode, int64_t g
                          int smem_bytes, cudaStream_t stream);
 
 cudaError_t rows_prepare();
+// ring = true (16-byte aligned rows only): the slices stream through the
+// shared-memory ring of bulk copies of specv_ring.cuh instead of register loads.
 cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
-                        int64_t grid, cudaStream_t stream);
+                        int64_t grid, cudaStream_t stream, bool ring = false);
 // The deferred token draws: one cluster of S CTAs per sequence (grid B * S),
 // after a rows_launch with defer_sampling = 1 on the same stream.
 cudaError_t rows_sample_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,

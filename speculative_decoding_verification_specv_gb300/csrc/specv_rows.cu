@@ -42,6 +42,7 @@
 #include "specv_block.cuh"
 #include "specv_device.cuh"
 #include "specv_internal.h"
+#include "specv_ring.cuh"
 #include "specv_segments.cuh"
 #include "specv_stream.cuh"
 
@@ -54,6 +55,17 @@ namespace {
 constexpr int kNT = kRowThreads;  // threads per CTA
 constexpr int kNW = kNT / 32;     // warps per CTA
 constexpr int kUnroll = 4;        // 16-byte groups per thread per batch
+constexpr int kRingU = kRingChunkGroups / kNT;  // groups per thread per row of a ring chunk
+static_assert(kRingChunkGroups % kNT == 0, "a ring chunk is whole groups per thread");
+
+// Marker in the scratch statistics of a position whose bulk copies did not
+// land in time (a sum of exponentials is never negative).
+constexpr float kCopyFailedSum = -1.0f;
+// The same marker in the greedy candidates (an index is never negative).
+constexpr int kCopyFailedIndex = -2;
+
+// Stages of the bulk-copy ring (dynamic shared memory of the ring variants).
+extern __shared__ __align__(128) unsigned char g_ring_buf[];
 
 struct Broadcast {
   int n;        // first rejected position (K if none), -1 if the sequence is invalid
@@ -64,7 +76,9 @@ struct Broadcast {
 
 struct __align__(16) RowsShared {
   BlockScratch<kNT> bs;
+  RingState ring;
   float part[4];
+  int pfail;              // this CTA's bulk copies did not land in time
   int last;
   Broadcast bc;
   float masses[2][kMaxCluster];
@@ -248,7 +262,7 @@ __device__ void draw_token(RowsShared &sh, cg::cluster_group &cluster, int S, in
   if (lane == 0) *out = tok;
 }
 
-template <typename T, int MODE, bool ALIGNED>
+template <typename T, int MODE, bool ALIGNED, bool RING>
 __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   constexpr int VW = Elem<T>::kPerVec;
   __shared__ RowsShared sh;
@@ -267,17 +281,39 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   const int g_lo = rank * a.groups_per_slice;
   const int g_hi = min(a.num_groups, g_lo + a.groups_per_slice);
   const float lam_seq = a.lam[b];
+  // The token-draw launch that follows (deferred sampling) may be scheduled
+  // from now on; it waits for this whole grid to complete before it reads
+  // anything this grid writes.
+  if (a.defer_sampling) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---------------------------------------------------------------- phase 1
   float mA = -INFINITY, sA = 0.0f, mB = -INFINITY, sB = 0.0f;
   const int seg_groups = a.seg_tiles * kSegGroups;
   const int nseg = a.segs_per_slice;
-  if (!pair && a.ws_seg != nullptr)
+  bool copy_ok = true;
+  if (!pair && a.ws_seg != nullptr) {
     bonus_segment_stats<T, ALIGNED>(rowA, V, g_lo, g_hi, seg_groups, nseg,
                                     a.ws_seg + (b * S + rank) * (int64_t)nseg, mA, sA);
-  else
+  } else if (RING) {
+    // the slice through the bulk-copy ring: thread t folds groups t, t + kNT, ... of each chunk
+    copy_ok = ring_stream<kNT>(sh.ring, g_ring_buf, rowA, rowB, pair, g_lo, g_hi,
+                               [&](const uint4 *cA, const uint4 *cB, int cnt, int) {
+                                 uint4 za[kRingU], zb[kRingU];
+                                 bool ok[kRingU];
+#pragma unroll
+                                 for (int u = 0; u < kRingU; ++u) {
+                                   const int g = (int)threadIdx.x + u * kNT;
+                                   ok[u] = g < cnt;
+                                   za[u] = ok[u] ? cA[g] : make_uint4(0u, 0u, 0u, 0u);
+                                   zb[u] = (ok[u] && pair) ? cB[g] : za[u];
+                                 }
+                                 fold_batch<T, MODE, kRingU>(za, zb, ok, pair, lam_seq, mA, sA,
+                                                             mB, sB);
+                               });
+  } else {
     slice_stats<T, MODE, ALIGNED, kNT, kUnroll>(rowA, rowB, pair, lam_seq, V, g_lo, g_hi, mA, sA,
                                                  mB, sB);
+  }
   block_merge_stats<kNT>(sh.bs, mA, sA, mB, sB);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -285,15 +321,19 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
     sh.part[1] = sA;
     sh.part[2] = mB;
     sh.part[3] = sB;
+    sh.pfail = copy_ok ? 0 : 1;
   }
   cluster.sync();  // partials of every rank are visible
   if (rank == 0 && threadIdx.x == 0) {
     float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
+    int fail = 0;
     for (int r = 0; r < S; ++r) {
       const float *pr = cluster.map_shared_rank(sh.part, r);
       merge_stats(m0, s0, pr[0], pr[1]);
       merge_stats(m1, s1, pr[2], pr[3]);
+      fail |= *cluster.map_shared_rank(&sh.pfail, r);
     }
+    if (fail) s0 = s1 = kCopyFailedSum;
     a.ws_stats[p] = make_float4(m0, s0, m1, s1);
     __threadfence();
     const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
@@ -337,7 +377,13 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
       if (rej != 0u && n == K) n = i0 + __ffs(rej) - 1;
     }
     const bool all_tok = __all_sync(0xffffffffu, lane_ok);  // every lane votes
-    const bool valid = lam_ok && all_tok;
+    bool copy_err = false;
+    if (RING) {  // a position whose bulk copies did not land: the sequence reports -2
+      for (int j = lane; j <= K; j += 32)
+        copy_err = copy_err || __ldcg(&a.ws_stats[b * (K + 1) + j]).y == kCopyFailedSum;
+      copy_err = __any_sync(0xffffffffu, copy_err);
+    }
+    const bool valid = lam_ok && all_tok && !copy_err;
     if (a.dbg_lse) {
       for (int j = lane; j <= K; j += 32) {
         const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + j]);
@@ -351,7 +397,7 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
       if (!valid || j != n) a.out_tokens[b * (K + 1) + j] = out;
     }
     if (lane == 0) {
-      a.out_n[b] = valid ? n : -1;
+      a.out_n[b] = valid ? n : (copy_err ? -2 : -1);
       Broadcast bc;
       bc.n = valid ? n : -1;
       bc.u = a.u_resample[b];
@@ -403,6 +449,9 @@ __global__ void __launch_bounds__(kNT, 4) rows_sample_kernel(RowArgs a) {
   const int rank = (int)cluster.block_rank();
   const int64_t b = (int64_t)blockIdx.x / S;
   const int K = a.K, V = a.V;
+  // launched as a programmatic dependent of the statistics launch: wait until
+  // that grid has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int n = a.out_n[b];
   if (n < 0) return;  // invalid sequence (or a timed-out copy): nothing to draw
   const float lam = a.lam[b];
@@ -446,7 +495,7 @@ __global__ void __launch_bounds__(kNT, 4) rows_sample_kernel(RowArgs a) {
 // accepts x_i iff it is the argmax of row i, stops at the first mismatch and
 // emits that argmax there, or the argmax of target row K when every draft
 // matches.  There is no sampling pass: each logit is read once.
-template <typename T, bool ALIGNED>
+template <typename T, bool ALIGNED, bool RING>
 __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
   constexpr int VW = Elem<T>::kPerVec;
   __shared__ RowsShared sh;
@@ -469,7 +518,28 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
 
   float best = -INFINITY;
   int bidx = INT_MAX;
-  for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += kNT * kUnroll) {
+  bool copy_ok = true;
+  if (RING) {
+    copy_ok = ring_stream<kNT>(sh.ring, g_ring_buf, rowA, rowB, pair, g_lo, g_hi,
+                               [&](const uint4 *cA, const uint4 *cB, int cnt, int c_lo) {
+#pragma unroll
+                                 for (int u = 0; u < kRingU; ++u) {
+                                   const int g = (int)threadIdx.x + u * kNT;
+                                   if (g < cnt) {
+                                     const uint4 za = cA[g];
+                                     const uint4 zb = pair ? cB[g] : za;
+#pragma unroll
+                                     for (int e = 0; e < VW; ++e) {
+                                       const float zt = Elem<T>::get(za, e);
+                                       const float w =
+                                           pair ? greedy_score(zt, Elem<T>::get(zb, e), lam) : zt;
+                                       argmax_merge(best, bidx, w, (c_lo + g) * VW + e);
+                                     }
+                                   }
+                                 }
+                               });
+  }
+  for (int g0 = g_lo + (int)threadIdx.x; !RING && g0 < g_hi; g0 += kNT * kUnroll) {
     uint4 za[kUnroll], zb[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -507,15 +577,19 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
     for (int w = 0; w < kNW; ++w) argmax_merge(m, ix, sh.bs.red[w][0], __float_as_int(sh.bs.red[w][1]));
     sh.part[0] = m;
     sh.part[1] = __int_as_float(ix);
+    sh.pfail = copy_ok ? 0 : 1;
   }
   cluster.sync();  // candidates of every rank are visible
   if (rank == 0 && threadIdx.x == 0) {
     float m = -INFINITY;
     int ix = INT_MAX;
+    int fail = 0;
     for (int r = 0; r < S; ++r) {
       const float *pr = cluster.map_shared_rank(sh.part, r);
       argmax_merge(m, ix, pr[0], __float_as_int(pr[1]));
+      fail |= *cluster.map_shared_rank(&sh.pfail, r);
     }
+    if (fail) ix = kCopyFailedIndex;
     a.ws_stats[p] = make_float4(m, __int_as_float(ix), 0.0f, 0.0f);
     __threadfence();
     const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
@@ -546,31 +620,38 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
     const unsigned rej = __ballot_sync(0xffffffffu, rejected);
     if (rej != 0u && n == K) n = i0 + __ffs(rej) - 1;
   }
-  const bool valid = lam_ok && __all_sync(0xffffffffu, lane_ok);  // every lane votes
+  bool copy_err = false;
+  if (RING) {  // a position whose bulk copies did not land: the sequence reports -2
+    for (int j = lane; j <= K; j += 32)
+      copy_err = copy_err ||
+                 __float_as_int(__ldcg(&a.ws_stats[b * (K + 1) + j]).y) == kCopyFailedIndex;
+    copy_err = __any_sync(0xffffffffu, copy_err);
+  }
+  const bool valid = lam_ok && __all_sync(0xffffffffu, lane_ok) && !copy_err;  // every lane votes
   for (int j = lane; j <= K; j += 32) {
     int out = -1;
     if (valid && j < n) out = a.tokens[b * K + j];
     if (valid && j == n) out = __float_as_int(__ldcg(&a.ws_stats[b * (K + 1) + n]).y);
     a.out_tokens[b * (K + 1) + j] = out;
   }
-  if (lane == 0) a.out_n[b] = valid ? n : -1;
+  if (lane == 0) a.out_n[b] = valid ? n : (copy_err ? -2 : -1);
 }
 
-template <typename T, int MODE, bool ALIGNED>
+template <typename T, int MODE, bool ALIGNED, bool RING>
 constexpr void (*row_kernel_of())(RowArgs) {
   if constexpr (MODE == kGreedy)
-    return rows_greedy_kernel<T, ALIGNED>;
+    return rows_greedy_kernel<T, ALIGNED, RING>;
   else
-    return rows_kernel<T, MODE, ALIGNED>;
+    return rows_kernel<T, MODE, ALIGNED, RING>;
 }
 
-template <typename T, int MODE, bool ALIGNED>
+template <typename T, int MODE, bool ALIGNED, bool RING = false>
 cudaError_t launch_one(const RowArgs &a, int S, int64_t grid, cudaStream_t stream) {
-  void (*kern)(RowArgs) = row_kernel_of<T, MODE, ALIGNED>();
+  void (*kern)(RowArgs) = row_kernel_of<T, MODE, ALIGNED, RING>();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kNT, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = RING ? kRingSmemBytes : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -589,20 +670,34 @@ cudaError_t launch_sample_one(const RowArgs &a, int S, int64_t grid, cudaStream_
   cfg.blockDim = dim3(kNT, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)S;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: scheduled while the statistics launch
+  // finishes, released by its completion (griddepcontrol.wait)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, rows_sample_kernel<T, MODE, ALIGNED>, a);
 }
 
 template <typename T, int MODE, bool ALIGNED>
 cudaError_t prepare_one() {
-  cudaError_t e = cudaFuncSetAttribute(row_kernel_of<T, MODE, ALIGNED>(),
+  cudaError_t e = cudaFuncSetAttribute(row_kernel_of<T, MODE, ALIGNED, false>(),
                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if constexpr (ALIGNED) {
+    void (*ring)(RowArgs) = row_kernel_of<T, MODE, true, true>();
+    cudaError_t er = cudaFuncSetAttribute(ring, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (er == cudaSuccess)
+      er = cudaFuncSetAttribute(ring, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemBytes);
+    if (er == cudaSuccess)
+      er = cudaFuncSetAttribute(ring, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess) e = er;
+  }
   if constexpr (MODE != kGreedy) {
     const cudaError_t e2 = cudaFuncSetAttribute(rows_sample_kernel<T, MODE, ALIGNED>,
                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -635,7 +730,17 @@ cudaError_t rows_prepare() {
 }
 
 cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
-                        int64_t grid, cudaStream_t stream) {
+                        int64_t grid, cudaStream_t stream, bool ring) {
+  if (ring && aligned) {
+    if (mode == kGreedy)
+      return dtype_bf16 ? launch_one<uint16_t, kGreedy, true, true>(a, S, grid, stream)
+                        : launch_one<float, kGreedy, true, true>(a, S, grid, stream);
+    if (dtype_bf16)
+      return mode == kProbMix ? launch_one<uint16_t, kProbMix, true, true>(a, S, grid, stream)
+                              : launch_one<uint16_t, kLogitMix, true, true>(a, S, grid, stream);
+    return mode == kProbMix ? launch_one<float, kProbMix, true, true>(a, S, grid, stream)
+                            : launch_one<float, kLogitMix, true, true>(a, S, grid, stream);
+  }
   if (mode == kGreedy) {
     if (dtype_bf16)
       return aligned ? launch_one<uint16_t, kGreedy, true>(a, S, grid, stream)

@@ -22,11 +22,90 @@
 
 namespace specv {
 
+// Elementwise maximum of two pairs of bf16 values (exact: the result is one of
+// the inputs).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Maximum of the elements of groups z[0..U) with ok[u] set (-inf if none).
+// bf16 rows reduce packed pairs first (one max per two elements), then widen
+// the two halves of the surviving pair; fp32 rows take one max per element.
+template <typename T, int U>
+__device__ __forceinline__ float batch_max(const uint4 (&z)[U], const bool (&ok)[U]) {
+  if constexpr (sizeof(T) == 2) {
+    uint32_t m = 0xff80ff80u;  // (-inf, -inf)
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (ok[u]) m = bf16x2_max(bf16x2_max(m, z[u].x), bf16x2_max(z[u].y, bf16x2_max(z[u].z, z[u].w)));
+    return fmaxf(__uint_as_float(m & 0xffff0000u), __uint_as_float(m << 16));
+  } else {
+    float m = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (ok[u]) m = fmaxf(fmaxf(__uint_as_float(z[u].x), __uint_as_float(z[u].y)),
+                           fmaxf(fmaxf(__uint_as_float(z[u].z), __uint_as_float(z[u].w)), m));
+    return m;
+  }
+}
+
+// Folds one batch of U groups per row (groups with ok[u] unset are skipped)
+// into the running statistics (mA, sA) of the A row and, if `pair`, (mB, sB)
+// of the B row.
+template <typename T, int MODE, int U>
+__device__ __forceinline__ void fold_batch(const uint4 (&za)[U], const uint4 (&zb)[U],
+                                           const bool (&ok)[U], bool pair, float lam, float &mA,
+                                           float &sA, float &mB, float &sB) {
+  constexpr int VW = Elem<T>::kPerVec;
+  // A-row value of element e of group u: the target logit, or in logit mode
+  // the mixed logit (entries past V stay -inf).
+  auto a_val = [&](int u, int e) -> float {
+    const float zt = Elem<T>::get(za[u], e);
+    if (MODE == kLogitMix && pair) {
+      const float zq = Elem<T>::get(zb[u], e);
+      return zq == -INFINITY ? -INFINITY : mix_logit(zt, zq, lam);
+    }
+    return zt;
+  };
+  float bmA;
+  if (MODE == kLogitMix && pair) {
+    bmA = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (ok[u]) {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) bmA = fmaxf(bmA, a_val(u, e));
+      }
+  } else {
+    bmA = batch_max<T, U>(za, ok);
+  }
+  const float bmB = pair ? batch_max<T, U>(zb, ok) : -INFINITY;
+  if (bmA > mA) {
+    sA = __fmul_rn(sA, exp_shifted(mA, bmA));
+    mA = bmA;
+  }
+  if (pair && bmB > mB) {
+    sB = __fmul_rn(sB, exp_shifted(mB, bmB));
+    mB = bmB;
+  }
+  const float nA = -__fmul_rn(mA, kLog2e), nB = -__fmul_rn(mB, kLog2e);
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    if (ok[u]) {
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        sA = __fadd_rn(sA, ex2(__fmaf_rn(a_val(u, e), kLog2e, nA)));
+        if (pair) sB = __fadd_rn(sB, ex2(__fmaf_rn(Elem<T>::get(zb[u], e), kLog2e, nB)));
+      }
+    }
+}
+
 template <typename T, int MODE, bool ALIGNED, int NT, int U>
 __device__ __forceinline__ void slice_stats(const T *rowA, const T *rowB, bool pair, float lam,
                                             int V, int g_lo, int g_hi, float &mA, float &sA,
                                             float &mB, float &sB) {
-  constexpr int VW = Elem<T>::kPerVec;
   for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += NT * U) {
     uint4 za[U], zb[U];
     bool ok[U];
@@ -39,44 +118,7 @@ __device__ __forceinline__ void slice_stats(const T *rowA, const T *rowB, bool p
         if (pair) zb[u] = load_group<T, ALIGNED>(rowB, g, V);
       }
     }
-    // A-row value of element e of group u: the target logit, or in logit mode
-    // the mixed logit (entries past V stay -inf).
-    auto a_val = [&](int u, int e) -> float {
-      const float zt = Elem<T>::get(za[u], e);
-      if (MODE == kLogitMix && pair) {
-        const float zq = Elem<T>::get(zb[u], e);
-        return zq == -INFINITY ? -INFINITY : mix_logit(zt, zq, lam);
-      }
-      return zt;
-    };
-    float bmA = -INFINITY, bmB = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (ok[u]) {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) {
-          bmA = fmaxf(bmA, a_val(u, e));
-          if (pair) bmB = fmaxf(bmB, Elem<T>::get(zb[u], e));
-        }
-      }
-    if (bmA > mA) {
-      sA = __fmul_rn(sA, exp_shifted(mA, bmA));
-      mA = bmA;
-    }
-    if (pair && bmB > mB) {
-      sB = __fmul_rn(sB, exp_shifted(mB, bmB));
-      mB = bmB;
-    }
-    const float nA = -__fmul_rn(mA, kLog2e), nB = -__fmul_rn(mB, kLog2e);
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (ok[u]) {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) {
-          sA = __fadd_rn(sA, ex2(__fmaf_rn(a_val(u, e), kLog2e, nA)));
-          if (pair) sB = __fadd_rn(sB, ex2(__fmaf_rn(Elem<T>::get(zb[u], e), kLog2e, nB)));
-        }
-      }
+    fold_batch<T, MODE, U>(za, zb, ok, pair, lam, mA, sA, mB, sB);
   }
 }
 

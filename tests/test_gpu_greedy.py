@@ -33,7 +33,7 @@ def specv():
 
 @pytest.fixture
 def env_guard():
-    keys = ("SPECV_CLUSTER_SIZE", "SPECV_ROWS_VARIANT")
+    keys = ("SPECV_CLUSTER_SIZE", "SPECV_ROWS_VARIANT", "SPECV_ROWS_RING")
     old = {k: os.environ.get(k) for k in keys}
     yield
     for k, v in old.items():
@@ -131,11 +131,14 @@ def test_greedy_ragged_shapes(specv, shape, lam):
     _check(specv, x)
 
 
+@pytest.mark.parametrize("ring", ["0", "1"], ids=["loads", "ring"])
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 7, 8, 16])
-def test_greedy_every_cluster_size_with_ties(specv, env_guard, S):
+def test_greedy_every_cluster_size_with_ties(specv, env_guard, S, ring):
     """Integer logits in a small range: every row has many equal maxima, spread
-    over all ranks of the cluster; the first one in index order must win."""
+    over all ranks of the cluster; the first one in index order must win (with
+    register loads and with the bulk-copy ring)."""
     os.environ["SPECV_CLUSTER_SIZE"] = str(S)
+    os.environ["SPECV_ROWS_RING"] = ring
     B, K, V = 6, 3, 50000
     g = torch.Generator().manual_seed(100 + S)
     zt = torch.randint(-3, 4, (B, K + 1, V), generator=g).float()
@@ -145,7 +148,8 @@ def test_greedy_every_cluster_size_with_ties(specv, env_guard, S):
          "u_accept": torch.rand((B, K), generator=g).to(DEV),
          "u_resample": torch.rand((B,), generator=g).to(DEV),
          "lam": torch.tensor([0.0, 0.5, 0.25, 1.0, 0.0, 0.75], dtype=torch.float32, device=DEV)}
-    assert specv.plan(B, K, V, 0, 2)["cluster"] == S
+    p = specv.plan(B, K, V, 0, 2)
+    assert p["cluster"] == S and p["kernel"] == ("rows-ring" if ring == "1" else "rows-stream")
     x = _follow_argmax(x, frac=0.6, seed=S)
     _check(specv, x)
     # the all-equal row: the argmax is index 0
