@@ -211,6 +211,15 @@ int split_from_env() {
   return s[0] == '1' ? 1 : (s[0] == '0' ? 0 : -1);
 }
 
+// SPECV_TILE_STAGE_KB=8..40 sets the bytes of one staged tile of the TMA tile
+// kernel (tuning); 0: the default.
+int tile_stage_from_env() {
+  const char *s = std::getenv("SPECV_TILE_STAGE_KB");
+  if (!s || !*s) return 0;
+  const int v = std::atoi(s);
+  return (v >= 8 && v <= 40) ? v * 1024 : 0;
+}
+
 // SPECV_ROWS_RING=0/1 forces the streaming row kernel's register loads or its
 // bulk-copy ring (16-byte aligned rows); -1: the plan.
 int ring_from_env() {
@@ -274,7 +283,8 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
       // two alternating tile buffers of <= 40 KiB each; one round of stage-A
       // row tasks (2K+1 per sequence) for the CTA's threads; at most one
       // stage-B lane group per sequence
-      ts = (int)(kTmaTileStageBytes / data_bytes);
+      const int env_stage = tile_stage_from_env();
+      ts = (int)((env_stage ? env_stage : kTmaTileStageBytes) / data_bytes);
       const int by_rows = specv::kTileThreads / (2 * K + 1);
       if (ts > by_rows && by_rows >= 1) ts = by_rows;
       if (ts > specv::kTmaTileMaxSeqs) ts = specv::kTmaTileMaxSeqs;
