@@ -17,7 +17,13 @@ constexpr int kMaxDevices = 64;
 constexpr int kDefaultSMs = 152;        // used by specv_plan when no device is visible
 constexpr int64_t kDefaultL2 = 126LL * 1024 * 1024;
 constexpr int kTileSmemBudget = 48 * 1024;
-constexpr int kTmaTileStageBytes = 40 * 1024;  // target + draft rows of one staged tile
+constexpr int kTmaTileStageBytes = 40 * 1024;  // target + draft rows of one staged tile, at most
+// The tile size the planner aims for: two alternating tiles of 28 KiB let four
+// CTAs share an SM (three with 40 KiB tiles).  Measured on the exactness
+// workload (B = 10^6, K = 4, V = 32 fp32): 268.7 vs 280.9 us (probability),
+// 234.4 vs 259.3 us (greedy), 316.0 vs 333.9 us (logit); smaller tiles cost
+// more per-tile overhead than the extra CTA gains (24 KiB: 298.6 us).
+constexpr int kTmaTileTargetBytes = 28 * 1024;
 constexpr int kTileMaxV = 256;
 constexpr int kTileMinSeqs = 4;
 constexpr int kTileMaxSeqs = 64;
@@ -228,20 +234,19 @@ int ring_from_env() {
   return s[0] == '1' ? 1 : (s[0] == '0' ? 0 : -1);
 }
 
-// Whether the streaming row kernel (grid of `ctas` CTAs) takes the bulk-copy
-// ring: rows on 16-byte boundaries, a grid of at most two waves of 4 CTAs per
-// SM (where CTAs that load in step leave HBM idle while they fold), and the
-// greedy or logit-mixture mode.  Measured on the Qwen-shaped batch (B = 32,
-// K = 5, V = 152064 bf16, one wave): greedy 32.7 vs 34.9 us, logit 59.7 vs
-// 61.3 us, but probability mode 46.9 vs 45.0 us (the ring folds two groups per
-// thread per chunk instead of four, and that mode's folds are the heaviest
-// part of its step).  Grids of many waves desynchronise by themselves and
-// stream at the copy peak with register loads.
+// Whether the streaming row kernel takes the bulk-copy ring instead of
+// register loads: only when SPECV_ROWS_RING=1 asks for it (rows on 16-byte
+// boundaries).  Measured on the Qwen-shaped batch (B = 32, K = 5, V = 152064
+// bf16, one wave of 576 CTAs), ring vs register loads: greedy 32.8 vs
+// 28.8 us, probability 46.9 vs 45.0 us, logit 60.3 vs 61.4 us; at the
+// batched workload (18 waves) both stream at the copy peak.  The ring's refill
+// of a stage waits for the slowest of the CTA's eight warps, and the folds
+// take two groups per thread per chunk instead of four.
 bool ring_choice(bool aligned, int64_t ctas, int sms, int mode) {
-  if (!aligned) return false;
-  const int env = ring_from_env();
-  if (env >= 0) return env == 1;
-  return mode != SPECV_PROB_MIX && ctas <= 2 * 4LL * sms;
+  (void)ctas;
+  (void)sms;
+  (void)mode;
+  return aligned && ring_from_env() == 1;
 }
 
 // "stream", "resident" or "spec" forces a row-kernel variant (tuning and tests).
@@ -280,11 +285,11 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     const bool tma = tma0;
     int ts;
     if (tma) {
-      // two alternating tile buffers of <= 40 KiB each; one round of stage-A
+      // two alternating tile buffers of about 28 KiB (40 KiB at most); one round of stage-A
       // row tasks (2K+1 per sequence) for the CTA's threads; at most one
       // stage-B lane group per sequence
       const int env_stage = tile_stage_from_env();
-      ts = (int)((env_stage ? env_stage : kTmaTileStageBytes) / data_bytes);
+      ts = (int)((env_stage ? env_stage : kTmaTileTargetBytes) / data_bytes);
       const int by_rows = specv::kTileThreads / (2 * K + 1);
       if (ts > by_rows && by_rows >= 1) ts = by_rows;
       if (ts > specv::kTmaTileMaxSeqs) ts = specv::kTmaTileMaxSeqs;

@@ -87,6 +87,35 @@ struct __align__(16) RowsShared {
   float segi[kMaxSegs];   // running sums of segm in index order (inclusive)
 };
 
+// Greedy: folds one 16-byte group (elements idx0, idx0 + 1, ...) into this
+// thread's candidate (best, bidx).  A thread visits its groups in increasing
+// index order, so the first maximum in index order is kept by taking a group
+// only when its maximum is strictly larger (or when it is the thread's first
+// group), and then its first entry equal to that maximum; the per-element
+// work is the score and one maximum.  Entries past V are -inf.
+template <typename T>
+__device__ __forceinline__ void greedy_fold_group(const uint4 &za, const uint4 &zb, bool pair,
+                                                  float lam, int idx0, float &best, int &bidx) {
+  constexpr int VW = Elem<T>::kPerVec;
+  float w[VW];
+#pragma unroll
+  for (int e = 0; e < VW; ++e) {
+    const float zt = Elem<T>::get(za, e);
+    w[e] = pair ? greedy_score(zt, Elem<T>::get(zb, e), lam) : zt;
+  }
+  float gm = w[0];
+#pragma unroll
+  for (int e = 1; e < VW; ++e) gm = fmaxf(gm, w[e]);
+  if (gm > best || (bidx == INT_MAX && gm == gm)) {
+    int first = VW - 1;
+#pragma unroll
+    for (int e = VW - 1; e >= 0; --e)
+      if (w[e] == gm) first = e;
+    best = gm;
+    bidx = idx0 + first;
+  }
+}
+
 // Phase 1 of the bonus row: (max, sum-exp) of every segment of this CTA's
 // slice, written to out[s] for s < nseg (an empty segment gives (-inf, 0)),
 // and merged into lane 0's running statistics (the other lanes keep theirs
@@ -525,17 +554,9 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
 #pragma unroll
                                  for (int u = 0; u < kRingU; ++u) {
                                    const int g = (int)threadIdx.x + u * kNT;
-                                   if (g < cnt) {
-                                     const uint4 za = cA[g];
-                                     const uint4 zb = pair ? cB[g] : za;
-#pragma unroll
-                                     for (int e = 0; e < VW; ++e) {
-                                       const float zt = Elem<T>::get(za, e);
-                                       const float w =
-                                           pair ? greedy_score(zt, Elem<T>::get(zb, e), lam) : zt;
-                                       argmax_merge(best, bidx, w, (c_lo + g) * VW + e);
-                                     }
-                                   }
+                                   if (g < cnt)
+                                     greedy_fold_group<T>(cA[g], pair ? cB[g] : cA[g], pair, lam,
+                                                          (c_lo + g) * VW, best, bidx);
                                  }
                                });
   }
@@ -552,17 +573,7 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int g = g0 + u * kNT;
-      if (g < g_hi) {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) {
-          const int idx = g * VW + e;
-          if (ALIGNED || idx < V) {
-            const float zt = Elem<T>::get(za[u], e);
-            const float w = pair ? greedy_score(zt, Elem<T>::get(zb[u], e), lam) : zt;
-            argmax_merge(best, bidx, w, idx);
-          }
-        }
-      }
+      if (g < g_hi) greedy_fold_group<T>(za[u], pair ? zb[u] : za[u], pair, lam, g * VW, best, bidx);
     }
   }
   warp_argmax(best, bidx);

@@ -143,23 +143,18 @@ def test_plan_cluster_size_model(lib):
 
 
 def test_plan_ring_choice(lib, monkeypatch):
-    """The streaming row kernel takes the bulk-copy ring for 16-byte aligned
-    rows on grids of at most two waves (4 CTAs per SM) in greedy and logit
-    mode, register loads in probability mode, for many waves or unaligned
-    rows; SPECV_ROWS_RING=0/1 forces either (the ring still needs aligned
-    rows)."""
+    """The streaming row kernel takes the bulk-copy ring only when
+    SPECV_ROWS_RING=1 asks for it, and only for 16-byte aligned rows."""
     monkeypatch.delenv("SPECV_ROWS_RING", raising=False)
-    assert specv.plan(32, 5, 152064, specv.BF16)["kernel"] == "rows-stream"
-    assert specv.plan(32, 5, 152064, specv.BF16, specv.LOGIT_MIX)["kernel"] == "rows-ring"
-    assert specv.plan(32, 5, 152064, specv.BF16, specv.GREEDY)["kernel"] == "rows-ring"
-    assert specv.plan(256, 8, 128256, specv.F32)["kernel"] == "rows-stream"  # 18 waves
-    assert specv.plan(2, 4, 131071, specv.F32)["kernel"] == "rows-stream"  # unaligned rows
-    monkeypatch.setenv("SPECV_ROWS_RING", "0")
-    assert specv.plan(32, 5, 152064, specv.BF16)["kernel"] == "rows-stream"
+    for mode in (specv.PROB_MIX, specv.LOGIT_MIX, specv.GREEDY):
+        assert specv.plan(32, 5, 152064, specv.BF16, mode)["kernel"] == "rows-stream"
     monkeypatch.setenv("SPECV_ROWS_RING", "1")
+    assert specv.plan(32, 5, 152064, specv.BF16)["kernel"] == "rows-ring"
     assert specv.plan(256, 8, 128256, specv.F32)["kernel"] == "rows-ring"
     assert specv.plan(256, 8, 128256, specv.F32, specv.GREEDY)["kernel"] == "rows-ring"
-    assert specv.plan(2, 4, 131071, specv.F32)["kernel"] == "rows-stream"
+    assert specv.plan(2, 4, 131071, specv.F32)["kernel"] == "rows-stream"  # unaligned rows
+    monkeypatch.setenv("SPECV_ROWS_RING", "0")
+    assert specv.plan(32, 5, 152064, specv.BF16, specv.GREEDY)["kernel"] == "rows-stream"
 
 
 def _host_call(B=2, K=3, V=100, dtype=0, mode=0, chunks=0, null=None):
