@@ -78,12 +78,14 @@ __global__ void __launch_bounds__(kNT, 4) alpha_kernel(AlphaArgs a) {
     sh.part[3] = sB;
   }
   cluster.sync();  // every rank's partials are visible
-  float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
-  for (int r = 0; r < S; ++r) {  // every thread merges the same partials in rank order
-    const float *pr = cluster.map_shared_rank(sh.part, r);
-    merge_stats(m0, s0, pr[0], pr[1]);
-    merge_stats(m1, s1, pr[2], pr[3]);
-  }
+  float m0, s0, m1, s1;
+  merge_stats2_n(  // every thread merges the same partials in rank order
+      S,
+      [&](int r) {
+        const float *pr = cluster.map_shared_rank(sh.part, r);
+        return make_float4(pr[0], pr[1], pr[2], pr[3]);
+      },
+      m0, s0, m1, s1);
   const SampleParams sp = make_sample_params(m0, s0, m1, s1, lam);
 
   // ------------------------------------------------ pass 2: sum of min(p~, q)

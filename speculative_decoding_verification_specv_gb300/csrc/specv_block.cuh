@@ -50,12 +50,11 @@ __device__ __forceinline__ void block_merge_stats(BlockScratch<NT> &bs, float &m
     bs.red[warp][3] = sB;
   }
   __syncthreads();
-  float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
-#pragma unroll
-  for (int w = 0; w < BlockScratch<NT>::kNW; ++w) {
-    merge_stats(m0, s0, bs.red[w][0], bs.red[w][1]);
-    merge_stats(m1, s1, bs.red[w][2], bs.red[w][3]);
-  }
+  float m0, s0, m1, s1;
+  merge_stats2_n(
+      BlockScratch<NT>::kNW,
+      [&](int w) { return make_float4(bs.red[w][0], bs.red[w][1], bs.red[w][2], bs.red[w][3]); },
+      m0, s0, m1, s1);
   __syncthreads();
   mA = m0;
   sA = s0;

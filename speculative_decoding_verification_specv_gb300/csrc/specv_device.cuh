@@ -112,6 +112,32 @@ __device__ __forceinline__ void merge_stats(float &m, float &s, float m2, float 
   s = __fadd_rn(a, b);
 }
 
+// Merge of n partial statistics of two rows at once; get(r) returns
+// (mA, sA, mB, sB) of partial r.  The maxima come first, then every partial is
+// scaled to them and summed in index order, so the n exponentials are
+// independent of one another (a pairwise merge would chain n rescales).
+// Empty partials are (-inf, 0) and add nothing.
+template <typename Get>
+__device__ __forceinline__ void merge_stats2_n(int n, Get get, float &mA, float &sA, float &mB,
+                                               float &sB) {
+  float MA = -INFINITY, MB = -INFINITY;
+  for (int r = 0; r < n; ++r) {
+    const float4 q = get(r);
+    MA = fmaxf(MA, q.x);
+    MB = fmaxf(MB, q.z);
+  }
+  float SA = 0.0f, SB = 0.0f;
+  for (int r = 0; r < n; ++r) {
+    const float4 q = get(r);
+    SA = __fadd_rn(SA, q.x == MA ? q.y : __fmul_rn(q.y, exp_shifted(q.x, MA)));
+    SB = __fadd_rn(SB, q.z == MB ? q.w : __fmul_rn(q.w, exp_shifted(q.z, MB)));
+  }
+  mA = MA;
+  sA = SA;
+  mB = MB;
+  sB = SB;
+}
+
 // Butterfly merge across a warp; every lane ends with the same result and the
 // combination order is fixed.
 __device__ __forceinline__ void warp_merge_stats(float &m, float &s) {

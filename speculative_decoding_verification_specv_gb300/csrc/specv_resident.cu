@@ -222,14 +222,10 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
     }
   }
   cluster.sync();  // every CTA holds every partial
-  float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
+  float m0, s0, m1, s1;
+  merge_stats2_n(S, [&](int r) { return sh.part[r]; }, m0, s0, m1, s1);
   int cerr = 0;
-  for (int r = 0; r < S; ++r) {
-    const float4 q = sh.part[r];
-    merge_stats(m0, s0, q.x, q.y);
-    merge_stats(m1, s1, q.z, q.w);
-    cerr |= sh.perr[r];
-  }
+  for (int r = 0; r < S; ++r) cerr |= sh.perr[r];
 
   // --------------------------------------------------------- local decision
   if (threadIdx.x == 0) {

@@ -149,12 +149,14 @@ __global__ void __launch_bounds__(kNT, 4) tree_kernel(TreeArgs a) {
   }
   cluster.sync();  // partials of every rank are visible
   if (rank == 0 && threadIdx.x == 0) {
-    float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
-    for (int r = 0; r < S; ++r) {
-      const float *pr = cluster.map_shared_rank(sh.part, r);
-      merge_stats(m0, s0, pr[0], pr[1]);
-      merge_stats(m1, s1, pr[2], pr[3]);
-    }
+    float m0, s0, m1, s1;
+    merge_stats2_n(
+        S,
+        [&](int r) {
+          const float *pr = cluster.map_shared_rank(sh.part, r);
+          return make_float4(pr[0], pr[1], pr[2], pr[3]);
+        },
+        m0, s0, m1, s1);
     a.ws_stats[p] = make_float4(m0, s0, m1, s1);
     __threadfence();
     const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
