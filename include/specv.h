@@ -186,7 +186,11 @@ specv_status specv_verify_debug(const void *target_logits, const void *draft_log
  *            forces the cluster size of the row kernels),
  *            5 = sweep row kernel: persistent CTAs stream fixed-size chunks of
  *            the rows through shared memory by bulk copies (only when
- *            SPECV_ROWS_VARIANT=sweep asks for it; rows on 16-byte boundaries)
+ *            SPECV_ROWS_VARIANT=sweep asks for it; rows on 16-byte boundaries),
+ *            6 = streaming cluster row kernel fed by a three-stage ring of
+ *            shared-memory chunks filled by bulk copies instead of register
+ *            loads (only when SPECV_ROWS_RING=1 asks for it; rows on 16-byte
+ *            boundaries)
  *   cluster: CTAs per thread-block cluster splitting each row (1 for kernel 0)
  *   ctas:    CTAs launched by a row kernel; tiles of sequences for kernels 0, 3
  *   workspace_bytes: scratch bytes of the row kernels' workspace (kept per

@@ -138,15 +138,19 @@ __device__ __forceinline__ void merge_stats2_n(int n, Get get, float &mA, float 
   sB = SB;
 }
 
-// Butterfly merge across a warp; every lane ends with the same result and the
-// combination order is fixed.
+// Merge across a warp: the warp's maximum by a butterfly, then every lane's
+// sum scaled to it and added by a butterfly (one exponential per lane instead
+// of one per level).  Addition is commutative, so every lane ends with the
+// same result, and the combination order is fixed.
 __device__ __forceinline__ void warp_merge_stats(float &m, float &s) {
+  float M = m;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-    float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-    merge_stats(m, s, m2, s2);
-  }
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float t = m == M ? s : __fmul_rn(s, exp_shifted(m, M));  // an empty lane (-inf, 0) adds 0
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, off));
+  m = M;
+  s = t;
 }
 
 // Greedy: of two (value, index) candidates keep the larger value, and the
