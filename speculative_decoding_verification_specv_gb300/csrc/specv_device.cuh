@@ -230,8 +230,19 @@ enum : int { kWResidual = 0, kWBonus = 1, kWMixture = 2, kWResidualC = 3 };
 
 struct SampleParams {
   float mA, invSA, mB, invSB, lam;
-  float c;  // threshold of kWResidualC
+  float c;       // threshold of kWResidualC
+  float nA, nB;  // -(m log2e + log2 S): a probability is 2^(z log2e + n) = exp(z - m) / S
 };
+
+// The exponent offsets nA, nB from the statistics: one fused multiply-add and
+// the SFU's 2^x per probability in the sampler.  log2 S comes from the SFU
+// (absolute error near 2^-22: a common factor within 2e-7 of 1 on a row's
+// probabilities).  Equal statistics give equal offsets (a residual of
+// identical rows stays exactly zero).
+__device__ __forceinline__ void set_exponent_offsets(SampleParams &p, float sA, float sB) {
+  p.nA = -__fmaf_rn(p.mA, kLog2e, lg2(sA));
+  p.nB = -__fmaf_rn(p.mB, kLog2e, lg2(sB));
+}
 
 // Sampler parameters of a position from its statistics.  The reciprocals are
 // SFU approximations: a common factor on a weight vector does not move its
@@ -245,15 +256,35 @@ __device__ __forceinline__ SampleParams make_sample_params(float mA, float sA, f
   p.invSB = __fdividef(1.0f, sB);
   p.lam = lam;
   p.c = 1.0f;
+  set_exponent_offsets(p, sA, sB);
   return p;
+}
+
+// The same with correctly rounded reciprocals.
+__device__ __forceinline__ SampleParams make_sample_params_rn(float mA, float sA, float mB,
+                                                              float sB, float lam) {
+  SampleParams p;
+  p.mA = mA;
+  p.invSA = __fdiv_rn(1.0f, sA);
+  p.mB = mB;
+  p.invSB = __fdiv_rn(1.0f, sB);
+  p.lam = lam;
+  p.c = 1.0f;
+  set_exponent_offsets(p, sA, sB);
+  return p;
+}
+
+// A probability exp(z - m) / S from the exponent offset n of its row.
+__device__ __forceinline__ float prob_from_offset(float z, float n) {
+  return ex2(__fmaf_rn(z, kLog2e, n));
 }
 
 __device__ __forceinline__ float sample_weight(int mode, int kind, const SampleParams &p, float zt,
                                                float zq) {
-  if (kind == kWBonus) return __fmul_rn(exp_shifted(zt, p.mA), p.invSA);
+  if (kind == kWBonus) return prob_from_offset(zt, p.nA);
   float a = (mode == kProbMix) ? zt : mix_logit(zt, zq, p.lam);
-  float pa = __fmul_rn(exp_shifted(a, p.mA), p.invSA);
-  float pq = __fmul_rn(exp_shifted(zq, p.mB), p.invSB);
+  float pa = prob_from_offset(a, p.nA);
+  float pq = prob_from_offset(zq, p.nB);
   if (kind == kWResidual) return fmaxf(0.0f, __fsub_rn(pa, pq));
   const float pt = (mode == kProbMix) ? __fmaf_rn(p.lam, pq, __fmul_rn(__fsub_rn(1.0f, p.lam), pa))
                                       : pa;
@@ -268,9 +299,9 @@ __device__ __forceinline__ float sample_weight(int mode, int kind, const SampleP
 __device__ __forceinline__ float sample_weight_sel(int mode, int kind, const SampleParams &p,
                                                    float zt, float zq) {
   const float a = (mode == kProbMix) ? zt : mix_logit(zt, zq, p.lam);
-  const float pa = __fmul_rn(exp_shifted(a, p.mA), p.invSA);
-  const float pq = __fmul_rn(exp_shifted(zq, p.mB), p.invSB);
-  const float bonus = (mode == kProbMix) ? pa : __fmul_rn(exp_shifted(zt, p.mA), p.invSA);
+  const float pa = prob_from_offset(a, p.nA);
+  const float pq = prob_from_offset(zq, p.nB);
+  const float bonus = (mode == kProbMix) ? pa : prob_from_offset(zt, p.nA);
   const float resid = fmaxf(0.0f, __fsub_rn(pa, pq));
   const float mixed =
       (mode == kProbMix) ? __fmaf_rn(p.lam, pq, __fmul_rn(__fsub_rn(1.0f, p.lam), pa)) : pa;

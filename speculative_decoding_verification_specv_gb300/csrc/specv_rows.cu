@@ -178,7 +178,7 @@ __device__ int bonus_from_stats(RowsShared &sh, const RowArgs &a, const T *row, 
     if (j >= total) return 0.0f;
     const float2 v = __ldcg(&st[j]);
     return v.x == -INFINITY ? 0.0f
-                            : __fmul_rn(__fmul_rn(v.y, exp_shifted(v.x, sp.mA)), sp.invSA);
+                            : __fmul_rn(v.y, prob_from_offset(v.x, sp.nA));
   };
   float W = 0.0f;
   for (int j0 = 0; j0 < total; j0 += kNT) {
@@ -433,12 +433,7 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
       bc.n = valid ? n : -1;
       bc.u = a.u_resample[b];
       const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + (valid ? n : 0)]);
-      bc.sp.mA = st4.x;
-      bc.sp.invSA = __fdiv_rn(1.0f, st4.y);
-      bc.sp.mB = st4.z;
-      bc.sp.invSB = __fdiv_rn(1.0f, st4.w);
-      bc.sp.lam = lam_seq;
-      bc.sp.c = 1.0f;
+      bc.sp = make_sample_params_rn(st4.x, st4.y, st4.z, st4.w, lam_seq);
       if (n == K)
         bc.kind = kWBonus;
       else if (MODE == kProbMix && !(lam_seq < 1.0f))
@@ -487,13 +482,7 @@ __global__ void __launch_bounds__(kNT, 4) rows_sample_kernel(RowArgs a) {
   if (n < 0) return;  // invalid sequence (or a timed-out copy): nothing to draw
   const float lam = a.lam[b];
   const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + n]);
-  SampleParams sp;
-  sp.mA = st4.x;
-  sp.invSA = __fdiv_rn(1.0f, st4.y);
-  sp.mB = st4.z;
-  sp.invSB = __fdiv_rn(1.0f, st4.w);
-  sp.lam = lam;
-  sp.c = 1.0f;
+  const SampleParams sp = make_sample_params_rn(st4.x, st4.y, st4.z, st4.w, lam);
   const int kind = n == K ? kWBonus
                           : ((MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual);
   const float u = a.u_resample[b];

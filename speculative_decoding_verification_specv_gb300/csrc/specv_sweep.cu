@@ -154,7 +154,7 @@ __device__ int bonus_token(SweepShared &sh, const SweepArgs &a, int64_t p, const
     if (c >= C) return 0.0f;
     const float4 v = __ldcg(&st[c]);
     return v.x == -INFINITY ? 0.0f
-                            : __fmul_rn(__fmul_rn(v.y, exp_shifted(v.x, sp.mA)), sp.invSA);
+                            : __fmul_rn(v.y, prob_from_offset(v.x, sp.nA));
   };
   float W = 0.0f;
   for (int c0 = 0; c0 < C; c0 += kNT) {
@@ -287,12 +287,7 @@ __device__ void finish_sequence(SweepShared &sh, const SweepArgs &a, int64_t b) 
       bc.n = valid ? n : -1;
       bc.u = a.u_resample[b];
       const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + (valid ? n : 0)]);
-      bc.sp.mA = st4.x;
-      bc.sp.invSA = __fdiv_rn(1.0f, st4.y);
-      bc.sp.mB = st4.z;
-      bc.sp.invSB = __fdiv_rn(1.0f, st4.w);
-      bc.sp.lam = lam;
-      bc.sp.c = 1.0f;
+      bc.sp = make_sample_params_rn(st4.x, st4.y, st4.z, st4.w, lam);
       if (n == K)
         bc.kind = kWBonus;
       else if (MODE == kProbMix && !(lam < 1.0f))

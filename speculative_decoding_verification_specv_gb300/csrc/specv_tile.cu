@@ -205,13 +205,7 @@ __global__ void __launch_bounds__(kNT) tile_kernel(TileArgs a) {
       if (!valid) continue;
 
       const float4 st4 = st_s[s * (K + 1) + n];
-      SampleParams sp;
-      sp.mA = st4.x;
-      sp.invSA = __fdiv_rn(1.0f, st4.y);
-      sp.mB = st4.z;
-      sp.invSB = __fdiv_rn(1.0f, st4.w);
-      sp.lam = lam;
-      sp.c = 1.0f;
+      const SampleParams sp = make_sample_params_rn(st4.x, st4.y, st4.z, st4.w, lam);
       int kind = (n == K) ? kWBonus
                           : ((MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual);
       const T *ra = st_t + ((int64_t)s * (K + 1) + n) * V;
