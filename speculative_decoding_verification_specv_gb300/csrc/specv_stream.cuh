@@ -69,14 +69,21 @@ __device__ __forceinline__ void fold_batch(const uint4 (&za)[U], const uint4 (&z
     }
     return zt;
   };
+  // logit mode with fp32 rows: the mixed logits are formed once and kept for
+  // both passes (bf16 batches hold twice the elements: there they are formed
+  // again in the second pass, which needs fewer registers)
+  constexpr bool kKeep = MODE == kLogitMix && sizeof(T) == 4;
+  float w[kKeep ? U : 1][kKeep ? VW : 1];
   float bmA;
   if (MODE == kLogitMix && pair) {
     bmA = -INFINITY;
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (ok[u]) {
 #pragma unroll
-        for (int e = 0; e < VW; ++e) bmA = fmaxf(bmA, a_val(u, e));
+      for (int e = 0; e < VW; ++e) {
+        const float v = ok[u] ? a_val(u, e) : -INFINITY;
+        if constexpr (kKeep) w[u][e] = v;
+        bmA = fmaxf(bmA, v);
       }
   } else {
     bmA = batch_max<T, U>(za, ok);
@@ -96,7 +103,12 @@ __device__ __forceinline__ void fold_batch(const uint4 (&za)[U], const uint4 (&z
     if (ok[u]) {
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
-        sA = __fadd_rn(sA, ex2(__fmaf_rn(a_val(u, e), kLog2e, nA)));
+        float av;
+        if constexpr (kKeep)
+          av = pair ? w[u][e] : a_val(u, e);
+        else
+          av = a_val(u, e);
+        sA = __fadd_rn(sA, ex2(__fmaf_rn(av, kLog2e, nA)));
         if (pair) sB = __fadd_rn(sB, ex2(__fmaf_rn(Elem<T>::get(zb[u], e), kLog2e, nB)));
       }
     }
