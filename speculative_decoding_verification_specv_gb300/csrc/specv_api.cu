@@ -8,6 +8,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "specv.h"
 #include "specv_internal.h"
 
@@ -788,6 +790,15 @@ specv_status verify_host(const void *target, const void *draft, const int32_t *t
   return SPECV_OK;
 }
 
+// An NVTX range named after the entry point around its host work and launches:
+// visible on the timeline of NVIDIA's profilers, a no-op when none is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 }  // namespace
 
 extern "C" {
@@ -797,6 +808,7 @@ specv_status specv_verify(const void *target_logits, const void *draft_logits,
                           const float *u_resample, const float *lambda, int64_t B, int32_t K,
                           int32_t V, specv_dtype dtype, specv_mode mode, int32_t *out_tokens,
                           int32_t *out_n_accepted, void *stream) {
+  NvtxRange range("specv_verify");
   return run(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lambda, B, K, V,
              dtype, mode, out_tokens, out_n_accepted, nullptr, nullptr, nullptr, stream);
 }
@@ -806,6 +818,7 @@ specv_status specv_verify_host(const void *target_logits, const void *draft_logi
                                const float *u_resample, const float *lambda, int64_t B, int32_t K,
                                int32_t V, specv_dtype dtype, specv_mode mode, int32_t *out_tokens,
                                int32_t *out_n_accepted, int32_t chunks, void *stream) {
+  NvtxRange range("specv_verify_host");
   return verify_host(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lambda, B,
                      K, V, dtype, mode, out_tokens, out_n_accepted, chunks, stream);
 }
@@ -818,6 +831,7 @@ specv_status specv_verify_debug(const void *target_logits, const void *draft_log
                                 float *out_ptilde_at_x, float *out_q_at_x, float *out_lse,
                                 void *stream) {
   if (mode == SPECV_GREEDY) return SPECV_ERR_UNSUPPORTED;  // no probabilities to report
+  NvtxRange range("specv_verify_debug");
   return run(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lambda, B, K, V,
              dtype, mode, out_tokens, out_n_accepted, out_ptilde_at_x, out_q_at_x, out_lse,
              stream);
@@ -856,6 +870,7 @@ specv_status specv_verify_tree(const void *target_logits, const void *draft_logi
                                int32_t M, int32_t V, specv_dtype dtype, specv_mode mode,
                                int32_t *out_tokens, int32_t *out_path, int32_t *out_n,
                                void *stream) {
+  NvtxRange range("specv_verify_tree");
   if (!target_logits || !parent || !draft_row || !tokens || !u_accept || !u_resample || !lambda ||
       !out_tokens || !out_path || !out_n || (M > 0 && !draft_logits))
     return SPECV_ERR_INVALID_ARG;
@@ -941,6 +956,7 @@ specv_status specv_acceptance_rates(const void *target_logits, const void *draft
                                     const float *lambda, int64_t B, int32_t K, int32_t V,
                                     specv_dtype dtype, specv_mode mode, float *out_alpha,
                                     void *stream) {
+  NvtxRange range("specv_acceptance_rates");
   if (!target_logits || !draft_logits || !lambda || !out_alpha) return SPECV_ERR_INVALID_ARG;
   if (!sizes_ok(B, K, V, dtype, mode)) return SPECV_ERR_INVALID_ARG;
   if (mode == SPECV_GREEDY) return SPECV_ERR_UNSUPPORTED;  // greedy has no p~ to overlap with q
