@@ -1,12 +1,14 @@
 // specv_ring.cuh -- a ring of shared-memory stages filled by 1-D bulk copies
 // (TMA), through which a CTA streams its slice of one row or of a row pair.
 //
-// Why: a CTA that loads its slice into registers issues a batch of loads,
-// waits for all of them, folds them, and only then issues the next batch.
-// When the grid is a single wave every CTA does this in step, so HBM idles
-// while the SMs fold and the SMs idle while HBM delivers.  Here the copies of
-// the next kRingStages - 1 chunks are always in flight while the threads fold
-// the current one, so HBM sees a steady queue of requests.
+// The idea: a CTA that loads its slice into registers issues a batch of
+// loads, waits for all of them, folds them, and only then issues the next
+// batch; here the copies of the next kRingStages - 1 chunks are always in
+// flight while the threads fold the current one.  Measured on GB300 it does
+// not beat register loads (a stage is refilled only after the slowest of the
+// CTA's warps is done with it, and the folds take two groups per thread per
+// chunk instead of four), so the planner uses it only when asked
+// (SPECV_ROWS_RING=1).
 //
 // Protocol (no producer warp, no CTA barrier per chunk):
 //   - chunk j (kRingChunkGroups 16-byte groups of each row, the last one

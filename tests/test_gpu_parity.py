@@ -194,6 +194,20 @@ def test_token_draws_in_one_or_two_launches(specv, cluster_env, shape, split, mo
     print(f"{shape} split={split} mode={mode}: {rep}")
 
 
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+@pytest.mark.parametrize("V,dt", [(64, "f32"), (1000, "bf16")])
+def test_maximum_draft_length(specv, V, dt, mode):
+    """K = 4096, the largest draft the boundary accepts: 4097 positions per
+    sequence.  The second sequence drafts the target itself, so all 4096 drafts
+    pass and the bonus row is drawn; the first rejects early."""
+    w = workloads.Workload("kmax", 2, 4096, V, dt, "half_equal:2.0:0.9:0.5", (0.3,), 31)
+    x = workloads.make_inputs(w, DEV)
+    rep, tok, n = _check(specv, x, mode, debug=False)
+    print(f"K=4096 V={V} {dt} mode={mode}: {rep}, n={n.tolist()}")
+    assert n[1] == 4096 and (tok[1, :4096] == x["draft_tokens"][1].cpu().numpy()).all()
+    assert 0 <= tok[1, 4096] < V
+
+
 RAGGED = [
     # (B, K, V, dtype, structure)
     (3, 1, 1001, "f32", "corr:2.0:0.8:1.0"),       # rows kernel, unaligned rows
