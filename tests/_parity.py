@@ -117,3 +117,37 @@ def check_probabilities(xh, mode, dbg, orc, seqs=None):
     assert err_p <= tol and err_q <= tol, (err_p, err_q, tol)
     return dict(max_abs_err_ptilde=float(err_p), max_abs_err_q=float(err_q),
                 max_rel_err_ptilde=float(rel_p))
+
+
+def check_rows(xh, mode, dbg, seqs, tol=None):
+    """Whole rows: the distributions implied by the GPU's log-normalisers
+    (p_t,v = exp(z_t,v - lse_A), q_v = exp(z_q,v - lse_B); in logit mode the
+    A row is the mixed row, formed in fp32 as the kernels form it) against the
+    oracle's fp64 p~ and q rows, entry by entry, for the listed sequences."""
+    if tol is None:
+        tol = TOL_BF16 if xh["target_logits"].dtype == torch.bfloat16 else TOL_F32
+    lse = dbg["lse"].cpu().numpy().astype(np.float64)
+    worst_p = worst_q = 0.0
+    for b in seqs:
+        zt32 = xh["target_logits"][b].float().numpy()
+        zq32 = xh["draft_logits"][b].float().numpy()
+        lam = float(xh["lam"][b])
+        pt_o, q_o = oracle.rows(xh["target_logits"][b], xh["draft_logits"][b], lam, mode)
+        K = zq32.shape[0]
+        for j in range(K + 1):
+            if j < K:
+                qg = np.exp(zq32[j].astype(np.float64) - lse[b, j, 1])
+                if mode == oracle.PROB_MIX:
+                    ptg = np.exp(zt32[j].astype(np.float64) - lse[b, j, 0])
+                    pg = (1.0 - lam) * ptg + lam * qg
+                else:
+                    lam32 = np.float32(lam)
+                    w = (zt32[j] + lam32 * (zq32[j] - zt32[j])).astype(np.float32)
+                    w = np.where(zq32[j] == -np.inf, -np.inf, w)
+                    pg = np.exp(w.astype(np.float64) - lse[b, j, 0])
+                worst_q = max(worst_q, float(np.abs(qg - q_o[j]).max()))
+            else:  # the bonus row: the target softmax
+                pg = np.exp(zt32[j].astype(np.float64) - lse[b, j, 0])
+            worst_p = max(worst_p, float(np.abs(pg - pt_o[j]).max()))
+    assert worst_p <= tol and worst_q <= tol, (worst_p, worst_q, tol)
+    return dict(max_abs_err_ptilde_rows=worst_p, max_abs_err_q_rows=worst_q)

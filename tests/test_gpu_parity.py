@@ -94,6 +94,23 @@ def test_parity_workloads(specv, cfg, mode):
 
 
 @pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_whole_row_probabilities(specv, cfg, mode):
+    """Every entry of p~ and q (not only at the drafted tokens), as implied by
+    the kernels' row log-normalisers, against the oracle's fp64 rows within
+    1e-5 (fp32 logits) / 2e-3 (bf16 logits); two sequences per workload."""
+    w = SMALL[cfg]
+    x = workloads.make_inputs(w, DEV)
+    args = (x["target_logits"], x["draft_logits"], x["draft_tokens"], x["u_accept"],
+            x["u_resample"], x["lam"])
+    dbg = specv.verify_debug(*args, mode=mode)
+    torch.cuda.synchronize()
+    xh = _parity.to_host(x)
+    rep = _parity.check_rows(xh, mode, dbg, seqs=[0, w.B - 1])
+    print(f"workload {cfg} mode={mode}: {rep}")
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
 def test_parity_full_size_batched_fp32_sampled(specv, mode):
     """B=256, K=8, V=128256 fp32 as benchmarked; the oracle checks 32 sampled
     sequences, and every drafted-equals-target sequence must accept all K."""
