@@ -44,8 +44,8 @@ struct __align__(16) AlphaShared {
 template <int MODE>
 __device__ __forceinline__ float overlap_term(float zt, float zq, float lam, const SampleParams &sp) {
   const float a = MODE == kLogitMix ? (zq == -INFINITY ? -INFINITY : mix_logit(zt, zq, lam)) : zt;
-  const float pa = __fmul_rn(exp_shifted(a, sp.mA), sp.invSA);
-  const float pq = __fmul_rn(exp_shifted(zq, sp.mB), sp.invSB);
+  const float pa = prob_from_offset(a, sp.nA);
+  const float pq = prob_from_offset(zq, sp.nB);
   const float pt = MODE == kProbMix ? __fmaf_rn(lam, pq, __fmul_rn(__fsub_rn(1.0f, lam), pa)) : pa;
   return fminf(pt, pq);
 }
