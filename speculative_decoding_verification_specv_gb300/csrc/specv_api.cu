@@ -244,12 +244,7 @@ int ring_from_env() {
 // batched workload (18 waves) both stream at the copy peak.  The ring's refill
 // of a stage waits for the slowest of the CTA's eight warps, and the folds
 // take two groups per thread per chunk instead of four.
-bool ring_choice(bool aligned, int64_t ctas, int sms, int mode) {
-  (void)ctas;
-  (void)sms;
-  (void)mode;
-  return aligned && ring_from_env() == 1;
-}
+bool ring_choice(bool aligned) { return aligned && ring_from_env() == 1; }
 
 // "stream", "resident" or "spec" forces a row-kernel variant (tuning and tests).
 int variant_from_env() {
@@ -327,7 +322,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     }
     while (S > 1 && P * S > INT32_MAX) S /= 2;
     if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
-    p->kernel = ring_choice(aligned && row_bytes % 16 == 0, P * S, sms, mode) ? 6 : 1;
+    p->kernel = ring_choice(aligned && row_bytes % 16 == 0) ? 6 : 1;
     p->cluster = S;
     p->ctas = P * S;
     p->num_groups = (int)G;
@@ -400,7 +395,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     while (S > 1 && P * S > INT32_MAX) S /= 2;
     if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
   }
-  if (kernel == 1 && ring_choice(aligned && row_bytes % 16 == 0, P * S, sms, mode)) kernel = 6;
+  if (kernel == 1 && ring_choice(aligned && row_bytes % 16 == 0)) kernel = 6;
   p->kernel = kernel;
   p->cluster = S;
   p->ctas = P * S;
