@@ -70,6 +70,21 @@ def test_noalloc_matches_specv_verify_on_two_calls(lib, cfg, mode):
         assert (n[far] == ref_n[far]).all() and (tok[far] == ref_tok[far]).all()
 
 
+@pytest.mark.parametrize("cfg", [3, 4])
+def test_noalloc_greedy_matches_specv_verify_exactly(lib, cfg):
+    """Greedy verification (an argmax decision, taken in fp32 on both paths):
+    the outputs equal specv_verify's exactly, on two calls in a row."""
+    import speculative_decoding_verification_specv_gb300 as specv
+    w = workloads.WORKLOADS[cfg].scaled(B=12)
+    for call in range(2):
+        x = workloads.make_inputs(w, DEV, seed_offset=10 + call)
+        ref_tok, ref_n = specv.verify(x["target_logits"], x["draft_logits"], x["draft_tokens"],
+                                      x["u_accept"], x["u_resample"], x["lam"], mode=2)
+        tok, n = _noalloc(lib, x, 2)
+        torch.cuda.synchronize()
+        assert torch.equal(tok, ref_tok) and torch.equal(n, ref_n)
+
+
 def test_noalloc_rejects_sizes_beyond_its_array(lib):
     # B*(K+1) above the array's 49152 positions: refused before any launch
     null = None
