@@ -112,6 +112,17 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def needed_bytes(n_accepted, K, V, elem):
+    """Bytes of logits the verify step needs when it stops at the first
+    rejection: the row pairs of positions 0..n and, when every draft passes,
+    the bonus row -- (2 min(n + 1, K) + [n = K]) V s per sequence.  An invalid
+    sequence (n < 0) is counted with every row."""
+    n = torch.as_tensor(n_accepted).to(torch.int64).cpu()
+    rows = torch.where(n < 0, torch.full_like(n, 2 * K + 1),
+                       2 * torch.clamp(n + 1, max=K) + (n == K).to(torch.int64))
+    return int(rows.sum().item()) * V * elem
+
+
 def capture_graph(launch, dev):
     """A CUDA graph of one launch() call, captured on a side stream after one
     plain call on that same stream: the library keeps its scratch per stream
@@ -584,7 +595,11 @@ def main():
 
     plan = specv.plan(w.B, w.K, w.V, 1 if w.dtype == "bf16" else 0, mode)
     kern_ms = statistics.mean(per_call_ms)
-    alg_bytes = w.roofline_bytes
+    # With early exit the step reads only the rows the outputs depend on, so
+    # the algorithmic bytes are those rows (from the outputs of this run);
+    # every row read once, (2K+1)BVs, is reported beside them.
+    all_rows = w.roofline_bytes
+    alg_bytes = needed_bytes(out_n, w.K, w.V, w.elem_bytes) if plan.get("early_exit") else all_rows
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
     traffic = profiled_traffic(w.name, args.mode)
@@ -597,6 +612,12 @@ def main():
                            plan["kernel"] in ("rows-stream", "rows-ring") else
                            PLAN_KERNEL_FUNCTION.get(plan["kernel"], plan["kernel"])),
                 "algorithmic_bytes_per_launch": alg_bytes,
+                "algorithmic_bytes": ("rows up to the first rejection (early exit): "
+                                      "(2 min(n+1, K) + [n = K]) V s per sequence"
+                                      if plan.get("early_exit") else
+                                      "every logit read once: (2K+1) B V s"),
+                "all_rows_bytes_per_launch": all_rows,
+                "frac_at_all_rows_bytes": all_rows / (kern_ms / 1e3) / 1e9 / peak,
                 "launch_ms_mean": kern_ms, "launch_ms_min": min(per_call_ms),
                 "timing": ("CUDA events around each replay of a CUDA graph holding one "
                            "specv_verify call" if graph is not None else

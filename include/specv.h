@@ -202,6 +202,25 @@ specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, spec
                         int64_t *workspace_bytes);
 
 /*
+ * specv_plan_flags -- host-only query of how the launch specv_verify would
+ * make for these sizes behaves (no device work, no allocation).  *flags
+ * (not NULL) receives a bit set:
+ *   SPECV_PLAN_EARLY_EXIT  -- the streaming row kernel runs position-major and
+ *       a position whose sequence already has a published rejection at an
+ *       earlier position reads none of its rows (the pages' loop stops at the
+ *       first rejection: RAPID explainer, "3) 候选验证机制（伪代码）"; SD
+ *       explainer, "修改的拒绝采样").  Taken on grids of more than two waves of
+ *       CTAs; the environment variable SPECV_EARLY_EXIT=0 turns it off.  The
+ *       outputs do not depend on it.
+ *   SPECV_PLAN_SPLIT_DRAWS -- the token draws run as a second launch.
+ * Returns SPECV_ERR_INVALID_ARG for sizes specv_verify would reject.
+ */
+#define SPECV_PLAN_EARLY_EXIT 1u
+#define SPECV_PLAN_SPLIT_DRAWS 2u
+specv_status specv_plan_flags(int64_t B, int32_t K, int32_t V, specv_dtype dtype,
+                              specv_mode mode, uint32_t *flags);
+
+/*
  * specv_verify_tree -- the verify/accept step for a tree of drafted tokens per
  * sequence (the speculative-decoding explainer's "Tree Speculation": several
  * candidate branches per position verified at once, so that another branch can

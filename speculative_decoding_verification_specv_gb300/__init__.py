@@ -84,6 +84,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.specv_plan.argtypes = [i64, i32, i32, ctypes.c_int, ctypes.c_int, i32p, i32p,
                                    ctypes.POINTER(i64), ctypes.POINTER(i64)]
         lib.specv_plan.restype = ctypes.c_int
+        lib.specv_plan_flags.argtypes = [i64, i32, i32, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_uint32)]
+        lib.specv_plan_flags.restype = ctypes.c_int
         lib.specv_status_string.argtypes = [ctypes.c_int]
         lib.specv_status_string.restype = ctypes.c_char_p
         lib.specv_last_cuda_error.argtypes = []
@@ -357,8 +360,12 @@ def plan(B: int, K: int, V: int, dtype: int = F32, mode: int = PROB_MIX) -> dict
     st = load().specv_plan(int(B), int(K), int(V), int(dtype), int(mode), ctypes.byref(kern),
                            ctypes.byref(clus), ctypes.byref(ctas), ctypes.byref(ws))
     _check(st, "specv_plan")
+    flags = ctypes.c_uint32(0)
+    _check(load().specv_plan_flags(int(B), int(K), int(V), int(dtype), int(mode),
+                                   ctypes.byref(flags)), "specv_plan_flags")
     return dict(kernel=KERNEL_NAMES.get(kern.value, str(kern.value)), cluster=clus.value,
-                ctas=ctas.value, workspace_bytes=ws.value)
+                ctas=ctas.value, workspace_bytes=ws.value,
+                early_exit=bool(flags.value & 1), split_draws=bool(flags.value & 2))
 
 
 def raw_call(name: str, *args) -> int:

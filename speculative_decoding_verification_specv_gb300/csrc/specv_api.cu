@@ -188,6 +188,7 @@ struct Plan {
   int split;             // streaming kernel: 1 = token draws in a second launch (rows_sample)
   int sample_cluster;    // its cluster size
   int sample_gps, sample_seg_tiles, sample_segs;  // its slice and segment geometry
+  int early_exit;        // streaming kernel: positions after a published rejection skip their rows
   int chunk_groups, chunks;       // sweep kernel: groups per chunk, chunks per row
   int sweep_smem;        // dynamic shared memory of the sweep kernel
   int64_t counters;      // arrival counters in the scratch
@@ -209,6 +210,17 @@ int cluster_from_env() {
   if (!s || !*s) return 0;
   const int v = std::atoi(s);
   return (v >= 1 && v <= specv::kMaxCluster) ? v : 0;
+}
+
+// Early exit (the pages' loop stops at the first rejection): on grids of more
+// than two waves the streaming kernels run position-major, every position
+// publishes its own rejection, and a position after a published rejection
+// reads none of its rows.  On grids of one or two waves every position streams
+// at the same time, so none would be skipped.  SPECV_EARLY_EXIT=0 reads every
+// row (tests, measurements).
+bool early_exit_from_env() {
+  const char *s = std::getenv("SPECV_EARLY_EXIT");
+  return !(s && s[0] == '0');
 }
 
 // SPECV_SAMPLE_SPLIT=0/1 forces the streaming kernel's token draws into the
@@ -330,6 +342,11 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     specv::rows_segments(p->groups_per_slice, &p->seg_tiles, &p->segs_per_slice);
     p->counters = B;
     p->ws_bytes = round16(P * 16) + round16(B * 4);
+    if (P * S > 2 * 4LL * sms && early_exit_from_env()) {  // early exit: one word per sequence
+      p->early_exit = 1;
+      p->counters = 2 * B;
+      p->ws_bytes += round16(B * 4);
+    }
     return SPECV_OK;
   }
   if (env_var == 5) {
@@ -425,6 +442,14 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
       p->sample_cluster = (int)s2;
       p->sample_gps = (int)((G + s2 - 1) / s2);
       specv::rows_segments(p->sample_gps, &p->sample_seg_tiles, &p->sample_segs);
+    }
+    // Early exit: the grid runs position-major and a position skips its rows
+    // when an earlier position of its sequence has published a rejection; one
+    // more word per sequence in the counter region (zero at entry, left zero).
+    if (!p->split && early_exit_from_env()) {
+      p->early_exit = 1;
+      p->counters = 2 * B;
+      p->ws_bytes += round16(B * 4);
     }
   }
   return SPECV_OK;
@@ -582,6 +607,11 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
                                     : reinterpret_cast<float2 *>(static_cast<char *>(wdata) +
                                                                  round16(B * (K + 1) * 16));
     a.defer_sampling = mode != SPECV_GREEDY && p.split;
+    // early exit, except for the debug entry point (which reports every position)
+    if (p.early_exit && dbg_ptilde == nullptr && dbg_lse == nullptr) {
+      a.ws_reject = cnt + B;
+      a.pos_major = 1;
+    }
     a.stats_cluster = p.cluster;
     a.stats_groups_per_slice = p.groups_per_slice;
     a.stats_seg_tiles = p.seg_tiles;
@@ -855,6 +885,27 @@ specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, spec
   if (cluster) *cluster = p.cluster;
   if (ctas) *ctas = p.ctas;
   if (workspace_bytes) *workspace_bytes = p.ws_bytes;
+  return SPECV_OK;
+}
+
+specv_status specv_plan_flags(int64_t B, int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,
+                              uint32_t *flags) {
+  if (!flags || !sizes_ok(B, K, V, dtype, mode)) return SPECV_ERR_INVALID_ARG;
+  int sms = kDefaultSMs;
+  int64_t l2 = kDefaultL2;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      sms = v;
+    (void)cudaGetLastError();
+  } else {
+    (void)cudaGetLastError();
+  }
+  Plan p;
+  specv_status s = make_plan(B, K, V, dtype, mode, sms, l2, true, &p);
+  if (s != SPECV_OK) return s;
+  *flags = (p.early_exit ? SPECV_PLAN_EARLY_EXIT : 0u) | (p.split ? SPECV_PLAN_SPLIT_DRAWS : 0u);
   return SPECV_OK;
 }
 

@@ -127,6 +127,12 @@ struct RowArgs {
                              // reads the bonus row again)
   int defer_sampling;        // 1: the last cluster stops after the decisions; rows_sample
                              // draws the tokens in a second launch
+  unsigned *ws_reject = nullptr;  // optional scratch [B] (zero at entry, left zero): early exit.
+                                  // K + 1 - j for the earliest position j whose own acceptance
+                                  // test is known to reject; positions after it skip their rows
+  int pos_major = 0;         // 1: the grid runs position-major (all sequences' position 0, then
+                             // position 1, ...), so that later positions of a sequence start
+                             // after its earlier ones have published their decisions
   // rows_sample only: the statistics launch's geometry (for the bonus segments)
   int stats_cluster;
   int stats_groups_per_slice;

@@ -298,10 +298,18 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
   const int S = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
-  const int64_t p = (int64_t)blockIdx.x / S;  // position index b*(K+1) + i
+  const int64_t pl = (int64_t)blockIdx.x / S;  // the cluster's position in launch order
   const int K = a.K, V = a.V;
-  const int64_t b = p / (K + 1);
-  const int i = (int)(p - b * (K + 1));
+  int64_t b;
+  int i;
+  if (a.pos_major) {
+    i = (int)(pl / a.B);
+    b = pl - (int64_t)i * a.B;
+  } else {
+    b = pl / (K + 1);
+    i = (int)(pl - b * (K + 1));
+  }
+  const int64_t p = b * (K + 1) + i;  // position index b*(K+1) + i
   const bool pair = i < K;
   const T *tgt = static_cast<const T *>(a.target);
   const T *dft = static_cast<const T *>(a.draft);
@@ -310,6 +318,15 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   const int g_lo = rank * a.groups_per_slice;
   const int g_hi = min(a.num_groups, g_lo + a.groups_per_slice);
   const float lam_seq = a.lam[b];
+  // Early exit (the pages' loop stops at the first rejection): a position
+  // after one whose rejection is already published reads none of its rows.
+  // Its partials stay empty; it never influences the outputs, since the first
+  // rejection lies before it.
+  bool skip = false;
+  if (a.ws_reject != nullptr) {
+    const unsigned v = __ldcg(&a.ws_reject[b]);
+    skip = v != 0u && K + 1 - (int)v < i;
+  }
   // The token-draw launch that follows (deferred sampling) may be scheduled
   // from now on; it waits for this whole grid to complete before it reads
   // anything this grid writes.
@@ -320,7 +337,9 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   const int seg_groups = a.seg_tiles * kSegGroups;
   const int nseg = a.segs_per_slice;
   bool copy_ok = true;
-  if (!pair && a.ws_seg != nullptr) {
+  if (skip) {
+    // nothing to read: a rejection before this position is already published
+  } else if (!pair && a.ws_seg != nullptr) {
     bonus_segment_stats<T, ALIGNED>(rowA, V, g_lo, g_hi, seg_groups, nseg,
                                     a.ws_seg + (b * S + rank) * (int64_t)nseg, mA, sA);
   } else if (RING) {
@@ -365,6 +384,19 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
     int fail = 0;
     for (int r = 0; r < S; ++r) fail |= *cluster.map_shared_rank(&sh.pfail, r);
     if (fail) s0 = s1 = kCopyFailedSum;
+    if (a.ws_reject != nullptr && pair && !fail && !skip) {
+      // publish this position's own decision when it rejects (the test the
+      // last cluster repeats from the same statistics, so the same outcome)
+      const int x = a.tokens[b * K + i];
+      if (x >= 0 && x < V && lambda_valid(lam_seq)) {
+        const PosStats st{m0, s0, m1, s1};
+        float qx = 0.0f;
+        const float ratio = accept_ratio(MODE, st, Elem<T>::load(rowA + x), Elem<T>::load(rowB + x),
+                                         lam_seq, nullptr, &qx);
+        if (!accept_test(a.u_accept[b * K + i], ratio))
+          atomicMax(&a.ws_reject[b], (unsigned)(K + 1 - i));
+      }
+    }
     a.ws_stats[p] = make_float4(m0, s0, m1, s1);
     __threadfence();
     const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
@@ -372,6 +404,7 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
     if (last) {
       __threadfence();
       a.ws_count[b] = 0;  // every position has arrived: leave the counter zero for the next call
+      if (a.ws_reject != nullptr) a.ws_reject[b] = 0;  // and the early-exit word
     }
     for (int r = 0; r < S; ++r) *cluster.map_shared_rank(&sh.last, r) = last;
   }
@@ -522,10 +555,18 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
   const int S = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
-  const int64_t p = (int64_t)blockIdx.x / S;
+  const int64_t pl = (int64_t)blockIdx.x / S;  // the cluster's position in launch order
   const int K = a.K, V = a.V;
-  const int64_t b = p / (K + 1);
-  const int i = (int)(p - b * (K + 1));
+  int64_t b;
+  int i;
+  if (a.pos_major) {
+    i = (int)(pl / a.B);
+    b = pl - (int64_t)i * a.B;
+  } else {
+    b = pl / (K + 1);
+    i = (int)(pl - b * (K + 1));
+  }
+  const int64_t p = b * (K + 1) + i;
   const bool pair = i < K;
   const T *tgt = static_cast<const T *>(a.target);
   const T *dft = static_cast<const T *>(a.draft);
@@ -535,11 +576,19 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
   const int g_hi = min(a.num_groups, g_lo + a.groups_per_slice);
   const float lam = a.lam[b];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // early exit: nothing to read after a published mismatch of this sequence
+  bool skip = false;
+  if (a.ws_reject != nullptr) {
+    const unsigned v = __ldcg(&a.ws_reject[b]);
+    skip = v != 0u && K + 1 - (int)v < i;
+  }
 
   float best = -INFINITY;
   int bidx = INT_MAX;
   bool copy_ok = true;
-  if (RING) {
+  if (skip) {
+    // an earlier position of this sequence is already known to mismatch
+  } else if (RING) {
     copy_ok = ring_stream<kNT>(sh.ring, g_ring_buf, rowA, rowB, pair, g_lo, g_hi,
                                [&](const uint4 *cA, const uint4 *cB, int cnt, int c_lo) {
 #pragma unroll
@@ -551,7 +600,7 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
                                  }
                                });
   }
-  for (int g0 = g_lo + (int)threadIdx.x; !RING && g0 < g_hi; g0 += kNT * kUnroll) {
+  for (int g0 = g_lo + (int)threadIdx.x; !RING && !skip && g0 < g_hi; g0 += kNT * kUnroll) {
     uint4 za[kUnroll], zb[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -592,6 +641,12 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
       fail |= *cluster.map_shared_rank(&sh.pfail, r);
     }
     if (fail) ix = kCopyFailedIndex;
+    if (a.ws_reject != nullptr && pair && !fail && !skip) {
+      // publish this position's mismatch (the last cluster repeats the test)
+      const int x = a.tokens[b * K + i];
+      if (x >= 0 && x < V && lambda_valid(lam) && ix != x)
+        atomicMax(&a.ws_reject[b], (unsigned)(K + 1 - i));
+    }
     a.ws_stats[p] = make_float4(m, __int_as_float(ix), 0.0f, 0.0f);
     __threadfence();
     const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
@@ -599,6 +654,7 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
     if (last) {
       __threadfence();
       a.ws_count[b] = 0;
+      if (a.ws_reject != nullptr) a.ws_reject[b] = 0;
     }
     for (int r = 0; r < S; ++r) *cluster.map_shared_rank(&sh.last, r) = last;
   }

@@ -116,7 +116,9 @@ def test_plan_greedy_mode(lib, monkeypatch):
     refused; the debug entry point (probabilities) is refused too."""
     assert specv.plan(1_000_000, 4, 32, specv.F32, specv.GREEDY)["kernel"] == "tile-tma"
     p4 = specv.plan(256, 8, 128256, specv.F32, specv.GREEDY)
-    assert p4["kernel"] == "rows-stream" and p4["workspace_bytes"] == 256 * 9 * 16 + 256 * 4
+    # position candidates, arrival counters and the early-exit words (18 waves of CTAs)
+    assert p4["kernel"] == "rows-stream" and p4["workspace_bytes"] == 256 * 9 * 16 + 2 * 256 * 4
+    assert p4["early_exit"]
     # short rows off 16-byte boundaries: the streaming row kernel, not the generic tile
     assert specv.plan(5, 3, 33, specv.F32, specv.GREEDY)["kernel"] == "rows-stream"
     for v in ("resident", "spec", "sweep"):
@@ -155,6 +157,27 @@ def test_plan_ring_choice(lib, monkeypatch):
     assert specv.plan(2, 4, 131071, specv.F32)["kernel"] == "rows-stream"  # unaligned rows
     monkeypatch.setenv("SPECV_ROWS_RING", "0")
     assert specv.plan(32, 5, 152064, specv.BF16, specv.GREEDY)["kernel"] == "rows-stream"
+
+
+def test_plan_early_exit(lib, monkeypatch):
+    """Early exit is planned for the streaming kernels on grids of more than
+    two waves (the batched workload), not on one-wave grids (the Qwen-shaped
+    batch draws in a second launch) nor for the resident or tile kernels;
+    SPECV_EARLY_EXIT=0 turns it off.  It adds one scratch word per sequence."""
+    monkeypatch.delenv("SPECV_EARLY_EXIT", raising=False)
+    for mode in (specv.PROB_MIX, specv.LOGIT_MIX, specv.GREEDY):
+        p4 = specv.plan(256, 8, 128256, specv.F32, mode)
+        assert p4["early_exit"] and not p4["split_draws"]
+    p3 = specv.plan(32, 5, 152064, specv.BF16)
+    assert not p3["early_exit"] and p3["split_draws"]
+    assert not specv.plan(1, 8, 128256, specv.BF16)["early_exit"]       # resident
+    assert not specv.plan(1_000_000, 4, 32, specv.F32)["early_exit"]    # TMA tile
+    ws_on = specv.plan(256, 8, 128256, specv.F32)["workspace_bytes"]
+    monkeypatch.setenv("SPECV_EARLY_EXIT", "0")
+    p_off = specv.plan(256, 8, 128256, specv.F32)
+    assert not p_off["early_exit"] and ws_on == p_off["workspace_bytes"] + 256 * 4
+    with pytest.raises(specv.SpecvError):
+        specv.plan(0, 8, 128256, specv.F32)
 
 
 def _host_call(B=2, K=3, V=100, dtype=0, mode=0, chunks=0, null=None):

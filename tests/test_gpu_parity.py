@@ -110,10 +110,14 @@ def test_whole_row_probabilities(specv, cfg, mode):
     print(f"workload {cfg} mode={mode}: {rep}")
 
 
+@pytest.mark.parametrize("early", ["0", "1"], ids=["all-rows", "early-exit"])
 @pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
-def test_parity_full_size_batched_fp32_sampled(specv, mode):
+def test_parity_full_size_batched_fp32_sampled(specv, cluster_env, mode, early):
     """B=256, K=8, V=128256 fp32 as benchmarked; the oracle checks 32 sampled
-    sequences, and every drafted-equals-target sequence must accept all K."""
+    sequences, and every drafted-equals-target sequence must accept all K.
+    With SPECV_EARLY_EXIT=1 positions after a published rejection skip their
+    rows: the outputs must not change."""
+    os.environ["SPECV_EARLY_EXIT"] = early
     w = workloads.WORKLOADS[4]
     x = workloads.make_inputs(w, DEV)
     seqs = list(range(0, 128, 8)) + list(range(128, 256, 8))
@@ -223,6 +227,33 @@ def test_maximum_draft_length(specv, V, dt, mode):
     print(f"K=4096 V={V} {dt} mode={mode}: {rep}, n={n.tolist()}")
     assert n[1] == 4096 and (tok[1, :4096] == x["draft_tokens"][1].cpu().numpy()).all()
     assert 0 <= tok[1, 4096] < V
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+@pytest.mark.parametrize("shape", [(400, 3, 4099, "f32", "corr:3.0:0.85:1.0"),
+                                   (96, 8, 65536, "bf16", "half_equal:3.0:0.85:1.0"),
+                                   (200, 6, 20000, "f32", "rho:3.0:0.5:0.95")],
+                         ids=lambda s: f"B{s[0]}K{s[1]}V{s[2]}{s[3]}")
+def test_early_exit_parity(specv, cluster_env, shape, mode):
+    """Early exit (SPECV_EARLY_EXIT=1): grids of several waves, position-major,
+    positions after a published rejection read nothing.  Every sequence agrees
+    with the oracle, and with the all-rows run bit for bit."""
+    B, K, V, dt, st = shape
+    w = workloads.Workload("early", B, K, V, dt, st, (0.3,), 37)
+    x = workloads.make_inputs(w, DEV)
+    args = (x["target_logits"], x["draft_logits"], x["draft_tokens"], x["u_accept"],
+            x["u_resample"], x["lam"])
+    os.environ["SPECV_EARLY_EXIT"] = "0"
+    t0, n0 = specv.verify(*args, mode=mode)
+    os.environ["SPECV_EARLY_EXIT"] = "1"
+    assert specv.plan(B, K, V, 1 if dt == "bf16" else 0, mode)["kernel"] == "rows-stream"
+    t1, n1 = specv.verify(*args, mode=mode)
+    t2, n2 = specv.verify(*args, mode=mode)  # the scratch words were left at zero
+    torch.cuda.synchronize()
+    assert torch.equal(t0, t1) and torch.equal(n0, n1)
+    assert torch.equal(t1, t2) and torch.equal(n1, n2)
+    rep, _, _ = _check(specv, x, mode, debug=False)
+    print(f"{shape} mode={mode}: {rep}")
 
 
 RAGGED = [

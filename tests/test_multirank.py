@@ -105,3 +105,16 @@ def test_l2_flush_runs_on_any_device():
     f = bench.L2Flush("cpu", 1 << 16)
     f(3)
     assert float(f.w[0]) == 3.0 and float(f.sink) == 0.0
+
+
+def test_needed_bytes_of_early_exit():
+    """The benchmark's algorithmic bytes under early exit: the row pairs of
+    positions 0..n and, when every draft passes, the bonus row; an invalid
+    sequence counts every row."""
+    K, V, s = 8, 10, 4
+    n = torch.tensor([0, 3, 8, -1], dtype=torch.int32)
+    rows = 2 * 1 + 2 * 4 + (2 * 8 + 1) + (2 * 8 + 1)
+    assert bench.needed_bytes(n, K, V, s) == rows * V * s
+    # every sequence accepting all drafts needs every row: (2K+1) B V s
+    allk = torch.full((5,), K, dtype=torch.int32)
+    assert bench.needed_bytes(allk, K, V, s) == (2 * K + 1) * 5 * V * s
