@@ -359,9 +359,13 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
                                                              mB, sB);
                                });
   } else {
-    slice_stats<T, MODE, ALIGNED, kNT, kUnroll>(rowA, rowB, pair, lam_seq, V, g_lo, g_hi, mA, sA,
-                                                 mB, sB);
+    // with early exit the stream stops when an earlier rejection is published meanwhile
+    const bool stopped = slice_stats<T, MODE, ALIGNED, kNT, kUnroll>(
+        rowA, rowB, pair, lam_seq, V, g_lo, g_hi, mA, sA, mB, sB,
+        a.ws_reject != nullptr ? &a.ws_reject[b] : nullptr, i, K);
+    skip = stopped;
   }
+  if (a.ws_reject != nullptr) skip = __syncthreads_or(skip) != 0;  // CTA-wide: partial statistics
   block_merge_stats<kNT>(sh.bs, mA, sA, mB, sB);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -600,7 +604,16 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
                                  }
                                });
   }
-  for (int g0 = g_lo + (int)threadIdx.x; !RING && !skip && g0 < g_hi; g0 += kNT * kUnroll) {
+  unsigned seen = 0u;  // early exit while streaming, as in slice_stats
+  int it = 0;
+  for (int g0 = g_lo + (int)threadIdx.x; !RING && !skip && g0 < g_hi; g0 += kNT * kUnroll, ++it) {
+    if (a.ws_reject != nullptr && it % kExitEvery == 0) {
+      if (seen != 0u && K + 1 - (int)seen < i) {
+        skip = true;
+        break;
+      }
+      seen = __ldcg(&a.ws_reject[b]);
+    }
     uint4 za[kUnroll], zb[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -616,6 +629,7 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
       if (g < g_hi) greedy_fold_group<T>(za[u], pair ? zb[u] : za[u], pair, lam, g * VW, best, bidx);
     }
   }
+  if (a.ws_reject != nullptr) skip = __syncthreads_or(skip) != 0;  // CTA-wide: partial candidates
   warp_argmax(best, bidx);
   if (lane == 0) {
     sh.bs.red[warp][0] = best;

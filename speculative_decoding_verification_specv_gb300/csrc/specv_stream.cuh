@@ -114,11 +114,28 @@ __device__ __forceinline__ void fold_batch(const uint4 (&za)[U], const uint4 (&z
     }
 }
 
+// Early exit while streaming: every kExitEvery batches each warp reads the
+// sequence's early-exit word (every lane the same address: one transaction)
+// and, when it shows a rejection before position `pos`, stops reading; a value
+// is acted on kExitEvery batches after it was loaded, so the load's latency is
+// never waited for.
+constexpr int kExitEvery = 4;
+
+// Returns true if the thread stopped early (its statistics are then partial:
+// the position lies after the sequence's first rejection and is never used).
 template <typename T, int MODE, bool ALIGNED, int NT, int U>
-__device__ __forceinline__ void slice_stats(const T *rowA, const T *rowB, bool pair, float lam,
+__device__ __forceinline__ bool slice_stats(const T *rowA, const T *rowB, bool pair, float lam,
                                             int V, int g_lo, int g_hi, float &mA, float &sA,
-                                            float &mB, float &sB) {
-  for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += NT * U) {
+                                            float &mB, float &sB,
+                                            const unsigned *exit_word = nullptr, int pos = 0,
+                                            int K = 0) {
+  unsigned seen = 0u;
+  int it = 0;
+  for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += NT * U, ++it) {
+    if (exit_word != nullptr && it % kExitEvery == 0) {
+      if (seen != 0u && K + 1 - (int)seen < pos) return true;
+      seen = __ldcg(exit_word);
+    }
     uint4 za[U], zb[U];
     bool ok[U];
 #pragma unroll
@@ -132,6 +149,7 @@ __device__ __forceinline__ void slice_stats(const T *rowA, const T *rowB, bool p
     }
     fold_batch<T, MODE, U>(za, zb, ok, pair, lam, mA, sA, mB, sB);
   }
+  return false;
 }
 
 }  // namespace specv
