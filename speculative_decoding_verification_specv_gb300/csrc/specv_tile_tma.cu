@@ -107,6 +107,7 @@ template <typename T, int MODE>
 __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
   constexpr bool GREEDY = MODE == kGreedy;  // argmax per row; no draft-row tasks, no sampling
   constexpr int VW = Elem<T>::kPerVec;
+  constexpr int kCacheC = 1;  // stage-B groups per lane whose weights are kept
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
   const int K = a.K, V = a.V, TS = a.tile_seqs;
@@ -345,10 +346,28 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
       const uint4 *ra = reinterpret_cast<const uint4 *>(st_t + (int64_t)pos * V);
       const uint4 *rb = reinterpret_cast<const uint4 *>(st_d + ((int64_t)sl * K + (nn < K ? nn : 0)) * V);
       int tok = -1;
+      // weights of the lane's first kCacheC groups, kept in registers for the
+      // owner's walk (short rows: every group of the lane)
+      float wc[kCacheC][VW];
       for (int attempt = 0; attempt < 2; ++attempt) {
         float mysum = 0.0f;
         int mylast = -1;
-        for (int c = 0; c < C; ++c) {
+#pragma unroll
+        for (int c = 0; c < kCacheC; ++c) {
+          const int g = gl * C + c;
+          if (c < C && g < G) {
+            const uint4 za = ra[g];
+            const uint4 zb = kind != kWBonus ? rb[g] : za;
+#pragma unroll
+            for (int e = 0; e < VW; ++e) {
+              const float w = sample_weight_sel(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e));
+              wc[c][e] = w;
+              mysum = __fadd_rn(mysum, w);
+              if (w > 0.0f) mylast = g * VW + e;
+            }
+          }
+        }
+        for (int c = kCacheC; c < C; ++c) {
           const int g = gl * C + c;
           if (g < G) {
             const uint4 za = ra[g];
@@ -381,7 +400,20 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
         if (own) {  // walk this lane's entries in order (no warp collectives inside)
           float c0 = excl;
           int lastg = -1;
-          for (int c = 0; c < C && pick < 0; ++c) {
+#pragma unroll
+          for (int c = 0; c < kCacheC; ++c) {
+            const int g = gl * C + c;
+            if (c < C && g < G && pick < 0) {
+#pragma unroll
+              for (int e = 0; e < VW; ++e) {
+                const float w = wc[c][e];
+                c0 = __fadd_rn(c0, w);
+                if (w > 0.0f) lastg = g * VW + e;
+                if (pick < 0 && c0 > t) pick = g * VW + e;
+              }
+            }
+          }
+          for (int c = kCacheC; c < C && pick < 0; ++c) {
             const int g = gl * C + c;
             if (g < G) {
               const uint4 za = ra[g];
