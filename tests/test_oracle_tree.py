@@ -8,7 +8,10 @@ the EAGLE explainer describe the trees, not this rule).
 Pinned by: reduction to the pinned chain loop when every node has one child;
 the lossless property (the first emitted token is distributed as p~ at the
 root) by exact enumeration of the drafted tokens and a rank-1 lattice over the
-uniforms; hand-worked cases; invalid inputs.
+uniforms; the same two levels deep (the second token, given the first, is
+distributed as p~ at the accepted child; this alone catches a walk that skips
+the residual update between siblings below the root); hand-worked cases;
+invalid inputs.
 """
 import math
 
@@ -92,6 +95,83 @@ def test_tree_is_lossless_at_the_root(oracle_mod, mode, lam, children):
         first = r.tokens[:, 0]
         dist += weight * np.bincount(first, minlength=V) / n
     np.testing.assert_allclose(dist, p_root, atol=2e-3)
+
+
+def _softmax64(z):
+    e = np.exp(np.asarray(z, np.float64) - np.max(z))
+    return e / e.sum()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("lam", [0.0, 0.35])
+def test_tree_is_lossless_two_levels_deep(oracle_mod, mode, lam):
+    """Root with two children, each with two leaf children (V = 3).  As for a
+    real model, a node's target row and the draft row of its children depend
+    only on the tokens of its path.  Over every draw of the six drafted tokens
+    (weighted by their probability under the drafting node's q) and a scrambled
+    Sobol set of the seven uniforms: the first token is distributed as p~ at the
+    root and, when a child was accepted (n >= 1), the second token given the
+    first token a is distributed as p~ at the child holding a.  A walk that kept
+    the root's p after an acceptance, tested the leaves against the root's q or
+    drew them from the wrong row would break the second statement."""
+    qmc = pytest.importorskip("scipy.stats.qmc")
+    V = 3
+    rng = np.random.default_rng(29)
+    R0 = rng.normal(0, 1.1, V).astype(np.float32)         # root target row
+    Q0 = rng.normal(0, 1.1, V).astype(np.float32)         # root's draft row
+    R1 = rng.normal(0, 1.1, (V, V)).astype(np.float32)    # target row of a child holding a
+    Q1 = rng.normal(0, 1.1, (V, V)).astype(np.float32)    # its draft row
+    R2 = rng.normal(0, 1.1, (V, V, V)).astype(np.float32)  # leaf rows (bonus only)
+    pad = np.zeros(V, np.float32)
+    p_root = oracle_mod.rows(np.stack([R0, pad]), Q0[None], lam, mode)[0][0]
+    p_child = np.stack([oracle_mod.rows(np.stack([R1[a], pad]), Q1[a][None], lam, mode)[0][0]
+                        for a in range(V)])
+    # the second statement can tell the child's p~ from the root's
+    assert np.abs(p_child - p_root[None]).max() > 0.1
+    q0 = _softmax64(Q0)
+    q1 = np.stack([_softmax64(Q1[a]) for a in range(V)])
+
+    n = 1 << 11
+    u = qmc.Sobol(d=7, scramble=True, seed=5).random_base2(m=11).astype(np.float32)
+    u = np.minimum(u, np.nextafter(np.float32(1), np.float32(0)))
+    leaves = np.array(list(np.ndindex(V, V, V, V)), np.int32)  # tokens of nodes 3, 4, 5, 6
+    L = len(leaves)
+    B = L * n
+    parent = np.tile(np.array([-1, 0, 0, 1, 1, 2, 2], np.int32), (B, 1))
+    drow = np.tile(np.array([0, 1, 2, -1, -1, -1, -1], np.int32), (B, 1))
+    ua = np.zeros((B, 7), np.float32)
+    ua[:, 1:] = np.tile(u[:, :6], (L, 1))
+    ur = np.tile(u[:, 6], L)
+    lam_b = np.full(B, lam, np.float32)
+    first = np.zeros(V)
+    reached = np.zeros(V)        # P(first token a, a child accepted)
+    joint = np.zeros((V, V))     # P(first token a, a child accepted, second token c)
+    for t1, t2 in np.ndindex(V, V):
+        tok = np.zeros((B, 7), np.int32)
+        tok[:, 1], tok[:, 2] = t1, t2
+        tok[:, 3:] = np.repeat(leaves, n, axis=0)
+        zt = np.empty((B, 7, V), np.float32)
+        zt[:, 0], zt[:, 1], zt[:, 2] = R0, R1[t1], R1[t2]
+        for j, par_tok in ((3, t1), (4, t1), (5, t2), (6, t2)):
+            zt[:, j] = R2[par_tok][tok[:, j]]
+        zq = np.empty((B, 3, V), np.float32)
+        zq[:, 0], zq[:, 1], zq[:, 2] = Q0, Q1[t1], Q1[t2]
+        r = oracle_mod.verify_tree(zt, zq, parent, drow, tok, ua, ur, lam_b, mode=mode)
+        w = q0[t1] * q0[t2] * np.prod(
+            [q1[t1][leaves[:, 0]], q1[t1][leaves[:, 1]], q1[t2][leaves[:, 2]],
+             q1[t2][leaves[:, 3]]], axis=0)                 # [L]
+        wb = np.repeat(w, n) / n                            # weight of each sequence
+        t0, s1 = r.tokens[:, 0], r.tokens[:, 1]
+        acc = r.n_accepted >= 1
+        for a in range(V):
+            first[a] += wb[t0 == a].sum()
+            reached[a] += wb[(t0 == a) & acc].sum()
+            for c in range(V):
+                joint[a, c] += wb[(t0 == a) & acc & (s1 == c)].sum()
+    assert abs(first.sum() - 1.0) < 1e-9
+    np.testing.assert_allclose(first, p_root, atol=4e-3)
+    assert reached.min() > 0.05
+    np.testing.assert_allclose(joint, reached[:, None] * p_child, atol=4e-3)
 
 
 def test_tree_hand_cases(oracle_mod):
