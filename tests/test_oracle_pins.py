@@ -288,6 +288,35 @@ def test_zero_uniform_accepts_unless_ptilde_is_zero(oracle_mod):
     assert r.n_accepted[0] == 0 and r.tokens[0].tolist() == [1, -1]
 
 
+def test_decision_margins_hand_case(oracle_mod):
+    """The margins that the GPU parity tests use to tell a rounding-order tie
+    from a real mismatch: accept_margin is the smallest |u_i - min(1, ratio_i)|
+    over the positions actually decided (none after the first rejection), and
+    cdf_margin the smallest |u - C_v / W| over the boundaries of the CDF the
+    token was drawn from."""
+    # p_t rows (0.25, 0.75), (0.5, 0.5), bonus row (0.5, 0.5); q rows (0.5, 0.5);
+    # lambda = 0; both drafts are token 0
+    zt = np.log(np.array([[[0.25, 0.75], [0.5, 0.5], [0.5, 0.5]]])).astype(np.float32)
+    zq = np.log(np.array([[[0.5, 0.5], [0.5, 0.5]]])).astype(np.float32)
+    tok = np.array([[0, 0]], np.int32)
+    lam = np.array([0.0], np.float32)
+    # position 0: ratio 0.5, u = 0.6 rejects; position 1 (u = 0.98, ratio 1) is
+    # never decided, so its distance 0.02 does not count.  Residual (0, 0.25):
+    # boundaries 0 and 1, u = 0.3 -> token 1 at distance 0.3.
+    r = oracle_mod.verify(zt, zq, tok, np.array([[0.6, 0.98]], np.float32),
+                          np.array([0.3], np.float32), lam)
+    assert r.n_accepted.tolist() == [0] and r.tokens.tolist() == [[1, -1, -1]]
+    assert r.accept_margin[0] == pytest.approx(0.1, abs=1e-6)
+    assert r.cdf_margin[0] == pytest.approx(0.3, abs=1e-6)
+    # both accepted (distances 0.1 and 0.02); bonus from (0.5, 0.5): boundaries
+    # 0.5 and 1, u = 0.3 -> token 0 at distance 0.2
+    r = oracle_mod.verify(zt, zq, tok, np.array([[0.4, 0.98]], np.float32),
+                          np.array([0.3], np.float32), lam)
+    assert r.n_accepted.tolist() == [2] and r.tokens.tolist() == [[0, 0, 0]]
+    assert r.accept_margin[0] == pytest.approx(0.02, abs=1e-6)
+    assert r.cdf_margin[0] == pytest.approx(0.2, abs=1e-6)
+
+
 def test_seq_range_and_threads_do_not_change_results(oracle_mod):
     w = workloads.WORKLOADS[3].scaled(B=12, V=999)
     x = workloads.make_inputs(w)
