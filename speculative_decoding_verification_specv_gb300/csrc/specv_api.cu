@@ -103,8 +103,13 @@ bool cached_workspace(int dev, cudaStream_t stream, int64_t B, size_t data_bytes
   if (w->count_len < B) {
     const size_t sz = grow_to((size_t)B * sizeof(unsigned));
     void *ptr = nullptr;
-    if (cudaMalloc(&ptr, sz) != cudaSuccess || cudaMemsetAsync(ptr, 0, sz, stream) != cudaSuccess) {
+    if (cudaMalloc(&ptr, sz) != cudaSuccess) {
       (void)cudaGetLastError();
+      return false;
+    }
+    if (cudaMemsetAsync(ptr, 0, sz, stream) != cudaSuccess) {
+      (void)cudaGetLastError();
+      (void)cudaFree(ptr);
       return false;
     }
     w->count = static_cast<unsigned *>(ptr);
