@@ -109,3 +109,51 @@ def test_inputs_are_seeded_and_offsets_differ():
     assert not torch.equal(a["u_accept"], c["u_accept"])
     u = torch.cat([a["u_accept"].ravel(), a["u_resample"]])
     assert (u >= 0).all() and (u < 1).all()
+
+
+@pytest.mark.parametrize("kind", ["chain", "kary:2", "kary:3", "star", "random:3"])
+def test_tree_shapes(kind):
+    N = 13
+    par = workloads.tree_shape(kind, N, seed=4)
+    assert len(par) == N + 1 and par[0] == -1
+    assert all(0 <= par[j] < j for j in range(1, N + 1))  # parents before children
+    name = kind.split(":")[0]
+    if name == "chain":
+        assert par[1:] == list(range(N))
+    elif name == "star":
+        assert par[1:] == [0] * N
+    elif name == "kary":
+        k = int(kind.split(":")[1])
+        for u in range(N + 1):
+            kids = [j for j in range(1, N + 1) if par[j] == u]
+            if kids:  # at most k children, numbered contiguously
+                assert len(kids) <= k and kids == list(range(kids[0], kids[0] + len(kids)))
+    else:
+        assert all(j - par[j] <= 3 for j in range(1, N + 1))
+
+
+def test_tree_inputs_draw_children_from_their_parents_draft_row():
+    """Draft rows are numbered in node order over the nodes with children;
+    every child's token is a draw from its parent's draft row (its average log
+    probability there beats every other draft row of the tree by a wide margin,
+    and the token counts pass a chi-square test against that row's softmax)."""
+    from scipy import stats
+    B, N, V = 3000, 6, 12
+    x = workloads.make_tree_inputs(B, N, V, "f32", "kary:2", s=1.5, a=0.3, e=1.5, seed=3)
+    par = x["parent"][0].tolist()
+    drow = x["draft_row"][0].tolist()
+    assert drow == [0, 1, 2, -1, -1, -1, -1]
+    assert (x["parent"] == x["parent"][:1]).all() and (x["draft_row"] == x["draft_row"][:1]).all()
+    zq = _np(x["draft_logits"])                        # [B][M][V]
+    logq = zq - zq.max(-1, keepdims=True)
+    logq -= np.log(np.exp(logq).sum(-1, keepdims=True))
+    tok = x["tokens"].numpy()
+    M = zq.shape[1]
+    for j in range(1, N + 1):
+        own = drow[par[j]]
+        ll = [float(np.mean(logq[np.arange(B), r, tok[:, j]])) for r in range(M)]
+        assert all(ll[own] > ll[r] + 0.1 for r in range(M) if r != own), (j, ll)
+        p = np.exp(logq[:, own, :])                    # [B][V]
+        counts = np.bincount(tok[:, j], minlength=V)
+        chi2, pval = stats.chisquare(counts, p.sum(0))
+        assert pval > 1e-4, (j, chi2, pval)
