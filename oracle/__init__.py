@@ -77,9 +77,14 @@ def _load():
         lib.oracle_verify.argtypes = [fp, fp, ip, fp, fp, fp, i64, i64, ctypes.c_int32, i64,
                                       ctypes.c_int, ip, ip, dp, dp, dp, dp, dp, dp, ip]
         lib.oracle_verify.restype = ctypes.c_int
-        lib.oracle_greedy_argmax.argtypes = [fp, fp, ctypes.c_float, i64]
+        lib.oracle_mix_logit_entry.argtypes = [ctypes.c_double] * 3
+        lib.oracle_mix_logit_entry.restype = ctypes.c_double
+        lib.oracle_greedy_scores.argtypes = [fp, fp, ctypes.c_float, i64, dp]
+        lib.oracle_greedy_scores.restype = None
+        lib.oracle_greedy_argmax.argtypes = [fp, fp, ctypes.c_float, i64, dp]
         lib.oracle_greedy_argmax.restype = i64
-        lib.oracle_verify_greedy.argtypes = [fp, fp, ip, fp, i64, i64, ctypes.c_int32, i64, ip, ip]
+        lib.oracle_verify_greedy.argtypes = [fp, fp, ip, fp, i64, i64, ctypes.c_int32, i64, ip, ip,
+                                             dp]
         lib.oracle_verify_greedy.restype = None
         lib.oracle_verify_tree.argtypes = [fp, fp, ip, ip, ip, fp, fp, fp, i64, i64,
                                            ctypes.c_int32, ctypes.c_int32, i64, ctypes.c_int, ip,
@@ -232,18 +237,41 @@ def verify(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam,
     return res
 
 
-def greedy_argmax(zt_row, zq_row, lam: float) -> int:
-    """Argmax of w = z_t + lam (z_q - z_t) over one row, in fp32 as the kernels
-    form it (zq_row None: w = z_t); the first index among equal maxima."""
+def mix_logit_entry(zt: float, zq: float, lam: float) -> float:
+    """One entry of (1 - lam) z_t + lam z_q with the masking rule (a -inf
+    logit of positive weight gives -inf; a term of weight zero drops out)."""
+    return float(_load().oracle_mix_logit_entry(float(zt), float(zq), float(lam)))
+
+
+def greedy_scores(zt_row, zq_row, lam: float) -> np.ndarray:
+    """The fp64 greedy scores w = (1 - lam) z_t + lam z_q of one row (zq_row
+    None: w = z_t), with lam taken as the fp32 value the kernels read."""
     zt = _f32(zt_row).reshape(-1)
     zq = None if zq_row is None else _f32(zq_row).reshape(-1)
-    return int(_load().oracle_greedy_argmax(_ptr(zt, ctypes.c_float), _ptr(zq, ctypes.c_float),
-                                            float(np.float32(lam)), zt.size))
+    out = np.empty(zt.size, np.float64)
+    _load().oracle_greedy_scores(_ptr(zt, ctypes.c_float), _ptr(zq, ctypes.c_float),
+                                 float(np.float32(lam)), zt.size, _ptr(out, ctypes.c_double))
+    return out
+
+
+def greedy_argmax(zt_row, zq_row, lam: float, with_gap: bool = False):
+    """Argmax of the fp64 greedy scores of one row (zq_row None: w = z_t), the
+    first index among equal maxima; with_gap also returns the relative gap
+    (w_best - w_second) / max |logit| of the row."""
+    zt = _f32(zt_row).reshape(-1)
+    zq = None if zq_row is None else _f32(zq_row).reshape(-1)
+    gap = ctypes.c_double(0.0)
+    idx = int(_load().oracle_greedy_argmax(_ptr(zt, ctypes.c_float), _ptr(zq, ctypes.c_float),
+                                           float(np.float32(lam)), zt.size, ctypes.byref(gap)))
+    return (idx, float(gap.value)) if with_gap else idx
 
 
 def verify_greedy(target_logits, draft_logits, draft_tokens, lam,
                   threads: int | None = None) -> Result:
-    """Greedy verification of a batch (same layouts as ``verify``)."""
+    """Greedy verification of a batch (same layouts as ``verify``).  Returns
+    tokens, n_accepted and tie_margin [B]: the smallest relative gap between
+    the best and second-best fp64 score over the mixed rows the decision read
+    (+inf if none)."""
     zt = _f32(target_logits)
     zq = _f32(draft_logits)
     tok = _i32(draft_tokens)
@@ -253,12 +281,14 @@ def verify_greedy(target_logits, draft_logits, draft_tokens, lam,
     assert zq.shape == (B, K, V) and tok.shape == (B, K) and lm.shape == (B,)
     out_tok = np.full((B, K + 1), -2, np.int32)
     out_n = np.full((B,), -2, np.int32)
+    margin = np.full((B,), np.nan, np.float64)
     lib = _load()
 
     def run(lo, hi):
         lib.oracle_verify_greedy(_ptr(zt, ctypes.c_float), _ptr(zq, ctypes.c_float),
                                  _ptr(tok, ctypes.c_int32), _ptr(lm, ctypes.c_float), lo, hi, K,
-                                 V, _ptr(out_tok, ctypes.c_int32), _ptr(out_n, ctypes.c_int32))
+                                 V, _ptr(out_tok, ctypes.c_int32), _ptr(out_n, ctypes.c_int32),
+                                 _ptr(margin, ctypes.c_double))
 
     nthreads = threads if threads is not None else (os.cpu_count() or 1)
     nthreads = max(1, min(nthreads, B))
@@ -268,7 +298,7 @@ def verify_greedy(target_logits, draft_logits, draft_tokens, lam,
         edges = np.linspace(0, B, nthreads + 1).astype(np.int64)
         with ThreadPoolExecutor(max_workers=nthreads) as ex:
             list(ex.map(lambda j: run(int(edges[j]), int(edges[j + 1])), range(nthreads)))
-    return Result(tokens=out_tok, n_accepted=out_n, threads=nthreads)
+    return Result(tokens=out_tok, n_accepted=out_n, tie_margin=margin, threads=nthreads)
 
 
 def verify_tree(target_logits, draft_logits, parent, draft_row, tokens, u_accept, u_resample,

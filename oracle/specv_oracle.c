@@ -46,16 +46,22 @@
  *   - Invalid input (a draft token outside [0, V), or lambda outside [0, 1]
  *     or NaN) gives n_accepted = -1 and all output tokens -1.
  *
+ *   - Masked logits (-inf: a padded vocabulary, a grammar or top-k mask) in
+ *     the logit mixture (1 - lambda) z_t + lambda z_q: a masked entry of a
+ *     row whose weight is positive masks the mixed entry, and a term of
+ *     weight zero drops out (so lambda = 0 gives z_t and lambda = 1 gives
+ *     z_q whatever the other row holds).
  *   - Greedy verification (the greedy clause of [EAGLE] "核心思路") is read as:
  *     accept x_i iff x_i is the argmax of the mixed logits
- *     w = z_t + lambda (z_q - z_t) of row i (the logit-space enhanced target,
- *     whose softmax is p~ in logit mode; lambda = 0 gives the target's own
- *     argmax, the clause as printed), emit that argmax at the first mismatch,
- *     and the argmax of target row K when every draft matches.  Equal maxima
- *     go to the smallest index.  w is formed in fp32 exactly as the kernels
- *     form it (one rounded subtraction, one fused multiply-add; -inf where
- *     z_q = -inf), because an argmax is an integer decided by floating point:
- *     both sides must decide it in the same precision.
+ *     w = (1 - lambda) z_t + lambda z_q of row i (the logit-space enhanced
+ *     target, whose softmax is p~ in logit mode; lambda = 0 gives the
+ *     target's own argmax, the clause as printed), emit that argmax at the
+ *     first mismatch, and the argmax of target row K when every draft
+ *     matches.  Equal maxima go to the smallest index.  w is formed in
+ *     double precision like everything else; for each decided mixed row the
+ *     oracle also reports the gap between the largest and the second largest
+ *     w relative to the row's largest logit magnitude, so that a caller can
+ *     tell which rows a lower-precision argmax may decide otherwise.
  *
  * Everything is computed in double precision.  fp32 inputs are promoted
  * exactly; bf16 inputs are widened to fp32 (exactly) by the caller first.
@@ -99,14 +105,31 @@ void oracle_mix_prob(const double *pt, const double *pq, double lambda, int64_t 
     for (int64_t v = 0; v < V; ++v) out[v] = (1.0 - lambda) * pt[v] + lambda * pq[v];
 }
 
+/* One entry of the logit-space mixture (1 - lambda) * z_t + lambda * z_q
+ * ([RAPID] "3) 候选验证机制": enhanced_target = (1-λ)*target_logits +
+ * λ*draft_logits), with the masking reading of the header: a -inf logit whose
+ * weight is positive gives -inf, a term of weight zero contributes nothing. */
+double oracle_mix_logit_entry(double zt, double zq, double lambda)
+{
+    double a = 1.0 - lambda, b = lambda, w = 0.0;
+    if (a > 0.0) {
+        if (zt == -INFINITY) return -INFINITY;
+        w += a * zt;
+    }
+    if (b > 0.0) {
+        if (zq == -INFINITY) return -INFINITY;
+        w += b * zq;
+    }
+    return w;
+}
+
 /* logit-mode mixture p~ = softmax((1 - lambda) * z_t + lambda * z_q)
- * [RAPID] "3) 候选验证机制": enhanced_target = (1-λ)*target_logits + λ*draft_logits,
- * then p_t = softmax(enhanced_target[i]). */
+ * [RAPID] "3) 候选验证机制": then p_t = softmax(enhanced_target[i]). */
 void oracle_mix_logit(const double *zt, const double *zq, double lambda, int64_t V,
                       double *out)
 {
     double *w = (double *)malloc((size_t)V * sizeof(double));
-    for (int64_t v = 0; v < V; ++v) w[v] = (1.0 - lambda) * zt[v] + lambda * zq[v];
+    for (int64_t v = 0; v < V; ++v) w[v] = oracle_mix_logit_entry(zt[v], zq[v], lambda);
     oracle_softmax(w, V, out);
     free(w);
 }
@@ -327,36 +350,63 @@ int oracle_verify(const float *zt, const float *zq, const int32_t *tok, const fl
 /* ------------------------------------------------------------------------ */
 /* Greedy verification (reading in the header).                              */
 
-/* w of one entry, in fp32 as the kernels form it. */
-static float greedy_w(float zt, float zq, float lam)
+/* The greedy scores of one row: w_v = (1 - lambda) z_t + lambda z_q with
+ * the masking rule (zq == NULL: w = z_t, the bonus position). */
+void oracle_greedy_scores(const float *zt, const float *zq, float lam, int64_t V, double *w)
 {
-    if (zq == -INFINITY) return -INFINITY;
-    float d = zq - zt;          /* one rounded fp32 subtraction */
-    return fmaf(lam, d, zt);    /* one fused multiply-add */
+    for (int64_t v = 0; v < V; ++v)
+        w[v] = zq ? oracle_mix_logit_entry((double)zt[v], (double)zq[v], (double)lam)
+                  : (double)zt[v];
 }
 
-/* Argmax over v of w_v (zq == NULL: w = z_t, the bonus position); the first
- * index among equal maxima. */
-int64_t oracle_greedy_argmax(const float *zt, const float *zq, float lam, int64_t V)
+/* Argmax over v of w_v, the first index among equal maxima.  If rel_gap is
+ * not NULL it receives (w_best - w_second) / A, where w_second is the largest
+ * w at any other index and A the largest finite |z_t|, |z_q| of the row: how
+ * far the decision is from a tie, on the scale of the rounding error of a
+ * lower-precision w (0 for an exact tie or an all-zero row, +inf when every
+ * other entry is masked). */
+int64_t oracle_greedy_argmax(const float *zt, const float *zq, float lam, int64_t V,
+                             double *rel_gap)
 {
     int64_t best = 0;
-    float bw = zq ? greedy_w(zt[0], zq[0], lam) : zt[0];
-    for (int64_t v = 1; v < V; ++v) {
-        float w = zq ? greedy_w(zt[v], zq[v], lam) : zt[v];
-        if (w > bw) {
+    double bw = -INFINITY, second = -INFINITY, A = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        double w = zq ? oracle_mix_logit_entry((double)zt[v], (double)zq[v], (double)lam)
+                      : (double)zt[v];
+        if (v == 0 || w > bw) {
+            if (v > 0) second = bw;
             bw = w;
             best = v;
+        } else if (w > second) {
+            second = w;
         }
+        double at = fabs((double)zt[v]);
+        if (at != INFINITY && at > A) A = at;
+        if (zq) {
+            double aq = fabs((double)zq[v]);
+            if (aq != INFINITY && aq > A) A = aq;
+        }
+    }
+    if (rel_gap) {
+        if (V < 2 || second == -INFINITY)
+            *rel_gap = INFINITY;
+        else if (bw == second || !(A > 0.0))
+            *rel_gap = 0.0;
+        else
+            *rel_gap = (bw - second) / A;
     }
     return best;
 }
 
 /* Greedy verification of sequences [b0, b1); same layouts as oracle_verify.
  * Invalid input (token outside [0, V), lambda outside [0, 1] or NaN) gives
- * n_accepted = -1 and all tokens -1. */
+ * n_accepted = -1 and all tokens -1.  tie_margin [B] (or NULL) receives the
+ * smallest rel_gap of oracle_greedy_argmax over the mixed rows the decision
+ * read (rows 0 .. min(n, K-1)); the bonus row's w is z_t itself, exact in
+ * any precision, and is left out (+inf when no row counts). */
 void oracle_verify_greedy(const float *zt, const float *zq, const int32_t *tok, const float *lam,
                           int64_t b0, int64_t b1, int32_t K, int64_t V, int32_t *out_tok,
-                          int32_t *out_n)
+                          int32_t *out_n, double *tie_margin)
 {
     for (int64_t b = b0; b < b1; ++b) {
         const float *zt_b = zt + b * (int64_t)(K + 1) * V;
@@ -364,18 +414,23 @@ void oracle_verify_greedy(const float *zt, const float *zq, const int32_t *tok, 
         const int32_t *tk = tok + b * K;
         int32_t *ot = out_tok + b * (K + 1);
         double lambda = (double)lam[b];
+        double margin = INFINITY;
         int invalid = !(lambda >= 0.0 && lambda <= 1.0);
         for (int32_t i = 0; i < K; ++i)
             if (tk[i] < 0 || (int64_t)tk[i] >= V) invalid = 1;
         if (invalid) {
             for (int32_t i = 0; i <= K; ++i) ot[i] = -1;
             out_n[b] = -1;
+            if (tie_margin) tie_margin[b] = margin;
             continue;
         }
         int32_t n = K;
         int64_t token = -1;
         for (int32_t i = 0; i < K; ++i) {
-            int64_t a = oracle_greedy_argmax(zt_b + (int64_t)i * V, zq_b + (int64_t)i * V, lam[b], V);
+            double g = INFINITY;
+            int64_t a = oracle_greedy_argmax(zt_b + (int64_t)i * V, zq_b + (int64_t)i * V, lam[b],
+                                             V, &g);
+            if (g < margin) margin = g;
             if (a != (int64_t)tk[i]) {
                 n = i;
                 token = a;
@@ -383,10 +438,11 @@ void oracle_verify_greedy(const float *zt, const float *zq, const int32_t *tok, 
             }
             ot[i] = tk[i];
         }
-        if (n == K) token = oracle_greedy_argmax(zt_b + (int64_t)K * V, NULL, lam[b], V);
+        if (n == K) token = oracle_greedy_argmax(zt_b + (int64_t)K * V, NULL, lam[b], V, NULL);
         ot[n] = (int32_t)token;
         for (int32_t i = n + 1; i <= K; ++i) ot[i] = -1;
         out_n[b] = n;
+        if (tie_margin) tie_margin[b] = margin;
     }
 }
 

@@ -332,8 +332,9 @@ def test_seq_range_and_threads_do_not_change_results(oracle_mod):
 # --------------------------------------------------------------------------- greedy
 # The greedy clause of the EAGLE explainer ("核心思路", step 3): a draft token
 # equal to the target's most likely token is accepted.  Read with RAPID's
-# mixture as: accept x_i iff x_i = argmax_v w_v, w = z_t + lambda (z_q - z_t);
-# emit the argmax at the first mismatch, the argmax of target row K if all match.
+# mixture as: accept x_i iff x_i = argmax_v w_v, w = (1 - lambda) z_t + lambda z_q
+# (in double precision); emit the argmax at the first mismatch, the argmax of
+# target row K if all match.
 
 def _np_greedy(zt, zq, tok, lam):
     """Independent restatement for inputs on which every fp32 operation of w is
@@ -426,3 +427,99 @@ def test_greedy_ties_masked_drafts_and_invalid_inputs(oracle_mod):
     assert (res.tokens[1:] == -1).all()
     # all-equal rows: every argmax is 0, so drafts of 0 are all accepted
     assert res.tokens[0].tolist() == [0, 0, 0]
+
+
+def test_greedy_takes_the_exact_argmax_where_fp32_orders_the_other_way(oracle_mod):
+    """Two entries whose mixed logits differ by 6.4e-8: in exact rational
+    arithmetic entry 1 is larger, while z_t + lambda (z_q - z_t) formed in fp32
+    (one rounded subtraction, one fused multiply-add) makes entry 0 larger.
+    The oracle follows the mathematics, not the fp32 rounding."""
+    from fractions import Fraction as Fr
+    lam = np.float32(0.2884209)
+    zt = np.array([1.0595762729644775, 3.342172622680664], np.float32)
+    zq = np.array([1.8662627935409546, -3.765256643295288], np.float32)
+    L = Fr(float(lam))
+    exact = [(1 - L) * Fr(float(zt[v])) + L * Fr(float(zq[v])) for v in range(2)]
+    assert exact[1] > exact[0] and float(exact[1] - exact[0]) > 6e-8
+    # the fp32 path: each operation exact in fp64 here, then rounded once to fp32
+    d = np.float32(zq - zt)
+    w32 = [np.float32(float(Fr(float(lam)) * Fr(float(d[v])) + Fr(float(zt[v])))) for v in range(2)]
+    assert w32[0] > w32[1]
+    idx, gap = oracle_mod.greedy_argmax(zt, zq, lam, with_gap=True)
+    assert idx == 1
+    # the relative gap is the exact difference over the largest |logit| (3.765...)
+    assert gap == pytest.approx(float((exact[1] - exact[0]) / Fr(float(abs(zq[1])))), rel=1e-6)
+    assert gap < 2.0 ** -20  # inside the tie band of the GPU parity tests
+
+
+def test_greedy_tie_margin_covers_the_decided_rows_only(oracle_mod):
+    # K = 2, V = 3, lambda = 0: w = z_t.  Row 0 [0, 4, 1]: gap 3, max |z| 4
+    # (both rows count, so A = max(|z_t|, |z_q|) = 8 from z_q) -> 3/8.
+    # Row 1 [2, 2, 0] is an exact tie (gap 0) but is read only when x_0 = 1.
+    zt = np.array([[[0, 4, 1], [2, 2, 0], [5, 0, 0]]], np.float32)
+    zq = np.array([[[8, 0, 0], [0, 0, 1]]], np.float32)
+    lam = np.array([0.0], np.float32)
+    res = oracle_mod.verify_greedy(zt, zq, np.array([[0, 0]], np.int32), lam)
+    assert res.n_accepted.tolist() == [0] and res.tokens.tolist() == [[1, -1, -1]]
+    assert res.tie_margin[0] == pytest.approx(3 / 8)
+    res = oracle_mod.verify_greedy(zt, zq, np.array([[1, 0]], np.int32), lam)
+    assert res.n_accepted.tolist() == [2] and res.tokens.tolist() == [[1, 0, 0]]
+    assert res.tie_margin[0] == 0.0
+    # only the bonus row left: nothing of rounding to report
+    res = oracle_mod.verify_greedy(zt[:, 1:], zq[:, 1:], np.array([[0]], np.int32), lam)
+    assert res.n_accepted.tolist() == [1] and res.tie_margin[0] == 0.0
+
+
+# ------------------------------------------------------------- masked logits
+# Reading for -inf logits in the logit mixture (1 - lambda) z_t + lambda z_q:
+# a -inf entry of positive weight gives -inf; a zero-weight term drops out.
+
+def test_masked_logit_mixture_rule(oracle_mod):
+    ninf = float("-inf")
+    assert oracle_mod.mix_logit_entry(ninf, 1.5, 1.0) == 1.5
+    assert oracle_mod.mix_logit_entry(ninf, 1.5, 0.5) == ninf
+    assert oracle_mod.mix_logit_entry(ninf, 1.5, 0.0) == ninf
+    assert oracle_mod.mix_logit_entry(2.0, ninf, 0.0) == 2.0
+    assert oracle_mod.mix_logit_entry(2.0, ninf, 0.25) == ninf
+    assert oracle_mod.mix_logit_entry(2.0, ninf, 1.0) == ninf
+    assert oracle_mod.mix_logit_entry(ninf, ninf, 0.0) == ninf
+    assert oracle_mod.mix_logit_entry(2.0, 4.0, 0.25) == 2.5
+    # softmax of the mixed row: masked entries get probability 0, the rest the
+    # closed form (lambda = 1/2: mixed entries [0, ln 3] -> weights [1, 3])
+    zt = np.array([0.0, ninf, 2.0 * np.log(3.0), 0.0])
+    zq = np.array([0.0, 5.0, 0.0, ninf])
+    p = oracle_mod.mix_logit(zt, zq, 0.5)
+    np.testing.assert_allclose(p, [0.25, 0.0, 0.75, 0.0], rtol=0, atol=1e-15)
+    p0 = oracle_mod.mix_logit(zt, zq, 0.0)  # lambda = 0: the target softmax
+    np.testing.assert_allclose(p0, oracle_mod.softmax(zt), rtol=0, atol=1e-15)
+    p1 = oracle_mod.mix_logit(zt, zq, 1.0)  # lambda = 1: the draft softmax
+    np.testing.assert_allclose(p1, oracle_mod.softmax(zq), rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+def test_draft_token_masked_in_the_draft_row(oracle_mod, mode):
+    """q(x) = 0: the ratio is +inf, so x is accepted whenever p~(x) > 0, and
+    rejected when p~(x) = 0 too (then the residual is drawn)."""
+    ninf = np.float32(-np.inf)
+    zt = np.array([[[0.0, 2.0, 1.0], [0.0, 0.0, 0.0]]], np.float32)
+    zq = np.array([[[1.0, ninf, 0.0]]], np.float32)
+    tok = np.array([[1]], np.int32)
+    ua = np.array([[0.999]], np.float32)
+    ur = np.array([0.5], np.float32)
+    # lambda = 0.3: p~(1) > 0 in probability mode (0.7 p_t(1)); in logit mode
+    # the mixed entry is -inf (the draft's mask has weight 0.3), so p~(1) = 0
+    res = oracle_mod.verify(zt, zq, tok, ua, ur, np.array([0.3], np.float32), mode=mode)
+    if mode == 0:
+        assert res.n_accepted.tolist() == [1] and res.ratio[0, 0] == np.inf
+    else:
+        assert res.n_accepted.tolist() == [0] and res.ratio[0, 0] == 0.0
+        # residual max(0, p~ - q): p~ = softmax([0.3, -inf, 0.7]) puts 0.599 on
+        # entry 2, q = softmax([1, -inf, 0]) puts 0.269 there (and more than p~
+        # on entry 0), so the residual lives on entry 2 alone
+        assert res.tokens.tolist() == [[2, -1]]
+    # lambda = 0 in logit mode: the draft's mask has weight 0, p~ = p_t, accept
+    res = oracle_mod.verify(zt, zq, tok, ua, ur, np.array([0.0], np.float32), mode=mode)
+    assert res.n_accepted.tolist() == [1]
+    # lambda = 1 in probability mode: p~ = q, p~(1) = 0: reject
+    res = oracle_mod.verify(zt, zq, tok, ua, ur, np.array([1.0], np.float32), mode=mode)
+    assert res.n_accepted.tolist() == [0]
