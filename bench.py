@@ -10,9 +10,16 @@ B*K per step; the roofline line reports the achieved HBM bandwidth of the
 verify kernel with the algorithmic bytes (2K+1)*B*V*sizeof(dtype) per launch.
 The inputs (2.2 GB) are larger than L2, so no flush is needed between steps.
 
-Under torchrun (N > 1) every rank runs the same per-GPU batch on its own GPU
-(weak scaling, no collective in the data path); the reported value is the
-sum of all ranks' rows over the slowest rank's time.
+Under torchrun (N > 1) one global batch of N x B sequences is split by rank
+into contiguous shards of B sequences (the library's specv_shard_bounds), each
+verified on its rank's GPU with no collective in the data path (weak scaling:
+the per-GPU batch is fixed); after the timed region the shards' outputs are
+gathered in order into the global batch's.  The reported value is all ranks'
+rows over the slowest rank's time.
+
+The line also carries `per_config`: the other workloads (B=1 Llama-shaped,
+B=32 Qwen-shaped, the 10^6-sequence exactness workload) and the batched
+workload reading every row, each timed the same way.
 """
 from __future__ import annotations
 
@@ -40,8 +47,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_specv_gb300", "csrc", f)
                   for f in ("specv_rows.cu", "specv_device.cuh", "specv_block.cuh",
-                            "specv_segments.cuh", "specv_stream.cuh", "specv_ring.cuh",
-                            "specv_internal.h")]
+                            "specv_segments.cuh", "specv_stream.cuh", "specv_internal.h")]
 
 
 def parse():
@@ -57,9 +63,14 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every step from the host instead of replaying a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-api", default="early-exit", choices=["early-exit", "chunked"],
+                    help="host-buffer call of the e2e leg: specv_verify_host_early_exit (copies "
+                         "the rows the step reaches) or specv_verify_host (copies every row)")
     ap.add_argument("--e2e-chunks", type=int, default=0,
                     help="chunks of the host-buffer call (0 = the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config block (the other workloads, timed the same way)")
     ap.add_argument("--tree", default=None, metavar="SHAPE",
                     help="time specv_verify_tree on a draft tree of this shape (chain, kary:k, "
                          "star, random:f) with --tree-nodes nodes besides the root")
@@ -90,6 +101,34 @@ def max_over_ranks(x, ws, device):
     return float(t.item())
 
 
+def global_batch_slice(w, n_shards, lo, hi, device):
+    """Sequences [lo, hi) of the global batch of n_shards * w.B sequences: the
+    concatenation of n_shards seeded batches of workload w (sub-batch j drawn
+    with seed offset j), so that any contiguous shard is reproducible on its
+    own rank."""
+    B = w.B
+    parts = []
+    for j in range(lo // B, max(lo // B + 1, (hi + B - 1) // B)):
+        x = workloads.make_inputs(w, device, seed_offset=j)
+        a, b = max(lo - j * B, 0), max(min(hi - j * B, B), 0)
+        parts.append({k: v[a:b] for k, v in x.items()})
+    return {k: torch.cat([p[k] for p in parts]).contiguous() for k in parts[0]}
+
+
+def gather_shards(tokens, n_accepted, ws):
+    """Every rank's output rows, concatenated in rank order (the shards are
+    contiguous and in order, so this is the global batch's output)."""
+    import numpy as np
+    t = tokens.cpu().numpy() if hasattr(tokens, "cpu") else np.asarray(tokens)
+    n = n_accepted.cpu().numpy() if hasattr(n_accepted, "cpu") else np.asarray(n_accepted)
+    if ws == 1:
+        return t, n
+    import torch.distributed as dist
+    objs = [None] * ws
+    dist.all_gather_object(objs, (t, n))
+    return np.concatenate([o[0] for o in objs]), np.concatenate([o[1] for o in objs])
+
+
 def job_throughput(rows_per_step, steps, ws, slowest_ms):
     """Whole-job rows/s: every rank verifies rows_per_step rows per step (weak
     scaling), all ranks' rows over the slowest rank's time."""
@@ -97,9 +136,8 @@ def job_throughput(rows_per_step, steps, ws, slowest_ms):
 
 
 # kernel function timed for the roofline, by the planner's kernel name
-PLAN_KERNEL_FUNCTION = {"tile": "tile_kernel", "rows-stream": "rows_kernel", "rows-ring": "rows_kernel",
-                        "rows-resident": "resident_kernel", "tile-tma": "tile_tma_kernel",
-                        "rows-spec": "resident_kernel", "rows-sweep": "sweep_kernel"}
+PLAN_KERNEL_FUNCTION = {"tile": "tile_kernel", "rows-stream": "rows_kernel",
+                        "rows-resident": "resident_kernel", "tile-tma": "tile_tma_kernel"}
 
 
 def measured_peak():
@@ -293,6 +331,84 @@ def cpu_baseline(w, mode, target_seconds, host_inputs=None):
                       f"{w.dtype}); {el:.1f} s wall on {min(threads, B)} host threads"}
 
 
+def launches_per_step(plan):
+    """Kernel launches of one specv_verify call under this plan."""
+    return 2 if plan.get("split_draws") else 1
+
+
+def time_verify(specv, w, mode, dev, steps, warmup, l2_bytes):
+    """Mean device time (ms) of one specv_verify call on workload w: a CUDA
+    graph of the call replayed between CUDA events on its stream, the L2
+    flushed before every step when the inputs are smaller than twice the L2.
+    Returns (ms, mean n_accepted, outputs)."""
+    x = workloads.make_inputs(w, dev)
+    out_tok = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((w.B,), dtype=torch.int32, device=dev)
+    args = (x["target_logits"], x["draft_logits"], x["draft_tokens"], x["u_accept"],
+            x["u_resample"], x["lam"])
+    graph = capture_graph(lambda: specv.verify(*args, mode=mode, out_tokens=out_tok,
+                                               out_n_accepted=out_n,
+                                               stream=torch.cuda.current_stream(dev)), dev)
+    flush = L2Flush(dev, l2_bytes) if w.roofline_bytes < 2 * l2_bytes else None
+    stream = torch.cuda.current_stream(dev)
+    for i in range(max(3, warmup)):
+        if flush is not None:
+            flush(i)
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush(i)
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return ms, float(out_n.float().mean().item()), (out_tok, out_n), flush is not None
+
+
+# the per_config block: (workload, mode, environment, steps)
+PER_CONFIG = [(2, "prob", {}, 400), (3, "prob", {}, 400), (5, "prob", {}, 200),
+              (4, "prob", {"SPECV_EARLY_EXIT": "0"}, 100)]
+
+
+def run_per_config(specv, dev, args, l2_bytes):
+    """The other workloads (and the batched one reading every row), each timed
+    like the headline step, with its rows/s and HBM fraction."""
+    peak, _ = measured_peak()
+    out = []
+    for cfg, mname, env, steps in PER_CONFIG:
+        w = workloads.WORKLOADS[cfg]
+        mode = MODES[mname]
+        old = {k: os.environ.get(k) for k in env}
+        os.environ.update(env)
+        try:
+            plan = specv.plan(w.B, w.K, w.V, 1 if w.dtype == "bf16" else 0, mode)
+            ms, mean_n, (_, n), flushed = time_verify(specv, w, mode, dev, steps, args.warmup,
+                                                      l2_bytes)
+        finally:
+            for k, v in old.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        alg = (needed_bytes(n, w.K, w.V, w.elem_bytes) if plan.get("early_exit")
+               else w.roofline_bytes)
+        gbs = alg / (ms / 1e3) / 1e9
+        out.append({"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "logits": w.dtype,
+                    "mode": mname, "env": env, "us_per_step": ms * 1e3,
+                    "rows_per_s": w.B * w.K / (ms / 1e3), "algorithmic_bytes": alg,
+                    "hbm_gbs": gbs, "frac": gbs / peak, "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+                    "every_row_frac": w.roofline_bytes / (ms / 1e3) / 1e9 / peak,
+                    "mean_accepted": mean_n, "plan": plan, "steps": steps,
+                    "gpu_launches": steps * launches_per_step(plan),
+                    "l2": "flushed before every step" if flushed else "inputs > L2"})
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -475,7 +591,10 @@ def main():
     if args.B:
         w = w.scaled(B=args.B, name=f"{w.name}-B{args.B}")
     mode = MODES[args.mode]
-    x = workloads.make_inputs(w, dev, seed_offset=rank)
+    # this rank's shard of one global batch of ws x B sequences
+    B_global = ws * w.B
+    shard_lo, shard_hi = specv.shard_bounds(B_global, ws, rank)
+    x = global_batch_slice(w, ws, shard_lo, shard_hi, dev)
     stream = torch.cuda.current_stream(dev)
     out_tok = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
     out_n = torch.empty((w.B,), dtype=torch.int32, device=dev)
@@ -537,6 +656,7 @@ def main():
         t_end.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
+    clk_summary = clk.summary()
     total_ms = t_start.elapsed_time(t_end)
     per_call_ms = [a.elapsed_time(b) for a, b in ev]
     if flush_buf is not None:  # the timed region holds the flushes: count the steps only
@@ -544,7 +664,9 @@ def main():
     total_ms = max_over_ranks(total_ms, ws, dev)
     rows_per_step = w.B * w.K
     value = job_throughput(rows_per_step, K, ws, total_ms)
-    mean_accepted = float(out_n.float().mean().item())
+    # the shards' outputs, concatenated in order: the global batch's outputs
+    _, n_global = gather_shards(out_tok, out_n, ws)
+    mean_accepted = float(n_global.astype("float64").mean())
 
     # end to end: pinned host inputs -> device, verify, result -> host, every step
     e2e = None
@@ -558,13 +680,23 @@ def main():
         d2h = host_tok.numel() * 4 + host_n.numel() * 4
         del x  # the device copies of the inputs: the host call stages its own
 
+        link = {}
+
         def e2e_step():
-            # one C-ABI call on host buffers: chunked host->device copies that
-            # overlap the verify launches, then the results back to the host
-            specv.verify_host(host["target_logits"], host["draft_logits"], host["draft_tokens"],
-                              host["u_accept"], host["u_resample"], host["lam"], mode=mode,
-                              out_tokens=host_tok, out_n_accepted=host_n,
-                              chunks=args.e2e_chunks, stream=stream)
+            # one C-ABI call on host buffers, then the results back to the host
+            if args.e2e_api == "early-exit":
+                # position by position, only the rows the verify step reaches
+                _, _, link["h2d"], link["d2h"] = specv.verify_host_early_exit(
+                    host["target_logits"], host["draft_logits"], host["draft_tokens"],
+                    host["u_accept"], host["u_resample"], host["lam"], mode=mode,
+                    out_tokens=host_tok, out_n_accepted=host_n, stream=stream)
+            else:
+                # every row, in chunks whose copies overlap the verify launches
+                specv.verify_host(host["target_logits"], host["draft_logits"],
+                                  host["draft_tokens"], host["u_accept"], host["u_resample"],
+                                  host["lam"], mode=mode, out_tokens=host_tok,
+                                  out_n_accepted=host_n, chunks=args.e2e_chunks, stream=stream)
+                link["h2d"], link["d2h"] = h2d, d2h
         for _ in range(max(3, args.warmup)):
             e2e_step()
         torch.cuda.synchronize(dev)
@@ -581,10 +713,13 @@ def main():
         barrier()
         e_ms = max_over_ranks(a.elapsed_time(b), ws, dev)
         e2e = {"value": job_throughput(rows_per_step, e_steps, ws, e_ms), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
-               "ms_per_step": e_ms / e_steps,
-               "api": "specv_verify_host (pinned host buffers, chunks="
-                      f"{args.e2e_chunks or 'auto'})"}
+               "h2d_bytes_per_step": link["h2d"], "d2h_bytes_per_step": link["d2h"],
+               "every_row_h2d_bytes": h2d, "steps": e_steps, "ms_per_step": e_ms / e_steps,
+               "api": ("specv_verify_host_early_exit (pinned host buffers; rows copied "
+                       "position by position up to each sequence's first rejection)"
+                       if args.e2e_api == "early-exit" else
+                       "specv_verify_host (pinned host buffers, chunks="
+                       f"{args.e2e_chunks or 'auto'})")}
         del host
 
     if rank != 0:
@@ -609,7 +744,7 @@ def main():
                 else "fallback 6.8 TB/s",
                 "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                 "kernel": ("rows_greedy_kernel" if args.mode == "greedy" and
-                           plan["kernel"] in ("rows-stream", "rows-ring") else
+                           plan["kernel"] == "rows-stream" else
                            PLAN_KERNEL_FUNCTION.get(plan["kernel"], plan["kernel"])),
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "algorithmic_bytes": ("rows up to the first rejection (early exit): "
@@ -622,10 +757,24 @@ def main():
                 "timing": ("CUDA events around each replay of a CUDA graph holding one "
                            "specv_verify call" if graph is not None else
                            "CUDA events around each specv_verify call") +
-                          " on its stream (the verify launches only)"}
+                          " on its stream (the verify launches only)",
+                # the roofline as the task states it: every logit read once,
+                # (2K+1) B V s per launch, whatever the kernel skips
+                "every_row_read_once": {
+                    "bytes_per_launch": all_rows,
+                    "gbs": all_rows / (kern_ms / 1e3) / 1e9,
+                    "frac_of_measured": all_rows / (kern_ms / 1e3) / 1e9 / peak,
+                    "frac_of_nominal_8tbs": all_rows / (kern_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                    "note": ("with early exit the kernel reads only the rows the outputs depend "
+                             "on, so this rate can exceed the copy peak; `frac` above is the "
+                             "bandwidth over those rows" if plan.get("early_exit") else
+                             "equal to `frac`: every row is read")}}
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
         cpu = cpu_baseline(w, mode, args.cpu_seconds)
+    per_config = None
+    if not args.no_per_config and ws == 1 and args.B is None:
+        per_config = run_per_config(specv, dev, args, l2_bytes)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
@@ -637,10 +786,14 @@ def main():
                    "l2": "L2 flushed before every timed step (2x-L2 write, then a 2x-L2 "
                          "read, outside the step events)" if flush_buf is not None else
                          "inputs larger than L2 (no flush)",
-                   "parallelism": f"replicas x{ws} (batch per GPU fixed)"},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
-        "gpu_launches": K, "mean_accepted": mean_accepted,
+                   "global_batch": B_global,
+                   "parallelism": (f"one global batch of {B_global} sequences split into {ws} "
+                                   f"contiguous shards of {w.B}, one per GPU" if ws > 1 else
+                                   "1 GPU")},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk_summary,
+        "gpu_launches": K * launches_per_step(plan), "mean_accepted": mean_accepted,
         "hbm_gbs_step": alg_bytes * ws / (total_ms / K / 1e3) / 1e9,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:

@@ -149,6 +149,83 @@ specv_status specv_verify_host(const void *target_logits, const void *draft_logi
                                int32_t *out_n_accepted, int32_t chunks, void *stream);
 
 /*
+ * specv_verify_host_early_exit -- specv_verify_host that copies only the rows
+ * the verify step reaches.  The pages' loop stops at the first rejection
+ * (RAPID explainer, "3) 候选验证机制（伪代码）"; SD explainer, "修改的拒绝采样":
+ * the rest of the draft is discarded), so a sequence's rows after its first
+ * rejected position never influence its outputs.  The call copies the batch
+ * position by position: level i sends row pair (b, i) (level K: target row
+ * K) of every sequence still live over the host link, decides position i of
+ * those sequences on the device, reads the B live flags back (one small copy
+ * and a wait on `stream` per level), and stops copying a sequence once a
+ * position clearly rejects (a margin of 1e-4 relative keeps every row the
+ * verify step could read under other rounding).  The ordinary verify step then
+ * runs on the staged batch.
+ *
+ *   Arguments, layouts and results as specv_verify_host (HOST pointers; the
+ *   outputs equal specv_verify's with a one-chunk plan), without `chunks`;
+ *   out_h2d_bytes and out_d2h_bytes (each may be NULL) receive the bytes
+ *   copied to the device and read back (the outputs and the live flags).
+ *
+ * Blocking: the call returns once every row it sends has been copied (it
+ * waits on `stream` after each level); the final verify step and the two
+ * output copies are still in flight on `stream` at return.  Staging memory is
+ * shared with specv_verify_host (per device and stream).  Errors as
+ * specv_verify_host (SPECV_ERR_UNSUPPORTED under stream capture).
+ */
+specv_status specv_verify_host_early_exit(const void *target_logits, const void *draft_logits,
+                                          const int32_t *draft_tokens, const float *u_accept,
+                                          const float *u_resample, const float *lambda,
+                                          int64_t B, int32_t K, int32_t V, specv_dtype dtype,
+                                          specv_mode mode, int32_t *out_tokens,
+                                          int32_t *out_n_accepted, int64_t *out_h2d_bytes,
+                                          int64_t *out_d2h_bytes, void *stream);
+
+/*
+ * specv_shard_bounds -- the sequences [*lo, *hi) of shard `shard` when a batch
+ * of B sequences is split over n_shards (1..64) shards for
+ * specv_verify_sharded_host: contiguous runs in order, lo = shard * (B /
+ * n_shards) + min(shard, B mod n_shards), sizes differing by at most one (a
+ * shard is empty when B < n_shards).  Sequences are independent (SD
+ * explainer, "批量投机（Batched Speculation）": each sequence of a batch is
+ * verified on its own), so the shards' outputs concatenate to the batch's.
+ * Host-only arithmetic.  SPECV_ERR_INVALID_ARG for a NULL output, B < 0 or a
+ * shard index outside [0, n_shards).
+ */
+specv_status specv_shard_bounds(int64_t B, int32_t n_shards, int32_t shard, int64_t *lo,
+                                int64_t *hi);
+
+/*
+ * specv_verify_sharded_host -- one batch in host memory verified on several
+ * devices: shard g (specv_shard_bounds) runs specv_verify_host on device
+ * devices[g] (a device may appear more than once: its shards then run on
+ * separate streams of that device), and its out_tokens / out_n_accepted rows
+ * land at the shard's offset in the caller's host arrays.  Arguments and
+ * layouts as specv_verify_host, all arrays HOST pointers (page-locked memory
+ * lets the shards' copies run at the same time); devices [n_shards], n_shards
+ * in 1..64.  No data crosses devices: no collective, no peer memory.
+ *
+ * Unlike specv_verify_host the call is synchronous: it returns after every
+ * shard has completed, the outputs in place.  It uses streams and staging
+ * memory the library owns per (device, shard index), and leaves the calling
+ * thread's current device unchanged.  Each sequence's outputs equal those of
+ * specv_verify_host on the whole batch whenever the launch plan is the same
+ * (it depends on a shard's size); otherwise decisions can differ only within
+ * rounding of a decision or CDF boundary (greedy verification not at all
+ * outside its tie band).
+ *
+ * Errors: SPECV_ERR_INVALID_ARG as specv_verify_host, for a NULL `devices`,
+ * n_shards outside 1..64, or a device index that does not exist; the first
+ * shard's error otherwise (shards already launched are waited for).
+ */
+specv_status specv_verify_sharded_host(const void *target_logits, const void *draft_logits,
+                                       const int32_t *draft_tokens, const float *u_accept,
+                                       const float *u_resample, const float *lambda, int64_t B,
+                                       int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,
+                                       int32_t *out_tokens, int32_t *out_n_accepted,
+                                       int32_t n_shards, const int32_t *devices);
+
+/*
  * specv_verify_debug -- specv_verify plus the intermediate probabilities, for
  * tests.  Same kernels and the same arithmetic as specv_verify; the extra
  * outputs (device pointers, each may be NULL) are:
@@ -178,19 +255,10 @@ specv_status specv_verify_debug(const void *target_logits, const void *draft_log
  *            memory by TMA; chosen when rows start on 16-byte boundaries and
  *            a slice fits shared memory, and the grid is a single wave),
  *            3 = small-vocabulary tile kernel with TMA-staged, double-buffered
- *            tiles (16-byte aligned rows),
- *            4 = resident cluster row kernel that samples the rejected row
- *            speculatively in place (only when the environment variable
- *            SPECV_ROWS_VARIANT=spec asks for it; =stream and =resident force
- *            kernels 1 and 2, and SPECV_CLUSTER_SIZE=1..16
- *            forces the cluster size of the row kernels),
- *            5 = sweep row kernel: persistent CTAs stream fixed-size chunks of
- *            the rows through shared memory by bulk copies (only when
- *            SPECV_ROWS_VARIANT=sweep asks for it; rows on 16-byte boundaries),
- *            6 = streaming cluster row kernel fed by a three-stage ring of
- *            shared-memory chunks filled by bulk copies instead of register
- *            loads (only when SPECV_ROWS_RING=1 asks for it; rows on 16-byte
- *            boundaries)
+ *            tiles (16-byte aligned rows).
+ *            For tests, the environment variable SPECV_ROWS_VARIANT=stream or
+ *            =resident forces kernel 1 or 2, and SPECV_CLUSTER_SIZE=1..16
+ *            forces the cluster size of the row kernels.
  *   cluster: CTAs per thread-block cluster splitting each row (1 for kernel 0)
  *   ctas:    CTAs launched by a row kernel; tiles of sequences for kernels 0, 3
  *   workspace_bytes: scratch bytes of the row kernels' workspace (kept per
@@ -212,7 +280,8 @@ specv_status specv_plan(int64_t B, int32_t K, int32_t V, specv_dtype dtype, spec
  *       explainer, "修改的拒绝采样").  Taken on grids of more than two waves of
  *       CTAs; the environment variable SPECV_EARLY_EXIT=0 turns it off.  The
  *       outputs do not depend on it.
- *   SPECV_PLAN_SPLIT_DRAWS -- the token draws run as a second launch.
+ *   SPECV_PLAN_SPLIT_DRAWS -- the token draws run as a second launch
+ *       (grids of one or two waves; SPECV_SAMPLE_SPLIT=0/1 forces either way).
  * Returns SPECV_ERR_INVALID_ARG for sizes specv_verify would reject.
  */
 #define SPECV_PLAN_EARLY_EXIT 1u
@@ -336,6 +405,18 @@ specv_status specv_verify_noalloc(const void *target_logits, const void *draft_l
 
 /* Human-readable name of a status. Never NULL. */
 const char *specv_status_string(specv_status status);
+
+/*
+ * specv_release_stream -- frees what the library keeps for (current device,
+ * stream): the row kernels' scratch (including buffers it outgrew) and the
+ * host-buffer calls' staging memory, copy stream and events.  It waits for
+ * the stream's queued work first.  Call it before destroying a stream on
+ * which the library ran, once no CUDA graph captured from library calls on
+ * that stream will be replayed (a graph refers to the scratch by address).
+ * The next call on the stream allocates afresh.  SPECV_ERR_UNSUPPORTED while
+ * the stream is being captured; SPECV_ERR_CUDA if waiting fails.
+ */
+specv_status specv_release_stream(void *stream);
 
 /* Text of the CUDA error behind the most recent SPECV_ERR_CUDA on this
  * thread ("" if none).  Never NULL. */

@@ -99,6 +99,15 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.specv_verify_tree.argtypes = [vp] * 8 + [i64, i32, i32, i32, ctypes.c_int,
                                                      ctypes.c_int, vp, vp, vp, vp]
         lib.specv_verify_tree.restype = ctypes.c_int
+        lib.specv_verify_host_early_exit.argtypes = common + [ctypes.POINTER(i64),
+                                                              ctypes.POINTER(i64), vp]
+        lib.specv_verify_host_early_exit.restype = ctypes.c_int
+        lib.specv_release_stream.argtypes = [vp]
+        lib.specv_release_stream.restype = ctypes.c_int
+        lib.specv_shard_bounds.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        lib.specv_shard_bounds.restype = ctypes.c_int
+        lib.specv_verify_sharded_host.argtypes = common + [i32, vp]
+        lib.specv_verify_sharded_host.restype = ctypes.c_int
         dbl = ctypes.c_double
         lib.specv_choose_k.argtypes = [dbl, dbl, dbl, dbl, i32, i32]
         lib.specv_choose_k.restype = ctypes.c_int32
@@ -220,6 +229,64 @@ def verify_host(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
         _dtype_code(target_logits), int(mode), out_tokens.data_ptr(), out_n.data_ptr(),
         int(chunks), _stream_ptr(stream, dev))
     _check(st, "specv_verify_host")
+    return out_tokens, out_n
+
+
+def verify_host_early_exit(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam,
+                           mode: int = PROB_MIX, out_tokens=None, out_n_accepted=None,
+                           stream=None):
+    """verify_host() that copies only the rows the verify step reaches, position
+    by position (a small read-back of the live sequences per position).  Returns
+    (out_tokens, out_n, h2d_bytes, d2h_bytes): the outputs are complete once
+    ``stream`` has completed; the byte counts are what crossed the host link."""
+    B, K, V, _, out_tokens, out_n = _args(target_logits, draft_logits, draft_tokens, u_accept,
+                                          u_resample, lam, mode, out_tokens, out_n_accepted,
+                                          host=True)
+    dev = stream.device if stream is not None else torch.device("cuda",
+                                                                torch.cuda.current_device())
+    h2d, d2h = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = load().specv_verify_host_early_exit(
+        target_logits.data_ptr(), draft_logits.data_ptr(), draft_tokens.data_ptr(),
+        u_accept.data_ptr(), u_resample.data_ptr(), lam.data_ptr(), B, K, V,
+        _dtype_code(target_logits), int(mode), out_tokens.data_ptr(), out_n.data_ptr(),
+        ctypes.byref(h2d), ctypes.byref(d2h), _stream_ptr(stream, dev))
+    _check(st, "specv_verify_host_early_exit")
+    return out_tokens, out_n, h2d.value, d2h.value
+
+
+def release_stream(stream=None):
+    """Free the scratch and staging the library keeps for ``stream`` (default:
+    the current stream) on the current device, after the stream's queued work;
+    only once no CUDA graph captured from library calls on it will be replayed."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _check(load().specv_release_stream(_stream_ptr(stream, dev)), "specv_release_stream")
+
+
+def shard_bounds(B: int, n_shards: int, shard: int) -> tuple[int, int]:
+    """Sequences [lo, hi) of shard `shard` of a batch of B split over n_shards
+    (the library's split: contiguous, in order, sizes within one)."""
+    lo, hi = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(load().specv_shard_bounds(int(B), int(n_shards), int(shard), ctypes.byref(lo),
+                                     ctypes.byref(hi)), "specv_shard_bounds")
+    return lo.value, hi.value
+
+
+def verify_sharded(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam,
+                   devices, mode: int = PROB_MIX, out_tokens=None, out_n_accepted=None):
+    """One batch in host memory verified on several devices: shard g of
+    len(devices) (shard_bounds) runs on CUDA device devices[g], and its outputs
+    land at its offset in out_tokens / out_n_accepted (host tensors, page-locked
+    ones allocated if not given).  Synchronous: returns the outputs complete."""
+    B, K, V, _, out_tokens, out_n = _args(target_logits, draft_logits, draft_tokens, u_accept,
+                                          u_resample, lam, mode, out_tokens, out_n_accepted,
+                                          host=True)
+    devs = (ctypes.c_int32 * len(devices))(*[int(d) for d in devices])
+    st = load().specv_verify_sharded_host(
+        target_logits.data_ptr(), draft_logits.data_ptr(), draft_tokens.data_ptr(),
+        u_accept.data_ptr(), u_resample.data_ptr(), lam.data_ptr(), B, K, V,
+        _dtype_code(target_logits), int(mode), out_tokens.data_ptr(), out_n.data_ptr(),
+        len(devices), devs)
+    _check(st, "specv_verify_sharded_host")
     return out_tokens, out_n
 
 
@@ -349,8 +416,7 @@ class AdaptiveK:
 
 
 # specv_plan's kernel codes
-KERNEL_NAMES = {0: "tile", 1: "rows-stream", 2: "rows-resident", 3: "tile-tma", 4: "rows-spec",
-                5: "rows-sweep", 6: "rows-ring"}
+KERNEL_NAMES = {0: "tile", 1: "rows-stream", 2: "rows-resident", 3: "tile-tma"}
 
 
 def plan(B: int, K: int, V: int, dtype: int = F32, mode: int = PROB_MIX) -> dict:

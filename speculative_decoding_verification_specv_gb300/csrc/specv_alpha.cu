@@ -43,7 +43,7 @@ struct __align__(16) AlphaShared {
 // p~_v and q_v of one entry from the row statistics.
 template <int MODE>
 __device__ __forceinline__ float overlap_term(float zt, float zq, float lam, const SampleParams &sp) {
-  const float a = MODE == kLogitMix ? (zq == -INFINITY ? -INFINITY : mix_logit(zt, zq, lam)) : zt;
+  const float a = MODE == kLogitMix ? mix_logit(zt, zq, lam) : zt;
   const float pa = prob_from_offset(a, sp.nA);
   const float pq = prob_from_offset(zq, sp.nB);
   const float pt = MODE == kProbMix ? __fmaf_rn(lam, pq, __fmul_rn(__fsub_rn(1.0f, lam), pa)) : pa;

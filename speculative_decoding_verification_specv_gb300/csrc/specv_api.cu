@@ -14,6 +14,17 @@
 #include "specv_internal.h"
 
 namespace {
+thread_local char g_last_cuda_error[256] = "";
+}  // namespace
+
+namespace specv {
+void note_cuda_error(cudaError_t e) {
+  std::strncpy(g_last_cuda_error, cudaGetErrorString(e), sizeof(g_last_cuda_error) - 1);
+  g_last_cuda_error[sizeof(g_last_cuda_error) - 1] = '\0';
+}
+}  // namespace specv
+
+namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultSMs = 152;        // used by specv_plan when no device is visible
@@ -35,9 +46,7 @@ constexpr int32_t kMaxK = 4096;
 // that three CTAs fit an SM.
 constexpr int kResidentMaxSmem = 200 * 1024;
 constexpr int kResidentTarget = 96 * 1024;
-// Sweep row kernel: CTAs per SM of its persistent grid (its launch bounds and
-// at most 96 KiB of stages per CTA let two fit).
-constexpr int kSweepBlocksPerSM = 2;
+
 
 struct DeviceState {
   bool ready = false;
@@ -56,8 +65,11 @@ DeviceState g_dev[kMaxDevices];
 // position statistics or records, which needs no clearing.  Counters sit in a
 // region of their own, so calls of any shape and kernel on one stream can
 // share it.  A call therefore needs no allocation and no clearing step.
-// Buffers are never freed while the process runs: a CUDA graph captured on a
-// stream may hold the pointers.
+// A CUDA graph captured on a stream may hold the pointers, so a grown part's
+// old buffer is not freed at once: it joins the entry's superseded list.
+// Sizes double on growth, so the superseded buffers of an entry add up to
+// less than its current ones.  specv_release_stream frees an entry (current
+// and superseded buffers) when its owner says no graph will use them again.
 struct Workspace {
   int dev;
   cudaStream_t stream;
@@ -65,6 +77,7 @@ struct Workspace {
   int64_t count_len;
   void *data;
   size_t data_bytes;
+  std::vector<void *> superseded;
 };
 std::vector<Workspace> g_ws;
 constexpr size_t kWsMinBytes = 64 * 1024;
@@ -96,10 +109,10 @@ bool cached_workspace(int dev, cudaStream_t stream, int64_t B, size_t data_bytes
   }
   if (cap != cudaStreamCaptureStatusNone) return false;  // no allocation while capturing
   if (w == nullptr) {
-    g_ws.push_back(Workspace{dev, stream, nullptr, 0, nullptr, 0});
+    g_ws.push_back(Workspace{dev, stream, nullptr, 0, nullptr, 0, {}});
     w = &g_ws.back();
   }
-  // grow a part by replacing it (the old part stays allocated: a graph may use it)
+  // grow a part by replacing it (the old part is kept: a graph may use it)
   if (w->count_len < B) {
     const size_t sz = grow_to((size_t)B * sizeof(unsigned));
     void *ptr = nullptr;
@@ -112,6 +125,7 @@ bool cached_workspace(int dev, cudaStream_t stream, int64_t B, size_t data_bytes
       (void)cudaFree(ptr);
       return false;
     }
+    if (w->count != nullptr) w->superseded.push_back(w->count);
     w->count = static_cast<unsigned *>(ptr);
     w->count_len = (int64_t)(sz / sizeof(unsigned));
   }
@@ -122,6 +136,7 @@ bool cached_workspace(int dev, cudaStream_t stream, int64_t B, size_t data_bytes
       (void)cudaGetLastError();
       return false;
     }
+    if (w->data != nullptr) w->superseded.push_back(w->data);
     w->data = ptr;
     w->data_bytes = sz;
   }
@@ -130,12 +145,7 @@ bool cached_workspace(int dev, cudaStream_t stream, int64_t B, size_t data_bytes
   return true;
 }
 
-thread_local char g_last_cuda_error[256] = "";
-
-void note_cuda_error(cudaError_t e) {
-  std::strncpy(g_last_cuda_error, cudaGetErrorString(e), sizeof(g_last_cuda_error) - 1);
-  g_last_cuda_error[sizeof(g_last_cuda_error) - 1] = '\0';
-}
+using specv::note_cuda_error;
 
 // One-time per-device set-up: opt the kernels into 16-CTA clusters and the
 // tile kernel into its shared-memory size; read the SM count.
@@ -163,8 +173,8 @@ specv_status ensure_device(int *sms_out, int64_t *l2_out) {
         (e = specv::resident_prepare(kResidentMaxSmem)) != cudaSuccess ||
         (e = specv::tile_prepare(kTileSmemBudget)) != cudaSuccess ||
         (e = specv::tile_tma_prepare(2 * kTmaTileStageBytes + 16 * 1024)) != cudaSuccess ||
-        (e = specv::sweep_prepare(specv::sweep_smem_bytes(1024))) != cudaSuccess ||
         (e = specv::alpha_prepare()) != cudaSuccess ||
+        (e = specv::level_prepare()) != cudaSuccess ||
         (e = specv::tree_prepare()) != cudaSuccess) {
       note_cuda_error(e);
       return SPECV_ERR_CUDA;
@@ -179,9 +189,7 @@ specv_status ensure_device(int *sms_out, int64_t *l2_out) {
 }
 
 struct Plan {
-  int kernel;            // 0 tile, 1 streaming row kernel, 2 resident row kernel, 3 TMA tile,
-                         // 4 resident row kernel reading in place (speculative sampling),
-                         // 5 sweep kernel, 6 streaming row kernel fed by the bulk-copy ring
+  int kernel;            // 0 tile, 1 streaming row kernel, 2 resident row kernel, 3 TMA tile
   int cluster;           // CTAs per cluster (row kernels)
   int64_t ctas;          // CTAs of the row kernels (tile kernel: tiles)
   int64_t ws_bytes;      // scratch bytes
@@ -194,8 +202,6 @@ struct Plan {
   int sample_cluster;    // its cluster size
   int sample_gps, sample_seg_tiles, sample_segs;  // its slice and segment geometry
   int early_exit;        // streaming kernel: positions after a published rejection skip their rows
-  int chunk_groups, chunks;       // sweep kernel: groups per chunk, chunks per row
-  int sweep_smem;        // dynamic shared memory of the sweep kernel
   int64_t counters;      // arrival counters in the scratch
 };
 
@@ -236,41 +242,13 @@ int split_from_env() {
   return s[0] == '1' ? 1 : (s[0] == '0' ? 0 : -1);
 }
 
-// SPECV_TILE_STAGE_KB=8..40 sets the bytes of one staged tile of the TMA tile
-// kernel (tuning); 0: the default.
-int tile_stage_from_env() {
-  const char *s = std::getenv("SPECV_TILE_STAGE_KB");
-  if (!s || !*s) return 0;
-  const int v = std::atoi(s);
-  return (v >= 8 && v <= 40) ? v * 1024 : 0;
-}
-
-// SPECV_ROWS_RING=0/1 forces the streaming row kernel's register loads or its
-// bulk-copy ring (16-byte aligned rows); -1: the plan.
-int ring_from_env() {
-  const char *s = std::getenv("SPECV_ROWS_RING");
-  if (!s || !*s) return -1;
-  return s[0] == '1' ? 1 : (s[0] == '0' ? 0 : -1);
-}
-
-// Whether the streaming row kernel takes the bulk-copy ring instead of
-// register loads: only when SPECV_ROWS_RING=1 asks for it (rows on 16-byte
-// boundaries).  Measured on the Qwen-shaped batch (B = 32, K = 5, V = 152064
-// bf16, one wave of 576 CTAs), ring vs register loads: greedy 32.8 vs
-// 28.8 us, probability 46.9 vs 45.0 us, logit 60.3 vs 61.4 us; at the
-// batched workload (18 waves) both stream at the copy peak.  The ring's refill
-// of a stage waits for the slowest of the CTA's eight warps, and the folds
-// take two groups per thread per chunk instead of four.
-bool ring_choice(bool aligned) { return aligned && ring_from_env() == 1; }
-
-// "stream", "resident" or "spec" forces a row-kernel variant (tuning and tests).
+// "stream" or "resident" forces a row-kernel variant (tests of both kernels
+// on one shape).
 int variant_from_env() {
   const char *s = std::getenv("SPECV_ROWS_VARIANT");
   if (!s) return 0;
   if (std::strcmp(s, "stream") == 0) return 1;
   if (std::strcmp(s, "resident") == 0) return 2;
-  if (std::strcmp(s, "spec") == 0) return 4;
-  if (std::strcmp(s, "sweep") == 0) return 5;
   return 0;
 }
 
@@ -302,8 +280,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
       // two alternating tile buffers of about 28 KiB (40 KiB at most); one round of stage-A
       // row tasks (2K+1 per sequence) for the CTA's threads; at most one
       // stage-B lane group per sequence
-      const int env_stage = tile_stage_from_env();
-      ts = (int)((env_stage ? env_stage : kTmaTileTargetBytes) / data_bytes);
+      ts = (int)(kTmaTileTargetBytes / data_bytes);
       const int by_rows = specv::kTileThreads / (2 * K + 1);
       if (ts > by_rows && by_rows >= 1) ts = by_rows;
       if (ts > specv::kTmaTileMaxSeqs) ts = specv::kTmaTileMaxSeqs;
@@ -330,16 +307,15 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
   const int64_t G = (V + vw - 1) / vw;
   const int env_S = cluster_from_env();
   const int env_var = variant_from_env();
+  const int64_t waves_slots = 2 * 4LL * sms;  // two waves of 4 CTAs per SM
   if (greedy) {
     // greedy needs no sampling pass: the streaming row kernel, one read of every logit
-    if (env_var != 0 && env_var != 1) return SPECV_ERR_UNSUPPORTED;
+    if (env_var == 2) return SPECV_ERR_UNSUPPORTED;
     int S = env_S;
-    if (S == 0) {
-      S = specv::stream_cluster_size(P, row_bytes, G, sms);
-    }
+    if (S == 0) S = specv::stream_cluster_size(P, row_bytes, G, sms);
     while (S > 1 && P * S > INT32_MAX) S /= 2;
     if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
-    p->kernel = ring_choice(aligned && row_bytes % 16 == 0) ? 6 : 1;
+    p->kernel = 1;
     p->cluster = S;
     p->ctas = P * S;
     p->num_groups = (int)G;
@@ -347,36 +323,14 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     specv::rows_segments(p->groups_per_slice, &p->seg_tiles, &p->segs_per_slice);
     p->counters = B;
     p->ws_bytes = round16(P * 16) + round16(B * 4);
-    if (P * S > 2 * 4LL * sms && early_exit_from_env()) {  // early exit: one word per sequence
+    if (P * S > waves_slots && early_exit_from_env()) {  // early exit: one word per sequence
       p->early_exit = 1;
       p->counters = 2 * B;
       p->ws_bytes += round16(B * 4);
     }
     return SPECV_OK;
   }
-  if (env_var == 5) {
-    // sweep kernel: persistent CTAs, kSweepBlocksPerSM per SM; chunks of 1024
-    // groups (16 KiB of a row), halved down to 256 while there are fewer than
-    // two items per CTA
-    if (!aligned || row_bytes % 16 != 0) return SPECV_ERR_UNSUPPORTED;
-    const int64_t grid_max = (int64_t)sms * kSweepBlocksPerSM;
-    int cg = 1024;
-    while (cg > specv::kSweepThreads && P * ((G + cg - 1) / cg) < 2 * grid_max) cg /= 2;
-    const int64_t C = (G + cg - 1) / cg;
-    if (P * C > INT64_MAX / 16 || C > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
-    p->kernel = 5;
-    p->cluster = 1;
-    p->chunk_groups = cg;
-    p->chunks = (int)C;
-    p->num_groups = (int)G;
-    specv::segment_geometry(G, specv::kSweepSegGroups, &p->seg_tiles, &p->segs_per_slice);
-    p->sweep_smem = specv::sweep_smem_bytes(cg);
-    p->ctas = P * C < grid_max ? P * C : grid_max;
-    p->counters = P + B;
-    p->ws_bytes = round16(P * C * 16) + round16(P * 16) + round16(p->counters * 4);
-    return SPECV_OK;
-  }
-  const bool can_resident = aligned && (row_bytes % 16 == 0) && env_var != 1 && env_var != 4;
+  const bool can_resident = aligned && (row_bytes % 16 == 0) && env_var != 1;
   auto slice_smem = [&](int S) { return 2 * ((G + S - 1) / S) * 16; };
   int S = 0;
   int kernel = 1;
@@ -392,40 +346,26 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
       if (S == 0 && slice_smem(specv::kMaxCluster) <= kResidentMaxSmem) S = specv::kMaxCluster;
       if (S)
         while (S < specv::kMaxCluster && P * S < 4LL * sms && row_bytes / (2 * S) >= 4096) S *= 2;
-      if (S && env_var != 2 && P * S > 2LL * sms) S = 0;  // several waves: streaming is faster
     }
+    if (S && env_var != 2 && P * S > 2LL * sms) S = 0;  // several waves: streaming is faster
     if (S) kernel = 2;
   }
   if (kernel == 2 && P * S > INT32_MAX) kernel = 1;
   if (env_var == 2 && kernel != 2) return SPECV_ERR_UNSUPPORTED;
-  // in-place variant: every position decides and samples at once, re-reading
-  // its own slice while it is still in L2 -- when the whole working set fits L2
-  const int64_t work_bytes = (int64_t)(2 * K + 1) * B * row_bytes;
-  const bool inplace_ok = aligned && (row_bytes % 16 == 0) && env_var != 1 && env_var != 2;
-  // (measured slower than the streaming kernel at 107 MB / 1536 CTAs: the
-  // speculative samples of every rejecting position outweigh the shorter
-  // tail, so it runs only when asked for)
-  (void)work_bytes;
-  (void)l2;
-  if (kernel == 1 && inplace_ok && env_var == 4) kernel = 4;
-  if (env_var == 4 && kernel != 4) return SPECV_ERR_UNSUPPORTED;
-  if (kernel == 1 || kernel == 4) {
+  if (kernel == 1) {
     S = env_S;
-    if (S == 0) {
-      S = specv::stream_cluster_size(P, row_bytes, G, sms);
-    }
+    if (S == 0) S = specv::stream_cluster_size(P, row_bytes, G, sms);
     while (S > 1 && P * S > INT32_MAX) S /= 2;
     if (P * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
   }
-  if (kernel == 1 && ring_choice(aligned && row_bytes % 16 == 0)) kernel = 6;
   p->kernel = kernel;
   p->cluster = S;
   p->ctas = P * S;
   p->num_groups = (int)G;
   p->groups_per_slice = (int)((G + S - 1) / S);
   p->counters = B;
-  if (kernel == 2 || kernel == 4) {
-    p->res_smem = kernel == 2 ? (int)slice_smem(S) : 0;
+  if (kernel == 2) {
+    p->res_smem = (int)slice_smem(S);
     p->ws_bytes = round16(P * 8) + round16(B * 4);
   } else {
     // position statistics, then the bonus rows' segment statistics
@@ -437,7 +377,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     // (about 48 KiB of the row pair per CTA, mostly still in L2).  Several
     // waves keep the draws in the statistics launch, overlapped with streaming.
     const int env_split = split_from_env();
-    const bool one_wave = P * S <= 2 * 4LL * sms;
+    const bool one_wave = P * S <= waves_slots;
     p->split = env_split >= 0 ? env_split : (one_wave ? 1 : 0);
     if (p->split) {
       int64_t s2 = (2 * row_bytes + 48 * 1024 - 1) / (48 * 1024);
@@ -534,36 +474,7 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     wdata = static_cast<char *>(ws) + round16(p.counters * 4);
     e = cudaMemsetAsync(cnt, 0, (size_t)p.counters * sizeof(unsigned), stream);
   }
-  if (p.kernel == 5) {
-    const int64_t P = B * (K + 1);
-    specv::SweepArgs w;
-    w.target = target;
-    w.draft = draft;
-    w.tokens = tokens;
-    w.u_accept = ua;
-    w.u_resample = ur;
-    w.lam = lam;
-    w.B = B;
-    w.K = K;
-    w.V = V;
-    w.out_tokens = out_tokens;
-    w.out_n = out_n;
-    w.ws_chunk = static_cast<float4 *>(wdata);
-    w.ws_stats = reinterpret_cast<float4 *>(static_cast<char *>(wdata) +
-                                            round16(P * (int64_t)p.chunks * 16));
-    w.row_count = cnt;
-    w.seq_count = cnt + P;
-    w.dbg_ptilde = dbg_ptilde;
-    w.dbg_q = dbg_q;
-    w.dbg_lse = dbg_lse;
-    w.num_groups = p.num_groups;
-    w.chunk_groups = p.chunk_groups;
-    w.chunks = p.chunks;
-    w.seg_tiles = p.seg_tiles;
-    w.nseg = p.segs_per_slice;
-    w.items = P * (int64_t)p.chunks;
-    if (e == cudaSuccess) e = specv::sweep_launch(w, bf16, mode, p.ctas, p.sweep_smem, stream);
-  } else if (p.kernel == 2 || p.kernel == 4) {
+  if (p.kernel == 2) {
     specv::ResArgs r;
     r.target = target;
     r.draft = draft;
@@ -584,8 +495,7 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     r.groups_per_slice = p.groups_per_slice;
     r.num_groups = p.num_groups;
     if (e == cudaSuccess)
-      e = specv::resident_launch(r, bf16, mode, p.kernel == 2, p.cluster, p.ctas, p.res_smem,
-                                 stream);
+      e = specv::resident_launch(r, bf16, mode, p.cluster, p.ctas, p.res_smem, stream);
   } else {
     specv::RowArgs a;
     a.target = target;
@@ -622,7 +532,7 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     a.stats_seg_tiles = p.seg_tiles;
     a.stats_segs_per_slice = p.segs_per_slice;
     if (e == cudaSuccess)
-      e = specv::rows_launch(a, bf16, mode, aligned, p.cluster, p.ctas, stream, p.kernel == 6);
+      e = specv::rows_launch(a, bf16, mode, aligned, p.cluster, p.ctas, stream);
     if (e == cudaSuccess && a.defer_sampling) {
       specv::RowArgs a2 = a;
       a2.groups_per_slice = p.sample_gps;
@@ -663,6 +573,8 @@ struct HostPipe {
   cudaEvent_t ready[kHostMaxChunks];
   void *stage;
   size_t stage_bytes;
+  unsigned char *h_alive;  // page-locked: the early-exit call's per-sequence flags
+  size_t h_alive_bytes;
 };
 std::vector<HostPipe *> g_pipes;  // never freed while the process runs
 
@@ -820,6 +732,315 @@ specv_status verify_host(const void *target, const void *draft, const int32_t *t
   return SPECV_OK;
 }
 
+// ---------------------------------------------------------------------------
+// One batch sharded over devices.  Sequences are independent, so shard g of G
+// is the contiguous run [lo_g, hi_g) of sequences with lo_g = g (B / G) +
+// min(g, B mod G): sizes differ by at most one, and the shards concatenate to
+// the batch in order.  Each shard runs verify_host on its device, on a stream
+// the library owns per (device, shard index); the outputs land in the
+// caller's host arrays at the shard's offset.  Nothing crosses devices: no
+// collective, no peer memory.
+constexpr int kMaxShards = 64;
+
+void shard_range(int64_t B, int32_t G, int32_t g, int64_t *lo, int64_t *hi) {
+  const int64_t q = B / G, r = B % G;
+  *lo = g * q + (g < r ? g : r);
+  *hi = *lo + q + (g < r ? 1 : 0);
+}
+
+struct ShardStream {
+  int dev;
+  int shard;
+  cudaStream_t stream;
+};
+std::vector<ShardStream> g_shard_streams;  // never destroyed while the process runs
+
+// The library's stream for (dev, shard); dev must be current.
+specv_status shard_stream(int dev, int shard, cudaStream_t *out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  for (const ShardStream &x : g_shard_streams)
+    if (x.dev == dev && x.shard == shard) {
+      *out = x.stream;
+      return SPECV_OK;
+    }
+  cudaStream_t s = nullptr;
+  const cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  g_shard_streams.push_back(ShardStream{dev, shard, s});
+  *out = s;
+  return SPECV_OK;
+}
+
+specv_status verify_sharded(const void *target, const void *draft, const int32_t *tokens,
+                            const float *ua, const float *ur, const float *lam, int64_t B,
+                            int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,
+                            int32_t *out_tokens, int32_t *out_n, int32_t G,
+                            const int32_t *devices) {
+  if (!target || !draft || !tokens || !ua || !ur || !lam || !out_tokens || !out_n || !devices)
+    return SPECV_ERR_INVALID_ARG;
+  if (!sizes_ok(B, K, V, dtype, mode) || G < 1 || G > kMaxShards) return SPECV_ERR_INVALID_ARG;
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  for (int g = 0; g < G; ++g)
+    if (devices[g] < 0 || devices[g] >= ndev) return SPECV_ERR_INVALID_ARG;
+  int caller_dev = 0;
+  if ((e = cudaGetDevice(&caller_dev)) != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  const size_t elem = dtype == SPECV_BF16 ? 2 : 4;
+  const size_t row = (size_t)V * elem;
+  specv_status status = SPECV_OK;
+  cudaStream_t streams[kMaxShards] = {};
+  // launch every shard (asynchronous: the devices work at the same time) ...
+  for (int g = 0; g < G && status == SPECV_OK; ++g) {
+    int64_t lo = 0, hi = 0;
+    shard_range(B, G, g, &lo, &hi);
+    if (hi == lo) continue;  // fewer sequences than shards
+    if ((e = cudaSetDevice(devices[g])) != cudaSuccess) {
+      note_cuda_error(e);
+      (void)cudaGetLastError();
+      status = SPECV_ERR_CUDA;
+      break;
+    }
+    if ((status = shard_stream(devices[g], g, &streams[g])) != SPECV_OK) break;
+    status = verify_host(static_cast<const char *>(target) + (size_t)lo * (K + 1) * row,
+                         static_cast<const char *>(draft) + (size_t)lo * K * row, tokens + lo * K,
+                         ua + lo * K, ur + lo, lam + lo, hi - lo, K, V, dtype, mode,
+                         out_tokens + lo * (K + 1), out_n + lo, 0, streams[g]);
+  }
+  // ... then wait for all that were launched, so the outputs are in place on return
+  for (int g = 0; g < G; ++g) {
+    if (streams[g] == nullptr) continue;
+    if ((e = cudaSetDevice(devices[g])) == cudaSuccess) e = cudaStreamSynchronize(streams[g]);
+    if (e != cudaSuccess && status == SPECV_OK) {
+      note_cuda_error(e);
+      (void)cudaGetLastError();
+      status = SPECV_ERR_CUDA;
+    }
+  }
+  (void)cudaSetDevice(caller_dev);
+  return status;
+}
+
+// ---------------------------------------------------------------------------
+// Verify on host buffers, copying only the rows the verify step reaches.  The
+// pages' loop stops at a sequence's first rejection, so the rows after it
+// never influence the outputs; over a host link slower than HBM by a factor of
+// about 30 those rows are most of the cost.  The batch goes over position by
+// position: level i copies row pair (b, i) (at i = K the bonus row) of every
+// sequence still alive, as one 2-D copy per run of live sequences, then the
+// decision pass (specv_host_levels.cu) clears the flag of every sequence
+// whose position i clearly rejects, and the host reads the flags back before
+// the next level.  The sequences are dealt into kEeGroups interleaved groups
+// (b mod kEeGroups), each with its own stream and level: while the host waits
+// for one group's flags, the link carries another group's rows.  Rows never
+// copied hold stale staging bytes; they all lie after their sequence's first
+// rejection (the decision pass only stops a sequence on a rejection the verify
+// step cannot see otherwise), so the ordinary verify step that follows on the
+// staged batch never uses them.
+constexpr int kEeGroups = 2;
+
+specv_status verify_host_early_exit(const void *target, const void *draft, const int32_t *tokens,
+                                    const float *ua, const float *ur, const float *lam, int64_t B,
+                                    int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,
+                                    int32_t *out_tokens, int32_t *out_n, int64_t *out_h2d,
+                                    int64_t *out_d2h, void *stream_ptr) {
+  if (!target || !draft || !tokens || !ua || !ur || !lam || !out_tokens || !out_n)
+    return SPECV_ERR_INVALID_ARG;
+  if (!sizes_ok(B, K, V, dtype, mode)) return SPECV_ERR_INVALID_ARG;
+  const size_t elem = dtype == SPECV_BF16 ? 2 : 4;
+  if ((uint64_t)B * (uint64_t)(2 * K + 1) > ((uint64_t)1 << 50) / elem / (uint64_t)V)
+    return SPECV_ERR_NO_MEMORY;
+  int sms = kDefaultSMs;
+  int64_t l2 = kDefaultL2;
+  specv_status s = ensure_device(&sms, &l2);
+  if (s != SPECV_OK) return s;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return SPECV_ERR_UNSUPPORTED;
+  int dev = 0;
+  (void)cudaGetDevice(&dev);
+
+  // staging: the layout of verify_host, then the live flags (group-major:
+  // group g's flags at g * Bg, Bg = ceil(B / kEeGroups))
+  const int64_t Bg = (B + kEeGroups - 1) / kEeGroups;
+  const size_t row = (size_t)V * elem;
+  const size_t t_bytes = (size_t)B * (K + 1) * row, d_bytes = (size_t)B * K * row;
+  const size_t bk4 = (size_t)B * K * 4, b4 = (size_t)B * 4, bk14 = (size_t)B * (K + 1) * 4;
+  const size_t o_d = round256(t_bytes), o_tok = o_d + round256(d_bytes);
+  const size_t o_ua = o_tok + round256(bk4), o_ur = o_ua + round256(bk4);
+  const size_t o_lam = o_ur + round256(b4), o_ot = o_lam + round256(b4);
+  const size_t o_on = o_ot + round256(bk14), o_al = o_on + round256(b4);
+  const size_t flags = (size_t)(kEeGroups * Bg);
+  const size_t need = o_al + round256(flags);
+  HostPipe *hp = nullptr;
+  if ((s = host_pipe(dev, stream, need, &hp)) != SPECV_OK) return s;
+  if (hp->h_alive_bytes < flags) {
+    if (hp->h_alive != nullptr) {  // no copy into it is pending, but drain the streams anyway
+      (void)cudaStreamSynchronize(stream);
+      (void)cudaStreamSynchronize(hp->copy);
+      (void)cudaFreeHost(hp->h_alive);
+    }
+    hp->h_alive = nullptr;
+    hp->h_alive_bytes = 0;
+    void *h = nullptr;
+    if (cudaHostAlloc(&h, grow_to(flags), cudaHostAllocDefault) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return SPECV_ERR_NO_MEMORY;
+    }
+    hp->h_alive = static_cast<unsigned char *>(h);
+    hp->h_alive_bytes = grow_to(flags);
+  }
+  char *st = static_cast<char *>(hp->stage);
+  unsigned char *alive = reinterpret_cast<unsigned char *>(st + o_al);
+  unsigned char *h_alive = hp->h_alive;
+  const char *tgt = static_cast<const char *>(target);
+  const char *dft = static_cast<const char *>(draft);
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+  int64_t copied = (int64_t)(2 * bk4 + 2 * b4), read_back = (int64_t)(bk14 + b4);
+  // group 0 works on the caller's stream, group 1 on the library's copy stream
+  static_assert(kEeGroups >= 1 && kEeGroups <= 2, "one stream per group");
+  cudaStream_t gs[2] = {stream, hp->copy};
+  e = cudaMemcpyAsync(st + o_tok, tokens, bk4, h2d, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st + o_ua, ua, bk4, h2d, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st + o_ur, ur, b4, h2d, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st + o_lam, lam, b4, h2d, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(alive, 1, flags, stream);
+  // the other group's stream starts after these (and after earlier work on `stream`)
+  if (e == cudaSuccess) e = cudaEventRecord(hp->start, stream);
+  for (int g = 1; g < kEeGroups && e == cudaSuccess; ++g) e = cudaStreamWaitEvent(gs[g], hp->start, 0);
+  std::memset(h_alive, 1, flags);
+
+  // the decision pass's geometry: one cluster per sequence
+  const int vw = (int)(16 / elem);
+  const int64_t G = (V + vw - 1) / vw;
+  int S = specv::stream_cluster_size(Bg, (int64_t)row, G, sms);
+  while (S > 1 && Bg * S > INT32_MAX) S /= 2;
+  if (Bg * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
+  const bool aligned = row % 16 == 0;
+  int level[kEeGroups];
+  bool active[kEeGroups];
+
+  // level lv of group g: the live members' rows, then (below K) the decision
+  // pass and the read-back of the group's flags, all on the group's stream
+  auto issue = [&](int g) -> cudaError_t {
+    const int64_t cnt = (B - g + kEeGroups - 1) / kEeGroups;  // members b = g + kEeGroups * j
+    const unsigned char *hf = h_alive + g * Bg;
+    const int lv = level[g];
+    const size_t tp = (size_t)kEeGroups * (K + 1) * row, dp = (size_t)kEeGroups * K * row;
+    int64_t live = 0;
+    cudaError_t err = cudaSuccess;
+    for (int64_t j0 = 0; j0 < cnt && err == cudaSuccess;) {
+      if (!hf[j0]) {
+        ++j0;
+        continue;
+      }
+      int64_t j1 = j0 + 1;
+      while (j1 < cnt && hf[j1]) ++j1;
+      const size_t h = (size_t)(j1 - j0);
+      const int64_t b0 = g + (int64_t)kEeGroups * j0;
+      const size_t ot = ((size_t)b0 * (K + 1) + lv) * row;
+      err = cudaMemcpy2DAsync(st + ot, tp, tgt + ot, tp, row, h, h2d, gs[g]);
+      copied += (int64_t)(h * row);
+      if (err == cudaSuccess && lv < K) {
+        const size_t od = ((size_t)b0 * K + lv) * row;
+        err = cudaMemcpy2DAsync(st + o_d + od, dp, dft + od, dp, row, h, h2d, gs[g]);
+        copied += (int64_t)(h * row);
+      }
+      live += j1 - j0;
+      j0 = j1;
+    }
+    if (err != cudaSuccess) return err;
+    if (lv == K || live == 0) {
+      active[g] = false;
+      return cudaSuccess;
+    }
+    specv::LevelArgs la;
+    la.target = st;
+    la.draft = st + o_d;
+    la.tokens = reinterpret_cast<const int32_t *>(st + o_tok);
+    la.u_accept = reinterpret_cast<const float *>(st + o_ua);
+    la.lam = reinterpret_cast<const float *>(st + o_lam);
+    la.alive = alive + g * Bg;
+    la.count = cnt;
+    la.group = g;
+    la.n_groups = kEeGroups;
+    la.K = K;
+    la.V = V;
+    la.level = lv;
+    la.num_groups = (int)G;
+    la.groups_per_slice = (int)((G + S - 1) / S);
+    err = specv::level_launch(la, dtype == SPECV_BF16, mode, aligned, S, gs[g]);
+    if (err == cudaSuccess)
+      err = cudaMemcpyAsync(h_alive + g * Bg, alive + g * Bg, (size_t)cnt, cudaMemcpyDeviceToHost,
+                            gs[g]);
+    if (err == cudaSuccess) err = cudaEventRecord(hp->ready[g], gs[g]);
+    read_back += cnt;
+    return err;
+  };
+  for (int g = 0; g < kEeGroups; ++g) {
+    level[g] = 0;
+    active[g] = g < B;
+  }
+  for (int g = 0; g < kEeGroups && e == cudaSuccess; ++g)
+    if (active[g]) e = issue(g);
+  for (bool any = true; any && e == cudaSuccess;) {
+    any = false;
+    for (int g = 0; g < kEeGroups && e == cudaSuccess; ++g) {
+      if (!active[g]) continue;
+      any = true;
+      e = cudaEventSynchronize(hp->ready[g]);  // the group's flags are on the host
+      if (e == cudaSuccess) {
+        ++level[g];
+        e = issue(g);
+      }
+    }
+  }
+  // the verify step on the staged batch once every group's copies are in
+  for (int g = 1; g < kEeGroups && e == cudaSuccess; ++g) {
+    e = cudaEventRecord(hp->ready[g], gs[g]);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, hp->ready[g], 0);
+  }
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  s = run(st, st + o_d, reinterpret_cast<const int32_t *>(st + o_tok),
+          reinterpret_cast<const float *>(st + o_ua), reinterpret_cast<const float *>(st + o_ur),
+          reinterpret_cast<const float *>(st + o_lam), B, K, V, dtype, mode,
+          reinterpret_cast<int32_t *>(st + o_ot), reinterpret_cast<int32_t *>(st + o_on), nullptr,
+          nullptr, nullptr, stream);
+  if (s != SPECV_OK) return s;
+  e = cudaMemcpyAsync(out_tokens, st + o_ot, bk14, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out_n, st + o_on, b4, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  if (out_h2d) *out_h2d = copied;
+  if (out_d2h) *out_d2h = read_back;
+  return SPECV_OK;
+}
+
 // An NVTX range named after the entry point around its host work and launches:
 // visible on the timeline of NVIDIA's profilers, a no-op when none is attached.
 struct NvtxRange {
@@ -851,6 +1072,39 @@ specv_status specv_verify_host(const void *target_logits, const void *draft_logi
   NvtxRange range("specv_verify_host");
   return verify_host(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lambda, B,
                      K, V, dtype, mode, out_tokens, out_n_accepted, chunks, stream);
+}
+
+specv_status specv_verify_host_early_exit(const void *target_logits, const void *draft_logits,
+                                          const int32_t *draft_tokens, const float *u_accept,
+                                          const float *u_resample, const float *lambda,
+                                          int64_t B, int32_t K, int32_t V, specv_dtype dtype,
+                                          specv_mode mode, int32_t *out_tokens,
+                                          int32_t *out_n_accepted, int64_t *out_h2d_bytes,
+                                          int64_t *out_d2h_bytes, void *stream) {
+  NvtxRange range("specv_verify_host_early_exit");
+  return verify_host_early_exit(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                                lambda, B, K, V, dtype, mode, out_tokens, out_n_accepted,
+                                out_h2d_bytes, out_d2h_bytes, stream);
+}
+
+specv_status specv_shard_bounds(int64_t B, int32_t n_shards, int32_t shard, int64_t *lo,
+                                int64_t *hi) {
+  if (!lo || !hi || B < 0 || n_shards < 1 || n_shards > kMaxShards || shard < 0 ||
+      shard >= n_shards)
+    return SPECV_ERR_INVALID_ARG;
+  shard_range(B, n_shards, shard, lo, hi);
+  return SPECV_OK;
+}
+
+specv_status specv_verify_sharded_host(const void *target_logits, const void *draft_logits,
+                                       const int32_t *draft_tokens, const float *u_accept,
+                                       const float *u_resample, const float *lambda, int64_t B,
+                                       int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,
+                                       int32_t *out_tokens, int32_t *out_n_accepted,
+                                       int32_t n_shards, const int32_t *devices) {
+  NvtxRange range("specv_verify_sharded_host");
+  return verify_sharded(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lambda,
+                        B, K, V, dtype, mode, out_tokens, out_n_accepted, n_shards, devices);
 }
 
 specv_status specv_verify_debug(const void *target_logits, const void *draft_logits,
@@ -1079,6 +1333,69 @@ int32_t specv_choose_k(double alpha, double cost_draft, double cost_verify_fixed
     }
   }
   return best_k;
+}
+
+specv_status specv_release_stream(void *stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if ((e = cudaStreamIsCapturing(s, &cap)) != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return SPECV_ERR_UNSUPPORTED;
+  std::vector<void *> dev_bufs, host_bufs;
+  std::vector<cudaStream_t> copy_streams;
+  std::vector<cudaEvent_t> events;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (size_t k = 0; k < g_ws.size();) {
+      Workspace &w = g_ws[k];
+      if (w.dev == dev && w.stream == s) {
+        if (w.count) dev_bufs.push_back(w.count);
+        if (w.data) dev_bufs.push_back(w.data);
+        for (void *p : w.superseded) dev_bufs.push_back(p);
+        g_ws.erase(g_ws.begin() + (std::ptrdiff_t)k);
+      } else {
+        ++k;
+      }
+    }
+    for (size_t k = 0; k < g_pipes.size();) {
+      HostPipe *hp = g_pipes[k];
+      if (hp->dev == dev && hp->stream == s) {
+        if (hp->stage) dev_bufs.push_back(hp->stage);
+        if (hp->h_alive) host_bufs.push_back(hp->h_alive);
+        copy_streams.push_back(hp->copy);
+        events.push_back(hp->start);
+        for (int c = 0; c < kHostMaxChunks; ++c) events.push_back(hp->ready[c]);
+        delete hp;
+        g_pipes.erase(g_pipes.begin() + (std::ptrdiff_t)k);
+      } else {
+        ++k;
+      }
+    }
+  }
+  // the stream's queued work may still use the buffers: let it finish first
+  e = cudaStreamSynchronize(s);
+  for (cudaStream_t c : copy_streams)
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c);
+  for (void *p : dev_bufs) (void)cudaFree(p);
+  for (void *p : host_bufs) (void)cudaFreeHost(p);
+  for (cudaEvent_t ev : events) (void)cudaEventDestroy(ev);
+  for (cudaStream_t c : copy_streams) (void)cudaStreamDestroy(c);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  return SPECV_OK;
 }
 
 const char *specv_status_string(specv_status status) {

@@ -39,9 +39,25 @@ __device__ __forceinline__ float exp_shifted(float z, float m) {
 }
 
 // Logit-mode mixture (1 - l) z_t + l z_q, written as z_t + l (z_q - z_t):
-// equal in exact arithmetic, and exactly z_t whenever z_q == z_t.
+// equal in exact arithmetic, and exactly z_t whenever z_q == z_t.  A term of
+// weight zero drops out, so l = 0 gives z_t and l = 1 gives z_q exactly,
+// whatever the other row holds.  Masked logits (-inf, e.g. a padded
+// vocabulary or a grammar mask): a masked entry of a row with positive weight
+// masks the mixed entry.  For 0 < l < 1 the expression is -inf when z_q is,
+// and NaN when z_t is -inf (inf - inf); fmaxf turns that NaN into -inf and
+// leaves every other value alone.
+__device__ __forceinline__ float mix_logit_interior(float zt, float zq, float lam) {
+  return fmaxf(__fmaf_rn(lam, __fsub_rn(zq, zt), zt), -INFINITY);
+}
 __device__ __forceinline__ float mix_logit(float zt, float zq, float lam) {
-  return __fmaf_rn(lam, __fsub_rn(zq, zt), zt);
+  return lam == 0.0f ? zt : (lam == 1.0f ? zq : mix_logit_interior(zt, zq, lam));
+}
+
+// The exponent offset -m log2e of a running maximum m, or 0 while m is -inf
+// (every entry folded so far is masked): then the masked entries give
+// 2^(-inf) = 0 instead of 2^(-inf + inf) = NaN.
+__device__ __forceinline__ float neg_scaled_max(float m) {
+  return m == -INFINITY ? 0.0f : -__fmul_rn(m, kLog2e);
 }
 
 // bf16 bits -> fp32 (exact).
@@ -173,10 +189,10 @@ __device__ __forceinline__ void warp_argmax(float &w, int &idx) {
   }
 }
 
-// Greedy score of one entry: the mixed logit z_t + l (z_q - z_t), -inf where
-// the draft logit is -inf (the draft rules the entry out).
+// Greedy score of one entry: the mixed logit z_t + l (z_q - z_t), with the
+// masking rule of mix_logit.
 __device__ __forceinline__ float greedy_score(float zt, float zq, float lam) {
-  return zq == -INFINITY ? -INFINITY : mix_logit(zt, zq, lam);
+  return mix_logit(zt, zq, lam);
 }
 
 // Statistics of one position: A = source row of p~ (target row in
@@ -191,21 +207,27 @@ struct PosStats {
 //   prob:  r = p_t(x)/q(x) = e^{(zt_x - mA) - (zq_x - mB)} * sB / sA and
 //          p~/q = 1 + (1 - l)(r - 1), which is exactly 1 when r == 1 or l == 1.
 //   logit: p~/q = e^{(w_x - mA) - (zq_x - mB)} * sB / sA, w_x = mix_logit(.).
+//   q(x) = 0 (the drafted token is masked in the draft row): the ratio is
+//   +inf (accept) if p~(x) > 0, else 0 (reject).
 __device__ __forceinline__ float accept_ratio(int mode, const PosStats &st, float zt_x, float zq_x,
                                               float lam, float *ptilde_x, float *q_x) {
   float a_x = (mode == kProbMix) ? zt_x : mix_logit(zt_x, zq_x, lam);
   float da = __fsub_rn(a_x, st.mA);
   float db = __fsub_rn(zq_x, st.mB);
-  float d = __fsub_rn(da, db);
-  float e = (d == 0.0f) ? 1.0f : ex2(__fmul_rn(d, kLog2e));
-  // sB / sA with the SFU reciprocal (a few ulp); exactly 1 for equal sums
-  float r = __fmul_rn(e, st.sB == st.sA ? 1.0f : __fdividef(st.sB, st.sA));
   if (ptilde_x != nullptr) {
     float q = __fdividef(ex2(__fmul_rn(db, kLog2e)), st.sB);
     float pa = __fdividef(ex2(__fmul_rn(da, kLog2e)), st.sA);
     *q_x = q;
     *ptilde_x = (mode == kProbMix) ? __fmaf_rn(lam, q, __fmul_rn(__fsub_rn(1.0f, lam), pa)) : pa;
   }
+  if (zq_x == -INFINITY) {
+    const bool pos = (mode == kProbMix) ? (lam < 1.0f && zt_x != -INFINITY) : (a_x != -INFINITY);
+    return pos ? INFINITY : 0.0f;
+  }
+  float d = __fsub_rn(da, db);
+  float e = (d == 0.0f) ? 1.0f : ex2(__fmul_rn(d, kLog2e));
+  // sB / sA with the SFU reciprocal (a few ulp); exactly 1 for equal sums
+  float r = __fmul_rn(e, st.sB == st.sA ? 1.0f : __fdividef(st.sB, st.sA));
   if (mode == kProbMix) r = __fmaf_rn(__fsub_rn(1.0f, lam), __fsub_rn(r, 1.0f), 1.0f);
   return r;
 }

@@ -6,6 +6,10 @@
 
 namespace specv {
 
+// Records the CUDA error behind a SPECV_ERR_CUDA for specv_last_cuda_error
+// (per host thread).
+void note_cuda_error(cudaError_t e);
+
 constexpr int kRowThreads = 256;   // threads per CTA of the cluster row kernel
 constexpr int kMaxCluster = 16;    // largest cluster (non-portable size, opt-in)
 constexpr int kTileThreads = 256;  // threads per CTA of the small-vocabulary kernel
@@ -34,42 +38,6 @@ inline void segment_geometry(int64_t groups, int tile_groups, int *seg_tiles, in
 inline void rows_segments(int groups_per_slice, int *seg_tiles, int *segs_per_slice) {
   segment_geometry(groups_per_slice, kSegGroups, seg_tiles, segs_per_slice);
 }
-
-// The sweep row kernel: persistent CTAs of kSweepThreads threads stream
-// chunks of rows through a ring of kSweepStages shared-memory stages filled by
-// 1-D bulk copies.  A stage holds one chunk of a target row and the same chunk
-// of its draft row.  The sampler reads tiles of 32 * kSweepLaneGroups groups.
-constexpr int kSweepThreads = 256;
-constexpr int kSweepStages = 3;
-constexpr int kSweepLaneGroups = 4;
-constexpr int kSweepSegGroups = 32 * kSweepLaneGroups;
-
-struct SweepArgs {
-  const void *target;        // [B][K+1][V], 16-byte aligned, V * sizeof(dtype) % 16 == 0
-  const void *draft;         // [B][K][V], same
-  const int32_t *tokens;     // [B][K]
-  const float *u_accept;     // [B][K]
-  const float *u_resample;   // [B]
-  const float *lam;          // [B]
-  int64_t B;
-  int K;
-  int V;
-  int32_t *out_tokens;       // [B][K+1]
-  int32_t *out_n;            // [B]
-  float4 *ws_chunk;          // scratch [B][K+1][chunks]: (mA, sA, mB, sB) of every chunk
-  float4 *ws_stats;          // scratch [B][K+1]: (mA, sA, mB, sB) of every position
-  unsigned *row_count;       // scratch [B][K+1]: chunks published (zero at entry, left zero)
-  unsigned *seq_count;       // scratch [B]: positions published (zero at entry, left zero)
-  float *dbg_ptilde;         // optional [B][K]
-  float *dbg_q;              // optional [B][K]
-  float *dbg_lse;            // optional [B][K+1][2]
-  int num_groups;            // V / elements per 16 bytes
-  int chunk_groups;          // groups per chunk (a multiple of kSweepThreads)
-  int chunks;                // chunks per row
-  int seg_tiles;             // sampler segment = seg_tiles * kSweepSegGroups groups
-  int nseg;                  // sampler segments per row (<= kMaxSegs)
-  int64_t items;             // B * (K+1) * chunks
-};
 
 // Cluster size of the streaming row kernels (verify, greedy, tree) for P
 // positions of rows of row_bytes bytes (groups 16-byte groups) on `sms` SMs.
@@ -187,10 +155,8 @@ struct ResArgs {
 };
 
 cudaError_t resident_prepare(int max_smem);
-// staged = true: slices staged in shared memory by TMA; false: read in place
-// from global memory (the sampler re-reads the slice, from L2 when it fits).
-cudaError_t resident_launch(const ResArgs &a, int dtype_bf16, int mode, bool staged, int S,
-                            int64_t grid, int smem, cudaStream_t stream);
+cudaError_t resident_launch(const ResArgs &a, int dtype_bf16, int mode, int S, int64_t grid,
+                            int smem, cudaStream_t stream);
 
 // Arguments of the acceptance-probability kernel (one cluster per drafted
 // position b*K + i).
@@ -237,22 +203,37 @@ cudaError_t tree_prepare();
 cudaError_t tree_launch(const TreeArgs &a, int dtype_bf16, int mode, bool aligned, int S,
                         int64_t grid, cudaStream_t stream);
 
-// Dynamic shared memory of the sweep kernel for chunks of chunk_groups groups.
-inline int sweep_smem_bytes(int chunk_groups) { return kSweepStages * 2 * chunk_groups * 16; }
-cudaError_t sweep_prepare(int max_smem_bytes);
-int sweep_blocks_per_sm(int dtype_bf16, int mode, int smem_bytes);
-cudaError_t sweep_launch(const SweepArgs &a, int dtype_bf16, int mode, int64_t grid,
-                         int smem_bytes, cudaStream_t stream);
-
 cudaError_t rows_prepare();
-// ring = true (16-byte aligned rows only): the slices stream through the
-// shared-memory ring of bulk copies of specv_ring.cuh instead of register loads.
 cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
-                        int64_t grid, cudaStream_t stream, bool ring = false);
+                        int64_t grid, cudaStream_t stream);
 // The deferred token draws: one cluster of S CTAs per sequence (grid B * S),
 // after a rows_launch with defer_sampling = 1 on the same stream.
 cudaError_t rows_sample_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
                                int64_t grid, cudaStream_t stream);
+
+// Arguments of the host-buffer call's decision pass (one cluster per
+// sequence of one group): the group holds sequences b = group + n_groups * j,
+// j in [0, count); position `level` of every one with alive[j] != 0 is
+// decided, and alive[j] is cleared when it clearly rejects.
+struct LevelArgs {
+  const void *target;        // [B][K+1][V] (staged; rows up to `level` present for live sequences)
+  const void *draft;         // [B][K][V]
+  const int32_t *tokens;     // [B][K]
+  const float *u_accept;     // [B][K]
+  const float *lam;          // [B]
+  unsigned char *alive;      // [count]: the group's flags
+  int64_t count;             // sequences in the group
+  int group;
+  int n_groups;
+  int K;
+  int V;
+  int level;                 // position decided, in [0, K)
+  int groups_per_slice;
+  int num_groups;
+};
+cudaError_t level_prepare();
+cudaError_t level_launch(const LevelArgs &a, int dtype_bf16, int mode, bool aligned, int S,
+                         cudaStream_t stream);
 
 cudaError_t tile_tma_prepare(int max_smem_bytes);
 int tile_tma_blocks_per_sm(int dtype_bf16, int mode, int smem_bytes);

@@ -52,27 +52,33 @@ int g_sms[kMaxDevices] = {};
 // kernel attributes, and the SM count.
 specv_status setup(int *dev_out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    specv::note_cuda_error(e);
     (void)cudaGetLastError();
     return SPECV_ERR_CUDA;
   }
+  if (dev < 0 || dev >= kMaxDevices) return SPECV_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_lock);
   if (g_scratch_ptr[dev] == nullptr) {
     void *ptr = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e != cudaSuccess || ptr == nullptr) {
+      specv::note_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
       (void)cudaGetLastError();
       return SPECV_ERR_CUDA;
     }
     int major = 0, cluster_ok = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&cluster_ok, cudaDevAttrClusterLaunch, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&cluster_ok, cudaDevAttrClusterLaunch, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+      specv::note_cuda_error(e);
       (void)cudaGetLastError();
       return SPECV_ERR_CUDA;
     }
     if (major < 10 || !cluster_ok) return SPECV_ERR_UNSUPPORTED;
-    if (specv::rows_prepare() != cudaSuccess) {
+    if ((e = specv::rows_prepare()) != cudaSuccess) {
+      specv::note_cuda_error(e);
       (void)cudaGetLastError();
       return SPECV_ERR_CUDA;
     }
@@ -147,6 +153,7 @@ extern "C" specv_status specv_verify_noalloc(const void *target_logits, const vo
   cudaError_t e = cudaMemsetAsync(a.ws_count, 0, (size_t)B * sizeof(unsigned), s);
   if (e == cudaSuccess) e = specv::rows_launch(a, bf16, mode, aligned, S, P * S, s);
   if (e != cudaSuccess) {
+    specv::note_cuda_error(e);
     (void)cudaGetLastError();
     return SPECV_ERR_CUDA;
   }

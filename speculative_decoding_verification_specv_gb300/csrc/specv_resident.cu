@@ -61,7 +61,7 @@ struct __align__(16) ResShared {
 };
 
 // Online (max, sum-exp) over this thread's groups of one chunk of the slice.
-template <typename T, int MODE, bool STAGED>
+template <typename T, int MODE>
 __device__ __forceinline__ void chunk_stats(const uint4 *cA, const uint4 *cB, int cnt, bool pair,
                                             float lam, float &mA, float &sA, float &mB, float &sB) {
   constexpr int VW = Elem<T>::kPerVec;
@@ -74,8 +74,8 @@ __device__ __forceinline__ void chunk_stats(const uint4 *cA, const uint4 *cB, in
       const int g = g0 + u * kNT;
       ok[u] = g < cnt;
       if (ok[u]) {
-        za[u] = ld_group_stream<STAGED>(cA + g);
-        if (pair) zb[u] = ld_group_stream<STAGED>(cB + g);
+        za[u] = cA[g];
+        if (pair) zb[u] = cB[g];
       }
     }
     auto a_val = [&](int u, int e) -> float {
@@ -101,13 +101,16 @@ __device__ __forceinline__ void chunk_stats(const uint4 *cA, const uint4 *cB, in
       sB = __fmul_rn(sB, exp_shifted(mB, bmB));
       mB = bmB;
     }
+    // while a running maximum is -inf every entry so far is masked: shift by 0
+    // (2^(-inf) = 0) instead of by -inf (NaN)
+    const float shA = mA == -INFINITY ? 0.0f : mA, shB = mB == -INFINITY ? 0.0f : mB;
 #pragma unroll
     for (int u = 0; u < U; ++u)
       if (ok[u]) {
 #pragma unroll
         for (int e = 0; e < VW; ++e) {
-          sA = __fadd_rn(sA, exp_shifted(a_val(u, e), mA));
-          if (pair) sB = __fadd_rn(sB, exp_shifted(Elem<T>::get(zb[u], e), mB));
+          sA = __fadd_rn(sA, exp_shifted(a_val(u, e), shA));
+          if (pair) sB = __fadd_rn(sB, exp_shifted(Elem<T>::get(zb[u], e), shB));
         }
       }
   }
@@ -141,7 +144,7 @@ __device__ void finalize_sequence(const ResArgs &a, int64_t b) {
   if (lane == 0) a.out_n[b] = n;
 }
 
-template <typename T, int MODE, bool STAGED>
+template <typename T, int MODE>
 __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
   constexpr int VW = Elem<T>::kPerVec;
   extern __shared__ __align__(128) unsigned char dsm[];
@@ -158,13 +161,13 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
   const T *rowB = static_cast<const T *>(a.draft) + (b * K + (pair ? i : 0)) * (int64_t)a.V;
   const int g_lo = rank * a.groups_per_slice;
   const int ng = max(0, min(a.num_groups, g_lo + a.groups_per_slice) - g_lo);
-  // the slice: staged in shared memory, or read in place from global memory
+  // the slice in global memory, and its copy in shared memory
   const uint4 *gA = reinterpret_cast<const uint4 *>(rowA + (int64_t)g_lo * VW);
   const uint4 *gB = reinterpret_cast<const uint4 *>(rowB + (int64_t)g_lo * VW);
   uint4 *stA = reinterpret_cast<uint4 *>(dsm);
   uint4 *stB = stA + a.groups_per_slice;
-  const uint4 *bA = STAGED ? stA : gA;
-  const uint4 *bB = STAGED ? stB : gB;
+  const uint4 *bA = stA;
+  const uint4 *bB = stB;
   const int nch = (ng + kChunkGroups - 1) / kChunkGroups;
   const float lam = a.lam[b];
 
@@ -183,21 +186,19 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
   }
 
   // ---------------------------------------------------------------- staging
-  if constexpr (STAGED) {
-    if (threadIdx.x == 0) {
-      for (int c = 0; c < nch; ++c) mbar_init(&sh.bar[c], 1);
-      mbar_fence_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int c = 0; c < nch; ++c) {
-        const int g0 = c * kChunkGroups;
-        const int cnt = min(kChunkGroups, ng - g0);
-        const uint32_t bytes = (uint32_t)cnt * 16u;
-        mbar_arrive_expect_tx(&sh.bar[c], pair ? 2u * bytes : bytes);
-        tma_load_1d(stA + g0, gA + g0, bytes, &sh.bar[c]);
-        if (pair) tma_load_1d(stB + g0, gB + g0, bytes, &sh.bar[c]);
-      }
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < nch; ++c) mbar_init(&sh.bar[c], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < nch; ++c) {
+      const int g0 = c * kChunkGroups;
+      const int cnt = min(kChunkGroups, ng - g0);
+      const uint32_t bytes = (uint32_t)cnt * 16u;
+      mbar_arrive_expect_tx(&sh.bar[c], pair ? 2u * bytes : bytes);
+      tma_load_1d(stA + g0, gA + g0, bytes, &sh.bar[c]);
+      if (pair) tma_load_1d(stB + g0, gB + g0, bytes, &sh.bar[c]);
     }
   }
 
@@ -205,12 +206,9 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
   float mA = -INFINITY, sA = 0.0f, mB = -INFINITY, sB = 0.0f;
   int err = 0;
   for (int c = 0; c < nch; ++c) {
-    if constexpr (STAGED) {
-      if (!mbar_wait(&sh.bar[c], 0)) err = 1;
-    }
+    if (!mbar_wait(&sh.bar[c], 0)) err = 1;
     const int g0 = c * kChunkGroups;
-    chunk_stats<T, MODE, STAGED>(bA + g0, bB + g0, min(kChunkGroups, ng - g0), pair, lam, mA, sA,
-                                 mB, sB);
+    chunk_stats<T, MODE>(bA + g0, bB + g0, min(kChunkGroups, ng - g0), pair, lam, mA, sA, mB, sB);
   }
   err = __syncthreads_or(err);
   block_merge_stats<kNT>(sh.bs, mA, sA, mB, sB);
@@ -250,7 +248,7 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
         a.dbg_q[b * K + i] = qx;
       }
       status = acc ? kRecAccepted : kRecRejected;
-      if (!acc) kind = (MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual;
+      if (!acc) kind = !(lam < 1.0f) ? kWMixture : kWResidual;
     }
     if (rank == 0 && a.dbg_lse) {
       a.dbg_lse[p * 2 + 0] = m0 + lg2(s0) * kLn2;
@@ -272,7 +270,7 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
     float R = 0.0f;
     int attempt = 0;
     for (;; ++attempt) {
-      const float mass = chunk_masses<T, MODE, STAGED, kNT>(sh, bA, bB, ng, kind, sp);
+      const float mass = chunk_masses<T, MODE, kNT>(sh, bA, bB, ng, kind, sp);
       if (threadIdx.x == 0)
         for (int r = 0; r < S; ++r) cluster.map_shared_rank(sh.masses[attempt], r)[rank] = mass;
       cluster.sync();  // all slice masses exchanged
@@ -304,7 +302,7 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
       }
       publisher = rstar;
       if (rank == rstar) {
-        const int local = chunk_search<T, MODE, STAGED, kNT>(sh, bA, bB, ng, kind, sp, tloc);
+        const int local = chunk_search<T, MODE, kNT>(sh, bA, bB, ng, kind, sp, tloc);
         token = local >= 0 ? g_lo * VW + local : -1;
       }
     }
@@ -326,12 +324,12 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
   if (sh.last && threadIdx.x < 32) finalize_sequence(a, b);
 }
 
-template <typename T, int MODE, bool STAGED>
+template <typename T, int MODE>
 cudaError_t launch_one(const ResArgs &a, int S, int64_t grid, int smem, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kNT, 1, 1);
-  cfg.dynamicSmemBytes = STAGED ? (size_t)smem : 0;
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -340,50 +338,39 @@ cudaError_t launch_one(const ResArgs &a, int S, int64_t grid, int smem, cudaStre
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, resident_kernel<T, MODE, STAGED>, a);
-}
-
-template <typename T, int MODE, bool STAGED>
-cudaError_t prepare_one(int max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(resident_kernel<T, MODE, STAGED>,
-                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess || !STAGED) return e;
-  return cudaFuncSetAttribute(resident_kernel<T, MODE, STAGED>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  return cudaLaunchKernelEx(&cfg, resident_kernel<T, MODE>, a);
 }
 
 template <typename T, int MODE>
-cudaError_t launch_variant(const ResArgs &a, bool staged, int S, int64_t grid, int smem,
-                           cudaStream_t stream) {
-  return staged ? launch_one<T, MODE, true>(a, S, grid, smem, stream)
-                : launch_one<T, MODE, false>(a, S, grid, smem, stream);
+cudaError_t prepare_one(int max_smem) {
+  cudaError_t e = cudaFuncSetAttribute(resident_kernel<T, MODE>,
+                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(resident_kernel<T, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              max_smem);
 }
 
 }  // namespace
 
 cudaError_t resident_prepare(int max_smem) {
   cudaError_t e = cudaSuccess, r;
-#define SPECV_PREP(T, M, ST) \
-  if ((r = prepare_one<T, M, ST>(max_smem)) != cudaSuccess) e = r;
-  SPECV_PREP(float, kProbMix, true)
-  SPECV_PREP(float, kLogitMix, true)
-  SPECV_PREP(uint16_t, kProbMix, true)
-  SPECV_PREP(uint16_t, kLogitMix, true)
-  SPECV_PREP(float, kProbMix, false)
-  SPECV_PREP(float, kLogitMix, false)
-  SPECV_PREP(uint16_t, kProbMix, false)
-  SPECV_PREP(uint16_t, kLogitMix, false)
+#define SPECV_PREP(T, M) \
+  if ((r = prepare_one<T, M>(max_smem)) != cudaSuccess) e = r;
+  SPECV_PREP(float, kProbMix)
+  SPECV_PREP(float, kLogitMix)
+  SPECV_PREP(uint16_t, kProbMix)
+  SPECV_PREP(uint16_t, kLogitMix)
 #undef SPECV_PREP
   return e;
 }
 
-cudaError_t resident_launch(const ResArgs &a, int dtype_bf16, int mode, bool staged, int S,
-                            int64_t grid, int smem, cudaStream_t stream) {
+cudaError_t resident_launch(const ResArgs &a, int dtype_bf16, int mode, int S, int64_t grid,
+                            int smem, cudaStream_t stream) {
   if (dtype_bf16)
-    return mode == kProbMix ? launch_variant<uint16_t, kProbMix>(a, staged, S, grid, smem, stream)
-                            : launch_variant<uint16_t, kLogitMix>(a, staged, S, grid, smem, stream);
-  return mode == kProbMix ? launch_variant<float, kProbMix>(a, staged, S, grid, smem, stream)
-                          : launch_variant<float, kLogitMix>(a, staged, S, grid, smem, stream);
+    return mode == kProbMix ? launch_one<uint16_t, kProbMix>(a, S, grid, smem, stream)
+                            : launch_one<uint16_t, kLogitMix>(a, S, grid, smem, stream);
+  return mode == kProbMix ? launch_one<float, kProbMix>(a, S, grid, smem, stream)
+                          : launch_one<float, kLogitMix>(a, S, grid, smem, stream);
 }
 
 }  // namespace specv

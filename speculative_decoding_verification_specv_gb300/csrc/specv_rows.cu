@@ -42,7 +42,6 @@
 #include "specv_block.cuh"
 #include "specv_device.cuh"
 #include "specv_internal.h"
-#include "specv_ring.cuh"
 #include "specv_segments.cuh"
 #include "specv_stream.cuh"
 
@@ -55,17 +54,6 @@ namespace {
 constexpr int kNT = kRowThreads;  // threads per CTA
 constexpr int kNW = kNT / 32;     // warps per CTA
 constexpr int kUnroll = 4;        // 16-byte groups per thread per batch
-constexpr int kRingU = kRingChunkGroups / kNT;  // groups per thread per row of a ring chunk
-static_assert(kRingChunkGroups % kNT == 0, "a ring chunk is whole groups per thread");
-
-// Marker in the scratch statistics of a position whose bulk copies did not
-// land in time (a sum of exponentials is never negative).
-constexpr float kCopyFailedSum = -1.0f;
-// The same marker in the greedy candidates (an index is never negative).
-constexpr int kCopyFailedIndex = -2;
-
-// Stages of the bulk-copy ring (dynamic shared memory of the ring variants).
-extern __shared__ __align__(128) unsigned char g_ring_buf[];
 
 struct Broadcast {
   int n;        // first rejected position (K if none), -1 if the sequence is invalid
@@ -76,9 +64,7 @@ struct Broadcast {
 
 struct __align__(16) RowsShared {
   BlockScratch<kNT> bs;
-  RingState ring;
-  float part[4];
-  int pfail;              // this CTA's bulk copies did not land in time
+  float4 part[kMaxCluster];  // every rank's partial, pushed into rank 0's copy
   int last;
   Broadcast bc;
   float masses[2][kMaxCluster];
@@ -86,35 +72,6 @@ struct __align__(16) RowsShared {
   float segm[kMaxSegs];   // sampler weight of each segment of the slice
   float segi[kMaxSegs];   // running sums of segm in index order (inclusive)
 };
-
-// Greedy: folds one 16-byte group (elements idx0, idx0 + 1, ...) into this
-// thread's candidate (best, bidx).  A thread visits its groups in increasing
-// index order, so the first maximum in index order is kept by taking a group
-// only when its maximum is strictly larger (or when it is the thread's first
-// group), and then its first entry equal to that maximum; the per-element
-// work is the score and one maximum.  Entries past V are -inf.
-template <typename T>
-__device__ __forceinline__ void greedy_fold_group(const uint4 &za, const uint4 &zb, bool pair,
-                                                  float lam, int idx0, float &best, int &bidx) {
-  constexpr int VW = Elem<T>::kPerVec;
-  float w[VW];
-#pragma unroll
-  for (int e = 0; e < VW; ++e) {
-    const float zt = Elem<T>::get(za, e);
-    w[e] = pair ? greedy_score(zt, Elem<T>::get(zb, e), lam) : zt;
-  }
-  float gm = w[0];
-#pragma unroll
-  for (int e = 1; e < VW; ++e) gm = fmaxf(gm, w[e]);
-  if (gm > best || (bidx == INT_MAX && gm == gm)) {
-    int first = VW - 1;
-#pragma unroll
-    for (int e = VW - 1; e >= 0; --e)
-      if (w[e] == gm) first = e;
-    best = gm;
-    bidx = idx0 + first;
-  }
-}
 
 // Phase 1 of the bonus row: (max, sum-exp) of every segment of this CTA's
 // slice, written to out[s] for s < nseg (an empty segment gives (-inf, 0)),
@@ -291,9 +248,43 @@ __device__ void draw_token(RowsShared &sh, cg::cluster_group &cluster, int S, in
   if (lane == 0) *out = tok;
 }
 
-template <typename T, int MODE, bool ALIGNED, bool RING>
+// Arrival of position (b, .) at the sequence's counter, after its statistics
+// (and its own draw, if any) are written: returns 1 for the last of the K + 1
+// positions, which resets the counter and the early-exit word for the next call.
+__device__ __forceinline__ int arrive(const RowArgs &a, int64_t b, int K) {
+  __threadfence();
+  const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
+  const int last = prev == (unsigned)K;
+  if (last) {
+    __threadfence();
+    a.ws_count[b] = 0;  // every position has arrived: leave the counter zero for the next call
+    if (a.ws_reject != nullptr) a.ws_reject[b] = 0;  // and the early-exit word
+  }
+  return last;
+}
+
+// Position statistics in the scratch: (mA, sA, mB, sB), with the sign of sB
+// (a sum of exponentials, never negative) carrying the position's own
+// decision: negative when its acceptance test rejects.
+__device__ __forceinline__ float4 pack_stats(float mA, float sA, float mB, float sB, bool rejected) {
+  return make_float4(mA, sA, mB, rejected ? -sB : sB);
+}
+__device__ __forceinline__ bool stats_rejected(const float4 &st) {
+  return (__float_as_uint(st.w) >> 31) != 0u;
+}
+__device__ __forceinline__ PosStats stats_of(const float4 &st) {
+  return PosStats{st.x, st.y, st.z, fabsf(st.w)};
+}
+
+// Sampler kind of the token at index n < K: the residual, or p~ itself when
+// the residual is identically zero (lambda = 1: p~ = q in either mixture).
+template <int MODE>
+__device__ __forceinline__ int residual_kind(float lam) {
+  return !(lam < 1.0f) ? kWMixture : kWResidual;
+}
+
+template <typename T, int MODE, bool ALIGNED>
 __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
-  constexpr int VW = Elem<T>::kPerVec;
   __shared__ RowsShared sh;
   cg::cluster_group cluster = cg::this_cluster();
   const int S = (int)cluster.num_blocks();
@@ -331,33 +322,28 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   // from now on; it waits for this whole grid to complete before it reads
   // anything this grid writes.
   if (a.defer_sampling) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // The inputs of this position's own acceptance test, loaded now so that
+  // their latency hides behind the stream (rank 0's thread 0 decides).
+  int x_own = -1;
+  float u_own = 0.0f, zt_own = 0.0f, zq_own = 0.0f;
+  if (rank == 0 && threadIdx.x == 0 && pair && !skip) {
+    x_own = a.tokens[b * K + i];
+    u_own = a.u_accept[b * K + i];
+    if (x_own >= 0 && x_own < V) {
+      zt_own = Elem<T>::load(rowA + x_own);
+      zq_own = Elem<T>::load(rowB + x_own);
+    }
+  }
 
   // ---------------------------------------------------------------- phase 1
   float mA = -INFINITY, sA = 0.0f, mB = -INFINITY, sB = 0.0f;
   const int seg_groups = a.seg_tiles * kSegGroups;
   const int nseg = a.segs_per_slice;
-  bool copy_ok = true;
   if (skip) {
     // nothing to read: a rejection before this position is already published
   } else if (!pair && a.ws_seg != nullptr) {
     bonus_segment_stats<T, ALIGNED>(rowA, V, g_lo, g_hi, seg_groups, nseg,
                                     a.ws_seg + (b * S + rank) * (int64_t)nseg, mA, sA);
-  } else if (RING) {
-    // the slice through the bulk-copy ring: thread t folds groups t, t + kNT, ... of each chunk
-    copy_ok = ring_stream<kNT>(sh.ring, g_ring_buf, rowA, rowB, pair, g_lo, g_hi,
-                               [&](const uint4 *cA, const uint4 *cB, int cnt, int) {
-                                 uint4 za[kRingU], zb[kRingU];
-                                 bool ok[kRingU];
-#pragma unroll
-                                 for (int u = 0; u < kRingU; ++u) {
-                                   const int g = (int)threadIdx.x + u * kNT;
-                                   ok[u] = g < cnt;
-                                   za[u] = ok[u] ? cA[g] : make_uint4(0u, 0u, 0u, 0u);
-                                   zb[u] = (ok[u] && pair) ? cB[g] : za[u];
-                                 }
-                                 fold_batch<T, MODE, kRingU>(za, zb, ok, pair, lam_seq, mA, sA,
-                                                             mB, sB);
-                               });
   } else {
     // with early exit the stream stops when an earlier rejection is published meanwhile
     const bool stopped = slice_stats<T, MODE, ALIGNED, kNT, kUnroll>(
@@ -368,48 +354,24 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   if (a.ws_reject != nullptr) skip = __syncthreads_or(skip) != 0;  // CTA-wide: partial statistics
   block_merge_stats<kNT>(sh.bs, mA, sA, mB, sB);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) {
-    sh.part[0] = mA;
-    sh.part[1] = sA;
-    sh.part[2] = mB;
-    sh.part[3] = sB;
-    sh.pfail = copy_ok ? 0 : 1;
-  }
-  cluster.sync();  // partials of every rank are visible
+  if (threadIdx.x == 0) cluster.map_shared_rank(sh.part, 0)[rank] = make_float4(mA, sA, mB, sB);
+  cluster.sync();  // every rank's partial is in rank 0's shared memory
   if (rank == 0 && threadIdx.x == 0) {
     float m0, s0, m1, s1;
-    merge_stats2_n(
-        S,
-        [&](int r) {
-          const float *pr = cluster.map_shared_rank(sh.part, r);
-          return make_float4(pr[0], pr[1], pr[2], pr[3]);
-        },
-        m0, s0, m1, s1);
-    int fail = 0;
-    for (int r = 0; r < S; ++r) fail |= *cluster.map_shared_rank(&sh.pfail, r);
-    if (fail) s0 = s1 = kCopyFailedSum;
-    if (a.ws_reject != nullptr && pair && !fail && !skip) {
-      // publish this position's own decision when it rejects (the test the
-      // last cluster repeats from the same statistics, so the same outcome)
-      const int x = a.tokens[b * K + i];
-      if (x >= 0 && x < V && lambda_valid(lam_seq)) {
-        const PosStats st{m0, s0, m1, s1};
-        float qx = 0.0f;
-        const float ratio = accept_ratio(MODE, st, Elem<T>::load(rowA + x), Elem<T>::load(rowB + x),
-                                         lam_seq, nullptr, &qx);
-        if (!accept_test(a.u_accept[b * K + i], ratio))
-          atomicMax(&a.ws_reject[b], (unsigned)(K + 1 - i));
-      }
+    merge_stats2_n(S, [&](int r) { return sh.part[r]; }, m0, s0, m1, s1);
+    // this position's own decision, from the merged statistics (the last
+    // cluster of the sequence reads it back instead of testing again)
+    bool own_reject = false;
+    if (pair && !skip && x_own >= 0 && x_own < V && lambda_valid(lam_seq)) {
+      const PosStats st{m0, s0, m1, s1};
+      float qx = 0.0f;
+      const float ratio = accept_ratio(MODE, st, zt_own, zq_own, lam_seq, nullptr, &qx);
+      own_reject = !accept_test(u_own, ratio);
     }
-    a.ws_stats[p] = make_float4(m0, s0, m1, s1);
-    __threadfence();
-    const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
-    const int last = prev == (unsigned)K;
-    if (last) {
-      __threadfence();
-      a.ws_count[b] = 0;  // every position has arrived: leave the counter zero for the next call
-      if (a.ws_reject != nullptr) a.ws_reject[b] = 0;  // and the early-exit word
-    }
+    // early exit: publish a rejection at once
+    if (own_reject && a.ws_reject != nullptr) atomicMax(&a.ws_reject[b], (unsigned)(K + 1 - i));
+    a.ws_stats[p] = pack_stats(m0, s0, m1, s1, own_reject);
+    const int last = arrive(a, b, K);
     for (int r = 0; r < S; ++r) *cluster.map_shared_rank(&sh.last, r) = last;
   }
   cluster.sync();  // sh.last is set in every rank; rank 0 is done reading partials
@@ -430,33 +392,27 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
         lane_ok = lane_ok && tok_ok;
         if (tok_ok && lam_ok) {
           const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + j]);
-          const PosStats st{st4.x, st4.y, st4.z, st4.w};
-          const float zt_x = Elem<T>::load(tgt + (b * (K + 1) + j) * (int64_t)V + x);
-          const float zq_x = Elem<T>::load(dft + (b * K + j) * (int64_t)V + x);
-          float px = 0.0f, qx = 0.0f;
-          const float ratio =
-              accept_ratio(MODE, st, zt_x, zq_x, lam_seq, a.dbg_ptilde ? &px : nullptr, &qx);
-          rejected = !accept_test(a.u_accept[b * K + j], ratio);
-          if (a.dbg_ptilde) a.dbg_ptilde[b * K + j] = px;
-          if (a.dbg_q) a.dbg_q[b * K + j] = qx;
+          rejected = stats_rejected(st4);  // the position's own decision
+          if (a.dbg_ptilde) {  // the debug entry point also reports p~(x), q(x)
+            const float zt_x = Elem<T>::load(tgt + (b * (K + 1) + j) * (int64_t)V + x);
+            const float zq_x = Elem<T>::load(dft + (b * K + j) * (int64_t)V + x);
+            float px = 0.0f, qx = 0.0f;
+            (void)accept_ratio(MODE, stats_of(st4), zt_x, zq_x, lam_seq, &px, &qx);
+            a.dbg_ptilde[b * K + j] = px;
+            if (a.dbg_q) a.dbg_q[b * K + j] = qx;
+          }
         }
       }
       const unsigned rej = __ballot_sync(0xffffffffu, rejected);
       if (rej != 0u && n == K) n = i0 + __ffs(rej) - 1;
     }
     const bool all_tok = __all_sync(0xffffffffu, lane_ok);  // every lane votes
-    bool copy_err = false;
-    if (RING) {  // a position whose bulk copies did not land: the sequence reports -2
-      for (int j = lane; j <= K; j += 32)
-        copy_err = copy_err || __ldcg(&a.ws_stats[b * (K + 1) + j]).y == kCopyFailedSum;
-      copy_err = __any_sync(0xffffffffu, copy_err);
-    }
-    const bool valid = lam_ok && all_tok && !copy_err;
+    const bool valid = lam_ok && all_tok;
     if (a.dbg_lse) {
       for (int j = lane; j <= K; j += 32) {
         const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + j]);
         a.dbg_lse[(b * (K + 1) + j) * 2 + 0] = st4.x + lg2(st4.y) * kLn2;
-        a.dbg_lse[(b * (K + 1) + j) * 2 + 1] = j < K ? st4.z + lg2(st4.w) * kLn2 : 0.0f;
+        a.dbg_lse[(b * (K + 1) + j) * 2 + 1] = j < K ? st4.z + lg2(fabsf(st4.w)) * kLn2 : 0.0f;
       }
     }
     for (int j = lane; j <= K; j += 32) {
@@ -465,18 +421,13 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
       if (!valid || j != n) a.out_tokens[b * (K + 1) + j] = out;
     }
     if (lane == 0) {
-      a.out_n[b] = valid ? n : (copy_err ? -2 : -1);
+      a.out_n[b] = valid ? n : -1;
       Broadcast bc;
       bc.n = valid ? n : -1;
       bc.u = a.u_resample[b];
-      const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + (valid ? n : 0)]);
-      bc.sp = make_sample_params_rn(st4.x, st4.y, st4.z, st4.w, lam_seq);
-      if (n == K)
-        bc.kind = kWBonus;
-      else if (MODE == kProbMix && !(lam_seq < 1.0f))
-        bc.kind = kWMixture;  // p~ = q: the residual is identically zero
-      else
-        bc.kind = kWResidual;
+      const PosStats st = stats_of(__ldcg(&a.ws_stats[b * (K + 1) + (valid ? n : 0)]));
+      bc.sp = make_sample_params_rn(st.mA, st.sA, st.mB, st.sB, lam_seq);
+      bc.kind = n == K ? kWBonus : residual_kind<MODE>(lam_seq);
       if (!a.defer_sampling)
         for (int r = 0; r < S; ++r) *cluster.map_shared_rank(&sh.bc, r) = bc;
     }
@@ -518,10 +469,9 @@ __global__ void __launch_bounds__(kNT, 4) rows_sample_kernel(RowArgs a) {
   const int n = a.out_n[b];
   if (n < 0) return;  // invalid sequence (or a timed-out copy): nothing to draw
   const float lam = a.lam[b];
-  const float4 st4 = __ldcg(&a.ws_stats[b * (K + 1) + n]);
-  const SampleParams sp = make_sample_params_rn(st4.x, st4.y, st4.z, st4.w, lam);
-  const int kind = n == K ? kWBonus
-                          : ((MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual);
+  const PosStats st = stats_of(__ldcg(&a.ws_stats[b * (K + 1) + n]));
+  const SampleParams sp = make_sample_params_rn(st.mA, st.sA, st.mB, st.sB, lam);
+  const int kind = n == K ? kWBonus : residual_kind<MODE>(lam);
   const float u = a.u_resample[b];
   const T *tgt = static_cast<const T *>(a.target);
   const T *dft = static_cast<const T *>(a.draft);
@@ -552,7 +502,7 @@ __global__ void __launch_bounds__(kNT, 4) rows_sample_kernel(RowArgs a) {
 // accepts x_i iff it is the argmax of row i, stops at the first mismatch and
 // emits that argmax there, or the argmax of target row K when every draft
 // matches.  There is no sampling pass: each logit is read once.
-template <typename T, bool ALIGNED, bool RING>
+template <typename T, bool ALIGNED>
 __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
   constexpr int VW = Elem<T>::kPerVec;
   __shared__ RowsShared sh;
@@ -589,24 +539,10 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
 
   float best = -INFINITY;
   int bidx = INT_MAX;
-  bool copy_ok = true;
-  if (skip) {
-    // an earlier position of this sequence is already known to mismatch
-  } else if (RING) {
-    copy_ok = ring_stream<kNT>(sh.ring, g_ring_buf, rowA, rowB, pair, g_lo, g_hi,
-                               [&](const uint4 *cA, const uint4 *cB, int cnt, int c_lo) {
-#pragma unroll
-                                 for (int u = 0; u < kRingU; ++u) {
-                                   const int g = (int)threadIdx.x + u * kNT;
-                                   if (g < cnt)
-                                     greedy_fold_group<T>(cA[g], pair ? cB[g] : cA[g], pair, lam,
-                                                          (c_lo + g) * VW, best, bidx);
-                                 }
-                               });
-  }
+  // (skip: an earlier position of this sequence is already known to mismatch)
   unsigned seen = 0u;  // early exit while streaming, as in slice_stats
   int it = 0;
-  for (int g0 = g_lo + (int)threadIdx.x; !RING && !skip && g0 < g_hi; g0 += kNT * kUnroll, ++it) {
+  for (int g0 = g_lo + (int)threadIdx.x; !skip && g0 < g_hi; g0 += kNT * kUnroll, ++it) {
     if (a.ws_reject != nullptr && it % kExitEvery == 0) {
       if (seen != 0u && K + 1 - (int)seen < i) {
         skip = true;
@@ -640,36 +576,21 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
     float m = -INFINITY;
     int ix = INT_MAX;
     for (int w = 0; w < kNW; ++w) argmax_merge(m, ix, sh.bs.red[w][0], __float_as_int(sh.bs.red[w][1]));
-    sh.part[0] = m;
-    sh.part[1] = __int_as_float(ix);
-    sh.pfail = copy_ok ? 0 : 1;
+    cluster.map_shared_rank(sh.part, 0)[rank] = make_float4(m, __int_as_float(ix), 0.0f, 0.0f);
   }
-  cluster.sync();  // candidates of every rank are visible
+  cluster.sync();  // every rank's candidate is in rank 0's shared memory
   if (rank == 0 && threadIdx.x == 0) {
     float m = -INFINITY;
     int ix = INT_MAX;
-    int fail = 0;
-    for (int r = 0; r < S; ++r) {
-      const float *pr = cluster.map_shared_rank(sh.part, r);
-      argmax_merge(m, ix, pr[0], __float_as_int(pr[1]));
-      fail |= *cluster.map_shared_rank(&sh.pfail, r);
-    }
-    if (fail) ix = kCopyFailedIndex;
-    if (a.ws_reject != nullptr && pair && !fail && !skip) {
+    for (int r = 0; r < S; ++r) argmax_merge(m, ix, sh.part[r].x, __float_as_int(sh.part[r].y));
+    if (a.ws_reject != nullptr && pair && !skip) {
       // publish this position's mismatch (the last cluster repeats the test)
       const int x = a.tokens[b * K + i];
       if (x >= 0 && x < V && lambda_valid(lam) && ix != x)
         atomicMax(&a.ws_reject[b], (unsigned)(K + 1 - i));
     }
     a.ws_stats[p] = make_float4(m, __int_as_float(ix), 0.0f, 0.0f);
-    __threadfence();
-    const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
-    const int last = prev == (unsigned)K;
-    if (last) {
-      __threadfence();
-      a.ws_count[b] = 0;
-      if (a.ws_reject != nullptr) a.ws_reject[b] = 0;
-    }
+    const int last = arrive(a, b, K);
     for (int r = 0; r < S; ++r) *cluster.map_shared_rank(&sh.last, r) = last;
   }
   cluster.sync();  // sh.last is set in every rank; rank 0 is done reading candidates
@@ -692,38 +613,31 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
     const unsigned rej = __ballot_sync(0xffffffffu, rejected);
     if (rej != 0u && n == K) n = i0 + __ffs(rej) - 1;
   }
-  bool copy_err = false;
-  if (RING) {  // a position whose bulk copies did not land: the sequence reports -2
-    for (int j = lane; j <= K; j += 32)
-      copy_err = copy_err ||
-                 __float_as_int(__ldcg(&a.ws_stats[b * (K + 1) + j]).y) == kCopyFailedIndex;
-    copy_err = __any_sync(0xffffffffu, copy_err);
-  }
-  const bool valid = lam_ok && __all_sync(0xffffffffu, lane_ok) && !copy_err;  // every lane votes
+  const bool valid = lam_ok && __all_sync(0xffffffffu, lane_ok);  // every lane votes
   for (int j = lane; j <= K; j += 32) {
     int out = -1;
     if (valid && j < n) out = a.tokens[b * K + j];
     if (valid && j == n) out = __float_as_int(__ldcg(&a.ws_stats[b * (K + 1) + n]).y);
     a.out_tokens[b * (K + 1) + j] = out;
   }
-  if (lane == 0) a.out_n[b] = valid ? n : (copy_err ? -2 : -1);
+  if (lane == 0) a.out_n[b] = valid ? n : -1;
 }
 
-template <typename T, int MODE, bool ALIGNED, bool RING>
+template <typename T, int MODE, bool ALIGNED>
 constexpr void (*row_kernel_of())(RowArgs) {
   if constexpr (MODE == kGreedy)
-    return rows_greedy_kernel<T, ALIGNED, RING>;
+    return rows_greedy_kernel<T, ALIGNED>;
   else
-    return rows_kernel<T, MODE, ALIGNED, RING>;
+    return rows_kernel<T, MODE, ALIGNED>;
 }
 
-template <typename T, int MODE, bool ALIGNED, bool RING = false>
+template <typename T, int MODE, bool ALIGNED>
 cudaError_t launch_one(const RowArgs &a, int S, int64_t grid, cudaStream_t stream) {
-  void (*kern)(RowArgs) = row_kernel_of<T, MODE, ALIGNED, RING>();
+  void (*kern)(RowArgs) = row_kernel_of<T, MODE, ALIGNED>();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kNT, 1, 1);
-  cfg.dynamicSmemBytes = RING ? kRingSmemBytes : 0;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -758,18 +672,8 @@ cudaError_t launch_sample_one(const RowArgs &a, int S, int64_t grid, cudaStream_
 
 template <typename T, int MODE, bool ALIGNED>
 cudaError_t prepare_one() {
-  cudaError_t e = cudaFuncSetAttribute(row_kernel_of<T, MODE, ALIGNED, false>(),
+  cudaError_t e = cudaFuncSetAttribute(row_kernel_of<T, MODE, ALIGNED>(),
                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if constexpr (ALIGNED) {
-    void (*ring)(RowArgs) = row_kernel_of<T, MODE, true, true>();
-    cudaError_t er = cudaFuncSetAttribute(ring, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (er == cudaSuccess)
-      er = cudaFuncSetAttribute(ring, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemBytes);
-    if (er == cudaSuccess)
-      er = cudaFuncSetAttribute(ring, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                cudaSharedmemCarveoutMaxShared);
-    if (e == cudaSuccess) e = er;
-  }
   if constexpr (MODE != kGreedy) {
     const cudaError_t e2 = cudaFuncSetAttribute(rows_sample_kernel<T, MODE, ALIGNED>,
                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -802,17 +706,7 @@ cudaError_t rows_prepare() {
 }
 
 cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
-                        int64_t grid, cudaStream_t stream, bool ring) {
-  if (ring && aligned) {
-    if (mode == kGreedy)
-      return dtype_bf16 ? launch_one<uint16_t, kGreedy, true, true>(a, S, grid, stream)
-                        : launch_one<float, kGreedy, true, true>(a, S, grid, stream);
-    if (dtype_bf16)
-      return mode == kProbMix ? launch_one<uint16_t, kProbMix, true, true>(a, S, grid, stream)
-                              : launch_one<uint16_t, kLogitMix, true, true>(a, S, grid, stream);
-    return mode == kProbMix ? launch_one<float, kProbMix, true, true>(a, S, grid, stream)
-                            : launch_one<float, kLogitMix, true, true>(a, S, grid, stream);
-  }
+                        int64_t grid, cudaStream_t stream) {
   if (mode == kGreedy) {
     if (dtype_bf16)
       return aligned ? launch_one<uint16_t, kGreedy, true>(a, S, grid, stream)

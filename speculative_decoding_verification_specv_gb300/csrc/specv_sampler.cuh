@@ -11,25 +11,12 @@
 
 namespace specv {
 
-// 16-byte group loads: from shared memory (staged slices) or from global
-// memory (the streaming variant; statistics pass without L1 allocation, the
-// sampler's second read through the read-only path, usually an L2 hit).
-template <bool STAGED>
-__device__ __forceinline__ uint4 ld_group(const uint4 *p) {
-  if constexpr (STAGED) return *p;
-  else return __ldg(p);
-}
-template <bool STAGED>
-__device__ __forceinline__ uint4 ld_group_stream(const uint4 *p) {
-  if constexpr (STAGED) return *p;
-  else return ld_stream16(p);
-}
-
-// Sampler weights of the slice, by warp chunks: warp w owns the contiguous
+// The slice is staged in shared memory (bA, bB: its groups of the target and
+// draft rows).  Sampler weights of the slice, by warp chunks: warp w owns the contiguous
 // groups [w*Cw, (w+1)*Cw) and its lanes stride through them.  Each warp's
 // mass goes to wmass[w] (fixed-order butterfly); the CTA mass is their sum in
 // warp order, so the search below routes by exactly these numbers.
-template <typename T, int MODE, bool STAGED, int NT, typename SH>
+template <typename T, int MODE, int NT, typename SH>
 __device__ float chunk_masses(SH &sh, const uint4 *bA, const uint4 *bB, int ng, int kind,
                               const SampleParams &sp) {
   constexpr int VW = Elem<T>::kPerVec;
@@ -38,8 +25,8 @@ __device__ float chunk_masses(SH &sh, const uint4 *bA, const uint4 *bB, int ng, 
   const int lo = warp * Cw, hi = min(ng, lo + Cw);
   float acc = 0.0f;
   for (int g = lo + lane; g < hi; g += 32) {
-    const uint4 za = ld_group<STAGED>(bA + g);
-    const uint4 zb = kind != kWBonus ? ld_group<STAGED>(bB + g) : za;
+    const uint4 za = bA[g];
+    const uint4 zb = kind != kWBonus ? bB[g] : za;
 #pragma unroll
     for (int e = 0; e < VW; ++e)
       acc = __fadd_rn(acc, sample_weight(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e)));
@@ -60,7 +47,7 @@ __device__ float chunk_masses(SH &sh, const uint4 *bA, const uint4 *bB, int ng, 
 // inside).  Returns the slice-local element index; if round-off leaves no
 // crossing, the last entry with positive weight of the routed warp's range
 // (-1 if none).  Call after chunk_masses, with the same kind and parameters.
-template <typename T, int MODE, bool STAGED, int NT, typename SH>
+template <typename T, int MODE, int NT, typename SH>
 __device__ int chunk_search(SH &sh, const uint4 *bA, const uint4 *bB, int ng, int kind,
                             const SampleParams &sp, float t) {
   constexpr int VW = Elem<T>::kPerVec;
@@ -93,8 +80,8 @@ __device__ int chunk_search(SH &sh, const uint4 *bA, const uint4 *bB, int ng, in
       float w[VW];
       float gs = 0.0f;
       if (g < hi) {
-        const uint4 za = ld_group<STAGED>(bA + g);
-        const uint4 zb = kind != kWBonus ? ld_group<STAGED>(bB + g) : za;
+        const uint4 za = bA[g];
+        const uint4 zb = kind != kWBonus ? bB[g] : za;
 #pragma unroll
         for (int e = 0; e < VW; ++e) {
           w[e] = sample_weight(MODE, kind, sp, Elem<T>::get(za, e), Elem<T>::get(zb, e));

@@ -14,6 +14,7 @@
 // instruction sequence, so identical rows give bitwise identical statistics.
 #pragma once
 
+#include <climits>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -59,14 +60,21 @@ __device__ __forceinline__ void fold_batch(const uint4 (&za)[U], const uint4 (&z
                                            const bool (&ok)[U], bool pair, float lam, float &mA,
                                            float &sA, float &mB, float &sB) {
   constexpr int VW = Elem<T>::kPerVec;
+  if constexpr (MODE == kLogitMix) {
+    // lambda = 0 or 1: the mixed row is the target or the draft row itself
+    // (mix_logit's exact cases), folded as a plain row (an invalid lambda
+    // only makes its sequence invalid, whatever is folded)
+    if (pair && !(lam > 0.0f && lam < 1.0f)) {
+      const uint4(&src)[U] = lam == 0.0f ? za : zb;
+      fold_batch<T, kProbMix, U>(src, zb, ok, pair, lam, mA, sA, mB, sB);
+      return;
+    }
+  }
   // A-row value of element e of group u: the target logit, or in logit mode
-  // the mixed logit (entries past V stay -inf).
+  // the mixed logit (entries past V stay -inf)
   auto a_val = [&](int u, int e) -> float {
     const float zt = Elem<T>::get(za[u], e);
-    if (MODE == kLogitMix && pair) {
-      const float zq = Elem<T>::get(zb[u], e);
-      return zq == -INFINITY ? -INFINITY : mix_logit(zt, zq, lam);
-    }
+    if (MODE == kLogitMix && pair) return mix_logit_interior(zt, Elem<T>::get(zb[u], e), lam);
     return zt;
   };
   // logit mode with fp32 rows: the mixed logits are formed once and kept for
@@ -97,7 +105,7 @@ __device__ __forceinline__ void fold_batch(const uint4 (&za)[U], const uint4 (&z
     sB = __fmul_rn(sB, exp_shifted(mB, bmB));
     mB = bmB;
   }
-  const float nA = -__fmul_rn(mA, kLog2e), nB = -__fmul_rn(mB, kLog2e);
+  const float nA = neg_scaled_max(mA), nB = neg_scaled_max(mB);
 #pragma unroll
   for (int u = 0; u < U; ++u)
     if (ok[u]) {
@@ -150,6 +158,35 @@ __device__ __forceinline__ bool slice_stats(const T *rowA, const T *rowB, bool p
     fold_batch<T, MODE, U>(za, zb, ok, pair, lam, mA, sA, mB, sB);
   }
   return false;
+}
+
+// Greedy: folds one 16-byte group (elements idx0, idx0 + 1, ...) into this
+// thread's candidate (best, bidx).  A thread visits its groups in increasing
+// index order, so the first maximum in index order is kept by taking a group
+// only when its maximum is strictly larger (or when it is the thread's first
+// group), and then its first entry equal to that maximum; the per-element
+// work is the score and one maximum.  Entries past V are -inf.
+template <typename T>
+__device__ __forceinline__ void greedy_fold_group(const uint4 &za, const uint4 &zb, bool pair,
+                                                  float lam, int idx0, float &best, int &bidx) {
+  constexpr int VW = Elem<T>::kPerVec;
+  float w[VW];
+#pragma unroll
+  for (int e = 0; e < VW; ++e) {
+    const float zt = Elem<T>::get(za, e);
+    w[e] = pair ? greedy_score(zt, Elem<T>::get(zb, e), lam) : zt;
+  }
+  float gm = w[0];
+#pragma unroll
+  for (int e = 1; e < VW; ++e) gm = fmaxf(gm, w[e]);
+  if (gm > best || (bidx == INT_MAX && gm == gm)) {
+    int first = VW - 1;
+#pragma unroll
+    for (int e = VW - 1; e >= 0; --e)
+      if (w[e] == gm) first = e;
+    best = gm;
+    bidx = idx0 + first;
+  }
 }
 
 }  // namespace specv

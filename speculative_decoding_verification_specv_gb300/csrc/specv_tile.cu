@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kNT) tile_kernel(TileArgs a) {
       const float4 st4 = st_s[s * (K + 1) + n];
       const SampleParams sp = make_sample_params_rn(st4.x, st4.y, st4.z, st4.w, lam);
       int kind = (n == K) ? kWBonus
-                          : ((MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual);
+                          : (!(lam < 1.0f) ? kWMixture : kWResidual);
       const T *ra = st_t + ((int64_t)s * (K + 1) + n) * V;
       const T *rb = st_d + ((int64_t)s * K + (n < K ? n : 0)) * V;
       float R = 0.0f;

@@ -50,7 +50,13 @@ template <typename T, int MODE>
 __device__ __forceinline__ float2 row_stats(const uint4 *ra, const uint4 *rb, int G, int rot,
                                             bool mixed, float lam) {
   constexpr int VW = Elem<T>::kPerVec;
-  float m = -INFINITY, mL = -INFINITY, s = 0.0f;
+  // lambda = 0 or 1: the mixed row is the target or the draft row itself
+  if (MODE == kLogitMix && mixed && !(lam > 0.0f && lam < 1.0f))
+    return row_stats<T, kProbMix>(lam == 0.0f ? ra : rb, rb, G, rot, false, 0.0f);
+  // mL starts finite so that masked (-inf) entries before the first finite
+  // one add 2^(-inf) = 0 rather than NaN; s is still 0 when m first grows, and
+  // the rescale exponent is clamped at 0 so that 0 * 2^x stays 0
+  float m = -INFINITY, mL = 0.0f, s = 0.0f;
   int g = rot;
   for (int k = 0; k < G; ++k) {
     float z[VW];
@@ -58,7 +64,8 @@ __device__ __forceinline__ float2 row_stats(const uint4 *ra, const uint4 *rb, in
     if (MODE == kLogitMix && mixed) {
       const uint4 vb = rb[g];
 #pragma unroll
-      for (int e = 0; e < VW; ++e) z[e] = mix_logit(Elem<T>::get(va, e), Elem<T>::get(vb, e), lam);
+      for (int e = 0; e < VW; ++e)
+        z[e] = mix_logit_interior(Elem<T>::get(va, e), Elem<T>::get(vb, e), lam);
     } else {
 #pragma unroll
       for (int e = 0; e < VW; ++e) z[e] = Elem<T>::get(va, e);
@@ -68,7 +75,7 @@ __device__ __forceinline__ float2 row_stats(const uint4 *ra, const uint4 *rb, in
     for (int e = 1; e < VW; ++e) bm = fmaxf(bm, z[e]);
     if (bm > m) {
       const float nmL = __fmul_rn(bm, kLog2e);
-      s = __fmul_rn(s, ex2(__fsub_rn(mL, nmL)));
+      s = __fmul_rn(s, ex2(fminf(__fsub_rn(mL, nmL), 0.0f)));
       m = bm;
       mL = nmL;
     }
@@ -342,7 +349,7 @@ __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
       const float4 st4 = reinterpret_cast<const float4 *>(st_s)[pos];
       const SampleParams sp = make_sample_params(st4.x, st4.y, st4.z, st4.w, lam);
       int kind = (nn == K) ? kWBonus
-                           : ((MODE == kProbMix && !(lam < 1.0f)) ? kWMixture : kWResidual);
+                           : (!(lam < 1.0f) ? kWMixture : kWResidual);
       const uint4 *ra = reinterpret_cast<const uint4 *>(st_t + (int64_t)pos * V);
       const uint4 *rb = reinterpret_cast<const uint4 *>(st_d + ((int64_t)sl * K + (nn < K ? nn : 0)) * V);
       int tok = -1;

@@ -17,6 +17,14 @@ import torch
 import oracle
 
 BAND = 1e-5          # decision-boundary band
+# Greedy tie band, relative to the row's largest |logit| A.  The kernels form
+# w = z_t + lam (z_q - z_t) in fp32 (one rounded subtraction, one fused
+# multiply-add): |w32 - w| <= u (lam |z_q - z_t| + |w|)(1 + u) <= 3 u A (1 + u)
+# with u = 2^-24, so two entries whose exact scores differ by more than
+# 6 u A (1 + u) < 2^-21 A are ordered the same way in fp32 as in fp64.  Rows
+# whose fp64 gap between the best and the second-best score is below
+# 2^-20 A (a factor 2 of margin) count as near-ties.
+GREEDY_BAND = 2.0 ** -20
 TOL_F32 = 1e-5       # |p_gpu - p_oracle| for fp32 logits
 TOL_BF16 = 2e-3      # |p_gpu - p_oracle| for bf16 logits
 
@@ -142,8 +150,12 @@ def check_rows(xh, mode, dbg, seqs, tol=None):
                     pg = (1.0 - lam) * ptg + lam * qg
                 else:
                     lam32 = np.float32(lam)
-                    w = (zt32[j] + lam32 * (zq32[j] - zt32[j])).astype(np.float32)
-                    w = np.where(zq32[j] == -np.inf, -np.inf, w)
+                    if lam32 == 0 or lam32 == 1:  # a zero-weight term drops out exactly
+                        w = zt32[j] if lam32 == 0 else zq32[j]
+                    else:
+                        with np.errstate(invalid="ignore"):
+                            w = (zt32[j] + lam32 * (zq32[j] - zt32[j])).astype(np.float32)
+                        w = np.where(np.isnan(w), -np.inf, w)  # a masked entry of weight > 0
                     pg = np.exp(w.astype(np.float64) - lse[b, j, 0])
                 worst_q = max(worst_q, float(np.abs(qg - q_o[j]).max()))
             else:  # the bonus row: the target softmax
@@ -151,3 +163,113 @@ def check_rows(xh, mode, dbg, seqs, tol=None):
             worst_p = max(worst_p, float(np.abs(pg - pt_o[j]).max()))
     assert worst_p <= tol and worst_q <= tol, (worst_p, worst_q, tol)
     return dict(max_abs_err_ptilde_rows=worst_p, max_abs_err_q_rows=worst_q)
+
+
+def _near_argmax(w, A, t, band):
+    return np.isfinite(w[t]) and w[t] >= w.max() - band * A or w[t] == w.max()
+
+
+def _valid_greedy_outcome(xh_b, n, toks, band=GREEDY_BAND):
+    """Is (n, toks) a greedy outcome that fp32 rounding of the scores could
+    give?  Every accepted draft is a near-maximum of its row, the token at a
+    mismatch is a near-maximum of that row other than the draft, and a bonus
+    token is the exact argmax of target row K (w = z_t there, no rounding)."""
+    K = xh_b["draft_tokens"].shape[0]
+    if not (0 <= n <= K):
+        return False
+    drafts = xh_b["draft_tokens"].numpy()
+    if list(toks[:n]) != list(drafts[:n]) or any(t != -1 for t in toks[n + 1:]):
+        return False
+    zt = xh_b["target_logits"].float().numpy()
+    zq = xh_b["draft_logits"].float().numpy()
+    lam = float(xh_b["lam"])
+    V = zt.shape[-1]
+
+    def row(i):
+        w = oracle.greedy_scores(zt[i], zq[i], lam)
+        a = np.abs(np.concatenate([zt[i], zq[i]]).astype(np.float64))
+        A = float(a[np.isfinite(a)].max(initial=0.0))
+        return w, A
+    for i in range(n):
+        w, A = row(i)
+        if not _near_argmax(w, A, int(drafts[i]), band):
+            return False
+    t = int(toks[n])
+    if not (0 <= t < V):
+        return False
+    if n == K:
+        return t == oracle.greedy_argmax(zt[K], None, lam)
+    w, A = row(n)
+    return t != int(drafts[n]) and _near_argmax(w, A, t, band)
+
+
+def compare_greedy(xh, gpu_tokens, gpu_n, orc, seqs=None, band=GREEDY_BAND):
+    """Greedy outputs against the fp64 oracle: bit-exact for every sequence
+    whose decided rows are all farther than the band from a tie; within the
+    band, counted, and the GPU's output must be a valid greedy outcome.
+    Raises AssertionError on any mismatch outside the band."""
+    gt = np.asarray(gpu_tokens)
+    gn = np.asarray(gpu_n)
+    seqs = list(range(gn.shape[0])) if seqs is None else list(seqs)
+    near = exact = near_same = 0
+    mism = []
+    for j, b in enumerate(seqs):
+        on, ot = int(orc.n_accepted[j]), orc.tokens[j]
+        if on == -1:
+            if not (gn[b] == -1 and (gt[b] == -1).all()):
+                mism.append((b, "invalid", on, int(gn[b])))
+            continue
+        same = gn[b] == on and (gt[b] == ot).all()
+        if float(orc.tie_margin[j]) < band:
+            near += 1
+            if same:
+                near_same += 1
+                continue
+            xb = {k: v[b] for k, v in xh.items()}
+            if not _valid_greedy_outcome(xb, int(gn[b]), gt[b], band):
+                mism.append((b, "invalid-outcome-near-tie", on, int(gn[b]), ot.tolist(),
+                             gt[b].tolist()))
+            continue
+        if not same:
+            mism.append((b, "mismatch", on, int(gn[b]), ot.tolist(), gt[b].tolist(),
+                         float(orc.tie_margin[j])))
+        else:
+            exact += 1
+    rep = dict(sequences=len(seqs), exact=exact, near_tie=near, near_tie_same=near_same,
+               mismatches=len(mism))
+    assert not mism, f"{len(mism)} greedy mismatches outside the tie band: {mism[:5]} report={rep}"
+    return rep
+
+
+def compare_tree(xh, gpu_tokens, gpu_path, gpu_n, orc, band=BAND):
+    """Tree verification against the oracle: exact (n, tokens, path) outside
+    the decision band; inside it the GPU's walk must still be valid (each
+    accepted node a child of the previous one, carrying its token, then one
+    token in [0, V), then -1).  Returns (exact, near)."""
+    tok, path, n = (np.asarray(a) for a in (gpu_tokens, gpu_path, gpu_n))
+    par = np.asarray(xh["parent"])
+    ntok = np.asarray(xh["tokens"])
+    V = xh["target_logits"].shape[-1]
+    exact = near = 0
+    for b in range(n.shape[0]):
+        on = int(orc.n_accepted[b])
+        if on == -1:
+            assert n[b] == -1 and (tok[b] == -1).all() and (path[b] == -1).all(), b
+            continue
+        if orc.accept_margin[b] >= band and orc.cdf_margin[b] >= band:
+            assert n[b] == on, (b, n[b], on)
+            np.testing.assert_array_equal(tok[b], orc.tokens[b])
+            np.testing.assert_array_equal(path[b], orc.path[b])
+            exact += 1
+            continue
+        near += 1
+        k = int(n[b])
+        assert 0 <= k <= par.shape[1] - 1
+        prev = 0
+        for j in range(k):
+            c = int(path[b, j])
+            assert par[b, c] == prev and tok[b, j] == ntok[b, c]
+            prev = c
+        assert 0 <= tok[b, k] < V
+        assert (tok[b, k + 1:] == -1).all() and (path[b, k:] == -1).all()
+    return exact, near

@@ -88,27 +88,6 @@ def test_plan_selects_kernels(lib):
         specv.plan(0, 4, 32)
 
 
-def test_plan_sweep_variant(lib, monkeypatch):
-    """The sweep row kernel (forced by SPECV_ROWS_VARIANT=sweep): persistent grid
-    of two CTAs per SM at most, scratch = chunk statistics + position statistics
-    + one counter per position and per sequence; rows not on 16-byte boundaries
-    are refused."""
-    monkeypatch.setenv("SPECV_ROWS_VARIANT", "sweep")
-    B, K, V = 256, 8, 128256
-    p = specv.plan(B, K, V, specv.F32)
-    P, G = B * (K + 1), V // 4
-    C = -(-G // 1024)
-    assert p["kernel"] == "rows-sweep" and p["cluster"] == 1
-    assert p["ctas"] <= 2 * 152
-    r16 = lambda x: -(-x // 16) * 16  # noqa: E731
-    assert p["workspace_bytes"] == r16(P * C * 16) + r16(P * 16) + r16((P + B) * 4)
-    # few positions: chunks shrink to 256 groups and the grid to the items
-    p1 = specv.plan(1, 4, 1000, specv.F32)
-    assert p1["kernel"] == "rows-sweep" and p1["ctas"] == 5
-    with pytest.raises(specv.SpecvError):
-        specv.plan(3, 2, 1001, specv.F32)
-
-
 def test_plan_greedy_mode(lib, monkeypatch):
     """Greedy verification (mode 2) never samples: short aligned rows use the
     TMA tile kernel, everything else the streaming row kernel with the position
@@ -121,10 +100,9 @@ def test_plan_greedy_mode(lib, monkeypatch):
     assert p4["early_exit"]
     # short rows off 16-byte boundaries: the streaming row kernel, not the generic tile
     assert specv.plan(5, 3, 33, specv.F32, specv.GREEDY)["kernel"] == "rows-stream"
-    for v in ("resident", "spec", "sweep"):
-        monkeypatch.setenv("SPECV_ROWS_VARIANT", v)
-        with pytest.raises(specv.SpecvError):
-            specv.plan(256, 8, 128256, specv.F32, specv.GREEDY)
+    monkeypatch.setenv("SPECV_ROWS_VARIANT", "resident")
+    with pytest.raises(specv.SpecvError):
+        specv.plan(256, 8, 128256, specv.F32, specv.GREEDY)
     monkeypatch.delenv("SPECV_ROWS_VARIANT")
     st = specv.raw_call("specv_verify_debug", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 0, 2,
                         FAKE, FAKE, None, None, None, None)
@@ -136,27 +114,13 @@ def test_plan_cluster_size_model(lib):
     workload keeps S = 2), waves x (slice + fixed cost) near one wave (192
     positions: S = 3 fills one wave where S = 4 needs two)."""
     assert specv.plan(256, 8, 128256, specv.F32)["cluster"] == 2
+    assert specv.plan(256, 8, 128256, specv.F32, specv.GREEDY)["cluster"] == 2
     p3 = specv.plan(32, 5, 152064, specv.BF16)
     assert p3["kernel"] == "rows-stream" and p3["cluster"] == 3 and p3["ctas"] == 192 * 3
     assert specv.plan(32, 5, 152064, specv.BF16, specv.GREEDY)["cluster"] == 3
     for B, K, V, dt in [(16, 8, 128256, 0), (64, 4, 32000, 1), (8, 4, 128256, 1), (3, 2, 9000, 0)]:
         S = specv.plan(B, K, V, dt)["cluster"]
         assert 1 <= S <= 16
-
-
-def test_plan_ring_choice(lib, monkeypatch):
-    """The streaming row kernel takes the bulk-copy ring only when
-    SPECV_ROWS_RING=1 asks for it, and only for 16-byte aligned rows."""
-    monkeypatch.delenv("SPECV_ROWS_RING", raising=False)
-    for mode in (specv.PROB_MIX, specv.LOGIT_MIX, specv.GREEDY):
-        assert specv.plan(32, 5, 152064, specv.BF16, mode)["kernel"] == "rows-stream"
-    monkeypatch.setenv("SPECV_ROWS_RING", "1")
-    assert specv.plan(32, 5, 152064, specv.BF16)["kernel"] == "rows-ring"
-    assert specv.plan(256, 8, 128256, specv.F32)["kernel"] == "rows-ring"
-    assert specv.plan(256, 8, 128256, specv.F32, specv.GREEDY)["kernel"] == "rows-ring"
-    assert specv.plan(2, 4, 131071, specv.F32)["kernel"] == "rows-stream"  # unaligned rows
-    monkeypatch.setenv("SPECV_ROWS_RING", "0")
-    assert specv.plan(32, 5, 152064, specv.BF16, specv.GREEDY)["kernel"] == "rows-stream"
 
 
 def test_plan_early_exit(lib, monkeypatch):
@@ -176,6 +140,7 @@ def test_plan_early_exit(lib, monkeypatch):
     monkeypatch.setenv("SPECV_EARLY_EXIT", "0")
     p_off = specv.plan(256, 8, 128256, specv.F32)
     assert not p_off["early_exit"] and ws_on == p_off["workspace_bytes"] + 256 * 4
+    monkeypatch.delenv("SPECV_EARLY_EXIT")
     with pytest.raises(specv.SpecvError):
         specv.plan(0, 8, 128256, specv.F32)
 

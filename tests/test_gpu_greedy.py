@@ -1,11 +1,14 @@
-"""GPU parity of greedy verification (mode GREEDY) against the oracle.
+"""GPU parity of greedy verification (mode GREEDY) against the fp64 oracle.
 
-Greedy decisions are integers decided by fp32 comparisons that both sides make
-in the same precision (the mixed logit w = z_t + lambda (z_q - z_t) is formed
-with one rounded subtraction and one fused multiply-add), so the GPU must match
-the oracle bit for bit: every n_accepted and every emitted token, with no band.
-Ties go to the smallest index; inputs with many equal logits check that rule
-across threads, warps, CTAs and cluster ranks.
+The kernels form the mixed logit w = z_t + lambda (z_q - z_t) in fp32, the
+oracle (1 - lambda) z_t + lambda z_q in double precision.  Every sequence
+whose decided rows are farther from a tie than the band derived in
+tests/_parity.py (GREEDY_BAND, relative to the row's largest |logit|) must
+match bit for bit: n_accepted and every emitted token.  Near-ties are counted
+and the GPU's output there must be a valid greedy outcome (accepted drafts and
+the emitted token near-maxima of their rows, the bonus the exact argmax of
+target row K).  Exact ties go to the smallest index; inputs with many equal
+logits check that rule across threads, warps, CTAs and cluster ranks.
 """
 import ctypes
 import os
@@ -16,6 +19,7 @@ import torch
 
 import oracle
 import workloads
+from tests import _parity
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +37,7 @@ def specv():
 
 @pytest.fixture
 def env_guard():
-    keys = ("SPECV_CLUSTER_SIZE", "SPECV_ROWS_VARIANT", "SPECV_ROWS_RING")
+    keys = ("SPECV_CLUSTER_SIZE", "SPECV_ROWS_VARIANT")
     old = {k: os.environ.get(k) for k in keys}
     yield
     for k, v in old.items():
@@ -69,18 +73,17 @@ def _check(specv, x, seqs=None):
     tok, n = specv.verify(*args, mode=specv.GREEDY)
     torch.cuda.synchronize()
     tok, n = tok.cpu().numpy(), n.cpu().numpy()
+    xh = _parity.to_host(x)
     if seqs is None:
-        orc = oracle.verify_greedy(x["target_logits"], x["draft_logits"], x["draft_tokens"],
-                                   x["lam"])
-        np.testing.assert_array_equal(n, orc.n_accepted)
-        np.testing.assert_array_equal(tok, orc.tokens)
+        orc = oracle.verify_greedy(xh["target_logits"], xh["draft_logits"], xh["draft_tokens"],
+                                   xh["lam"])
     else:
         idx = torch.as_tensor(seqs)
-        sub = {k: v.cpu().index_select(0, idx) for k, v in x.items()}
+        sub = {k: v.index_select(0, idx) for k, v in xh.items()}
         orc = oracle.verify_greedy(sub["target_logits"], sub["draft_logits"],
                                    sub["draft_tokens"], sub["lam"])
-        np.testing.assert_array_equal(n[seqs], orc.n_accepted)
-        np.testing.assert_array_equal(tok[seqs], orc.tokens)
+    rep = _parity.compare_greedy(xh, tok, n, orc, seqs=seqs)
+    print("greedy parity:", rep)
     return tok, n
 
 
@@ -131,14 +134,11 @@ def test_greedy_ragged_shapes(specv, shape, lam):
     _check(specv, x)
 
 
-@pytest.mark.parametrize("ring", ["0", "1"], ids=["loads", "ring"])
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 7, 8, 16])
-def test_greedy_every_cluster_size_with_ties(specv, env_guard, S, ring):
+def test_greedy_every_cluster_size_with_ties(specv, env_guard, S):
     """Integer logits in a small range: every row has many equal maxima, spread
-    over all ranks of the cluster; the first one in index order must win (with
-    register loads and with the bulk-copy ring)."""
+    over all ranks of the cluster; the first one in index order must win."""
     os.environ["SPECV_CLUSTER_SIZE"] = str(S)
-    os.environ["SPECV_ROWS_RING"] = ring
     B, K, V = 6, 3, 50000
     g = torch.Generator().manual_seed(100 + S)
     zt = torch.randint(-3, 4, (B, K + 1, V), generator=g).float()
@@ -149,7 +149,7 @@ def test_greedy_every_cluster_size_with_ties(specv, env_guard, S, ring):
          "u_resample": torch.rand((B,), generator=g).to(DEV),
          "lam": torch.tensor([0.0, 0.5, 0.25, 1.0, 0.0, 0.75], dtype=torch.float32, device=DEV)}
     p = specv.plan(B, K, V, 0, 2)
-    assert p["cluster"] == S and p["kernel"] == ("rows-ring" if ring == "1" else "rows-stream")
+    assert p["cluster"] == S and p["kernel"] == "rows-stream"
     x = _follow_argmax(x, frac=0.6, seed=S)
     _check(specv, x)
     # the all-equal row: the argmax is index 0

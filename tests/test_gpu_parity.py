@@ -31,7 +31,7 @@ def specv():
 
 @pytest.fixture
 def cluster_env():
-    keys = ("SPECV_CLUSTER_SIZE", "SPECV_ROWS_VARIANT", "SPECV_SAMPLE_SPLIT", "SPECV_ROWS_RING")
+    keys = ("SPECV_CLUSTER_SIZE", "SPECV_ROWS_VARIANT", "SPECV_SAMPLE_SPLIT", "SPECV_EARLY_EXIT")
     old = {k: os.environ.get(k) for k in keys}
     yield
     for k, v in old.items():
@@ -42,14 +42,8 @@ def cluster_env():
 
 
 def _set_variant(variant):
-    """Force a row kernel: "stream" (register loads), "ring" (the streaming
-    kernel fed by the bulk-copy ring), "resident" or "spec"."""
-    if variant in ("stream", "ring"):
-        os.environ["SPECV_ROWS_VARIANT"] = "stream"
-        os.environ["SPECV_ROWS_RING"] = "1" if variant == "ring" else "0"
-    else:
-        os.environ["SPECV_ROWS_VARIANT"] = variant
-        os.environ.pop("SPECV_ROWS_RING", None)
+    """Force a row kernel: "stream" (the streaming kernel) or "resident"."""
+    os.environ["SPECV_ROWS_VARIANT"] = variant
 
 
 def _run(specv, x, mode, debug=True):
@@ -137,7 +131,7 @@ def test_parity_full_size_exactness_workload(specv, mode):
 
 
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 6, 8, 15, 16])
-@pytest.mark.parametrize("variant", ["stream", "ring", "resident", "spec"])
+@pytest.mark.parametrize("variant", ["stream", "resident"])
 def test_every_cluster_size(specv, cluster_env, variant, S):
     os.environ["SPECV_CLUSTER_SIZE"] = str(S)
     _set_variant(variant)
@@ -161,38 +155,33 @@ def test_every_cluster_size(specv, cluster_env, variant, S):
 
 @pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
 @pytest.mark.parametrize("cfg", [2, 3, 4])
-@pytest.mark.parametrize("variant", ["stream", "ring", "spec"])
-def test_row_variants_on_workloads(specv, cluster_env, variant, cfg, mode):
-    _set_variant(variant)
+def test_streaming_kernel_on_workloads(specv, cluster_env, cfg, mode):
+    _set_variant("stream")
     w = SMALL[cfg]
     x = workloads.make_inputs(w, DEV)
-    assert specv.plan(w.B, w.K, w.V, 1 if w.dtype == "bf16" else 0)["kernel"] == "rows-" + variant
+    assert specv.plan(w.B, w.K, w.V, 1 if w.dtype == "bf16" else 0)["kernel"] == "rows-stream"
     rep, _, _ = _check(specv, x, mode)
-    print(f"{variant} variant, workload {cfg}: {rep}")
+    print(f"streaming kernel, workload {cfg}: {rep}")
 
 
-@pytest.mark.parametrize("variant", ["stream", "ring"])
 @pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
 @pytest.mark.parametrize("V,dt", [(300000, "f32"), (300001, "f32"), (600000, "bf16")])
-def test_long_slices_multi_tile_segments(specv, cluster_env, V, dt, mode, variant):
+def test_long_slices_multi_tile_segments(specv, cluster_env, V, dt, mode):
     """One CTA per row and slices of 75000 groups: more groups than the sampler's
     segment table holds in single tiles, so every segment spans two tiles.  Half
     the sequences accept every draft (bonus rows sampled from the segment
     statistics of the first pass), the rest reject (residual walk)."""
     os.environ["SPECV_CLUSTER_SIZE"] = "1"
-    _set_variant(variant)
+    _set_variant("stream")
     w = workloads.Workload("long-slices", 6, 3, V, dt, "half_equal:3.0:0.85:1.0", (0.2,), 11)
     plan = specv.plan(w.B, w.K, w.V, 1 if dt == "bf16" else 0, mode)
-    aligned = V * (2 if dt == "bf16" else 4) % 16 == 0  # the ring takes 16-byte aligned rows
-    expect = "rows-ring" if variant == "ring" and aligned else "rows-stream"
-    assert plan["kernel"] == expect and plan["cluster"] == 1
+    assert plan["kernel"] == "rows-stream" and plan["cluster"] == 1
     x = workloads.make_inputs(w, DEV)
     rep, _, n = _check(specv, x, mode)
     assert (n == w.K).any() and (n < w.K).any()
     print(f"V={V} {dt} mode={mode}: {rep}")
 
 
-@pytest.mark.parametrize("variant", ["stream", "ring"])
 @pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
 @pytest.mark.parametrize("split", ["0", "1"], ids=["fused", "split"])
 @pytest.mark.parametrize("shape", [(8, 5, 152064, "bf16", "rho:3.0:0.5:0.95"),
@@ -201,12 +190,11 @@ def test_long_slices_multi_tile_segments(specv, cluster_env, V, dt, mode, varian
                                    (3, 33, 515, "bf16", "corr:3.0:0.9:0.7"),
                                    (6, 4, 300001, "f32", "half_equal:3.0:0.85:1.0")],
                          ids=lambda s: f"B{s[0]}K{s[1]}V{s[2]}{s[3]}")
-def test_token_draws_in_one_or_two_launches(specv, cluster_env, shape, split, mode, variant):
+def test_token_draws_in_one_or_two_launches(specv, cluster_env, shape, split, mode):
     """The streaming kernel's token draws in the statistics launch (fused) or in
     a second launch with a wider cluster per sequence (split): both give the
-    oracle's decisions, bonus rows included; with register loads or the
-    bulk-copy ring (which only takes 16-byte aligned rows)."""
-    _set_variant(variant)
+    oracle's decisions, bonus rows included."""
+    _set_variant("stream")
     os.environ["SPECV_SAMPLE_SPLIT"] = split
     B, K, V, dt, st = shape
     w = workloads.Workload("split", B, K, V, dt, st, (0.3,), 17)

@@ -14,6 +14,7 @@ import torch
 
 import oracle
 import workloads
+from tests import _parity
 
 pytestmark = pytest.mark.gpu
 
@@ -50,30 +51,7 @@ def _check(specv, x, mode):
     torch.cuda.synchronize()
     tok, path, n = tok.cpu().numpy(), path.cpu().numpy(), n.cpu().numpy()
     orc = oracle.verify_tree(*[v.cpu() for v in _args(x)], mode=mode)
-    par = x["parent"].cpu().numpy()
-    ntok = x["tokens"].cpu().numpy()
-    V = x["target_logits"].shape[-1]
-    near = 0
-    for b in range(n.shape[0]):
-        on = int(orc.n_accepted[b])
-        if on == -1:
-            assert n[b] == -1 and (tok[b] == -1).all() and (path[b] == -1).all(), b
-            continue
-        if orc.accept_margin[b] >= BAND and orc.cdf_margin[b] >= BAND:
-            assert n[b] == on, (b, n[b], on)
-            np.testing.assert_array_equal(tok[b], orc.tokens[b])
-            np.testing.assert_array_equal(path[b], orc.path[b])
-            continue
-        near += 1  # a boundary case: the GPU's walk must still be valid
-        k = int(n[b])
-        assert 0 <= k <= par.shape[1] - 1
-        prev = 0
-        for j in range(k):
-            c = int(path[b, j])
-            assert par[b, c] == prev and tok[b, j] == ntok[b, c]
-            prev = c
-        assert 0 <= tok[b, k] < V
-        assert (tok[b, k + 1:] == -1).all() and (path[b, k:] == -1).all()
+    _, near = _parity.compare_tree({k: v.cpu() for k, v in x.items()}, tok, path, n, orc)
     return n, near
 
 

@@ -170,3 +170,79 @@ def test_full_size_batched_fp32(specv):
     orc = _parity.run_oracle(h, 0, seqs)
     _parity.compare(h, 0, tok, n, orc, seqs)
     assert len(differ) <= 4, differ
+
+
+def _early_exit_run(specv, h, mode):
+    tok, n, h2d, d2h = specv.verify_host_early_exit(*(h[k] for k in KEYS), mode=mode)
+    torch.cuda.synchronize()
+    K = h["draft_tokens"].shape[1]
+    B = h["draft_tokens"].shape[0]
+    assert B * (K + 2) * 4 <= d2h <= B * (K + 2) * 4 + K * B  # outputs, then one flag byte a level
+    return tok.numpy().copy(), n.numpy().copy(), h2d
+
+
+EE_SHAPES = SHAPES + [(4, dict(B=24, K=8, V=128256)),   # half the batch drafts the target
+                      (3, dict(B=6))]                    # Qwen-shaped bf16 rows
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["prob", "logit", "greedy"])
+@pytest.mark.parametrize("shape", EE_SHAPES, ids=lambda s: f"w{s[0]}-" + "-".join(
+    f"{k}{v}" for k, v in s[1].items()))
+def test_early_exit_host_call_equals_device_verify(specv, shape, mode):
+    """specv_verify_host_early_exit copies position by position and stops at a
+    sequence's first clear rejection: its outputs equal specv_verify's bit for
+    bit (the rows it leaves out are never read for an output), it copies no
+    more than every row and at least every row the outputs depend on.  The
+    staging first holds another batch's rows (a call on other inputs), so the
+    rows left out are stale, not zero."""
+    cfg, kw = shape
+    w = workloads.WORKLOADS[cfg].scaled(**kw)
+    other = workloads.make_inputs(w, DEV, seed_offset=5)
+    _host_run(specv, _host(other), mode, chunks=1)  # stale rows in the staging
+    x = workloads.make_inputs(w, DEV)
+    ref_tok, ref_n = _device_ref(specv, x, mode)
+    tok, n, h2d = _early_exit_run(specv, _host(x), mode)
+    np.testing.assert_array_equal(n, ref_n)
+    np.testing.assert_array_equal(tok, ref_tok)
+    s = w.elem_bytes
+    every = (2 * w.K + 1) * w.B * w.V * s + 2 * w.B * w.K * 4 + 2 * w.B * 4
+    rows_needed = sum(2 * min(int(k) + 1, w.K) + (int(k) == w.K) for k in n)
+    assert rows_needed * w.V * s <= h2d <= every
+    print(f"{shape} mode={mode}: copied {h2d / every:.3f} of every row")
+
+
+def test_release_stream_frees_and_reallocates(specv):
+    """specv_release_stream frees a stream's scratch (grown twice, so with
+    superseded buffers) and staging; later calls on the stream allocate afresh
+    and give the same outputs.  Under capture it refuses."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    outs = []
+    for B in (4, 9, 17):  # the scratch grows
+        w = workloads.WORKLOADS[3].scaled(B=B)
+        x = workloads.make_inputs(w, DEV)
+        with torch.cuda.stream(s):
+            outs.append([t.clone() for t in specv.verify(*(x[k] for k in KEYS), stream=s)])
+    h = _host(x)
+    with torch.cuda.stream(s):
+        ref_h = specv.verify_host(*(h[k] for k in KEYS), chunks=1, stream=s)
+        s.synchronize()  # the host outputs are complete only once the stream is
+        ref_h = [t.clone() for t in ref_h]
+        specv.verify_host_early_exit(*(h[k] for k in KEYS), stream=s)
+    s.synchronize()
+    before = torch.cuda.mem_get_info()[0]
+    with torch.cuda.stream(s):
+        specv.release_stream(s)
+    after = torch.cuda.mem_get_info()[0]
+    assert after >= before  # the staging and scratch went back to the device
+    with torch.cuda.stream(s):
+        again = specv.verify(*(x[k] for k in KEYS), stream=s)
+        again_h = specv.verify_host(*(h[k] for k in KEYS), chunks=1, stream=s)
+    s.synchronize()
+    assert torch.equal(again[0], outs[-1][0]) and torch.equal(again[1], outs[-1][1])
+    assert torch.equal(again_h[0], ref_h[0]) and torch.equal(again_h[1], ref_h[1])
+    g = torch.cuda.CUDAGraph()
+    s2 = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s2):
+        st = specv.raw_call("specv_release_stream", s2.cuda_stream)
+    assert st == 2

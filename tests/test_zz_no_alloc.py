@@ -85,8 +85,32 @@ def test_noalloc_greedy_matches_specv_verify_exactly(lib, cfg):
         assert torch.equal(tok, ref_tok) and torch.equal(n, ref_n)
 
 
+@pytest.mark.parametrize("mode", [0, 2], ids=["prob", "greedy"])
+def test_noalloc_at_the_array_limit(lib, mode):
+    """B*(K+1) = 49152 positions, the most the array holds: the last
+    position's statistics end exactly where the counters begin.  Two calls in
+    a row, both against the oracle (exact outside the bands)."""
+    w = workloads.Workload("noalloc-limit", 6144, 7, 32, "f32", "corr:1.5:0.8:1.0", (0.3,), 31)
+    for call in range(2):
+        x = workloads.make_inputs(w, DEV, seed_offset=20 + call)
+        tok, n = _noalloc(lib, x, mode)
+        torch.cuda.synchronize()
+        xh = _parity.to_host(x)
+        tok, n = tok.cpu().numpy(), n.cpu().numpy()
+        if mode == 2:
+            import oracle
+            orc = oracle.verify_greedy(xh["target_logits"], xh["draft_logits"],
+                                       xh["draft_tokens"], xh["lam"])
+            _parity.compare_greedy(xh, tok, n, orc)
+        else:
+            _parity.compare(xh, mode, tok, n, _parity.run_oracle(xh, mode))
+
+
 def test_noalloc_rejects_sizes_beyond_its_array(lib):
     # B*(K+1) above the array's 49152 positions: refused before any launch
     null = None
     st = lib.specv_verify_noalloc(16, 16, 16, 16, 16, 16, 10000, 8, 32, 0, 0, 16, 16, null)
+    assert st == 1
+    # one position too many (3781 * 13 = 49153)
+    st = lib.specv_verify_noalloc(16, 16, 16, 16, 16, 16, 3781, 12, 32, 0, 0, 16, 16, null)
     assert st == 1
