@@ -774,7 +774,9 @@ def main():
         cpu = cpu_baseline(w, mode, args.cpu_seconds)
     per_config = None
     if not args.no_per_config and ws == 1 and args.B is None:
-        per_config = run_per_config(specv, dev, args, l2_bytes)
+        with ClockSampler(local) as pclk:
+            per_config = {"workloads": run_per_config(specv, dev, args, l2_bytes)}
+        per_config["clocks"] = pclk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,

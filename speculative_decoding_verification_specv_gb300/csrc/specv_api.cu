@@ -569,6 +569,7 @@ struct HostPipe {
   int dev;
   cudaStream_t stream;
   cudaStream_t copy;
+  cudaStream_t aux;        // the early-exit call's second decision stream
   cudaEvent_t start;
   cudaEvent_t ready[kHostMaxChunks];
   void *stage;
@@ -592,6 +593,7 @@ specv_status host_pipe(int dev, cudaStream_t stream, size_t need, HostPipe **out
     hp->dev = dev;
     hp->stream = stream;
     e = cudaStreamCreateWithFlags(&hp->copy, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->aux, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->start, cudaEventDisableTiming);
     for (int c = 0; c < kHostMaxChunks && e == cudaSuccess; ++c)
       e = cudaEventCreateWithFlags(&hp->ready[c], cudaEventDisableTiming);
@@ -606,6 +608,7 @@ specv_status host_pipe(int dev, cudaStream_t stream, size_t need, HostPipe **out
     // earlier calls on this pipe may still read or write the old staging
     e = cudaStreamSynchronize(stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(hp->copy);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(hp->aux);
     if (e == cudaSuccess && hp->stage != nullptr) e = cudaFree(hp->stage);
     if (e != cudaSuccess) {
       note_cuda_error(e);
@@ -896,6 +899,7 @@ specv_status verify_host_early_exit(const void *target, const void *draft, const
     if (hp->h_alive != nullptr) {  // no copy into it is pending, but drain the streams anyway
       (void)cudaStreamSynchronize(stream);
       (void)cudaStreamSynchronize(hp->copy);
+      (void)cudaStreamSynchronize(hp->aux);
       (void)cudaFreeHost(hp->h_alive);
     }
     hp->h_alive = nullptr;
@@ -915,16 +919,23 @@ specv_status verify_host_early_exit(const void *target, const void *draft, const
   const char *dft = static_cast<const char *>(draft);
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
   int64_t copied = (int64_t)(2 * bk4 + 2 * b4), read_back = (int64_t)(bk14 + b4);
-  // group 0 works on the caller's stream, group 1 on the library's copy stream
-  static_assert(kEeGroups >= 1 && kEeGroups <= 2, "one stream per group");
-  cudaStream_t gs[2] = {stream, hp->copy};
+  // Every host-to-device copy goes through one stream, in the order issued, so
+  // that the link carries one group's rows while another group's decision pass
+  // and read-back run (two copy streams would share the link and finish
+  // together); group 0 decides on the caller's stream, group 1 on a second
+  // stream of the pipe.  Events: ready[g] after group g's read-back, ready[2 + g]
+  // after group g's copies.
+  static_assert(kEeGroups >= 1 && kEeGroups <= 2, "one decision stream per group");
+  cudaStream_t cs = hp->copy;
+  cudaStream_t gs[2] = {stream, hp->aux};
   e = cudaMemcpyAsync(st + o_tok, tokens, bk4, h2d, stream);
   if (e == cudaSuccess) e = cudaMemcpyAsync(st + o_ua, ua, bk4, h2d, stream);
   if (e == cudaSuccess) e = cudaMemcpyAsync(st + o_ur, ur, b4, h2d, stream);
   if (e == cudaSuccess) e = cudaMemcpyAsync(st + o_lam, lam, b4, h2d, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(alive, 1, flags, stream);
-  // the other group's stream starts after these (and after earlier work on `stream`)
+  // the other streams start after these (and after earlier work on `stream`)
   if (e == cudaSuccess) e = cudaEventRecord(hp->start, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, hp->start, 0);
   for (int g = 1; g < kEeGroups && e == cudaSuccess; ++g) e = cudaStreamWaitEvent(gs[g], hp->start, 0);
   std::memset(h_alive, 1, flags);
 
@@ -957,11 +968,11 @@ specv_status verify_host_early_exit(const void *target, const void *draft, const
       const size_t h = (size_t)(j1 - j0);
       const int64_t b0 = g + (int64_t)kEeGroups * j0;
       const size_t ot = ((size_t)b0 * (K + 1) + lv) * row;
-      err = cudaMemcpy2DAsync(st + ot, tp, tgt + ot, tp, row, h, h2d, gs[g]);
+      err = cudaMemcpy2DAsync(st + ot, tp, tgt + ot, tp, row, h, h2d, cs);
       copied += (int64_t)(h * row);
       if (err == cudaSuccess && lv < K) {
         const size_t od = ((size_t)b0 * K + lv) * row;
-        err = cudaMemcpy2DAsync(st + o_d + od, dp, dft + od, dp, row, h, h2d, gs[g]);
+        err = cudaMemcpy2DAsync(st + o_d + od, dp, dft + od, dp, row, h, h2d, cs);
         copied += (int64_t)(h * row);
       }
       live += j1 - j0;
@@ -972,6 +983,9 @@ specv_status verify_host_early_exit(const void *target, const void *draft, const
       active[g] = false;
       return cudaSuccess;
     }
+    err = cudaEventRecord(hp->ready[2 + g], cs);  // the group's rows of this level are in
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(gs[g], hp->ready[2 + g], 0);
+    if (err != cudaSuccess) return err;
     specv::LevelArgs la;
     la.target = st;
     la.draft = st + o_d;
@@ -1013,7 +1027,9 @@ specv_status verify_host_early_exit(const void *target, const void *draft, const
       }
     }
   }
-  // the verify step on the staged batch once every group's copies are in
+  // the verify step on the staged batch once every copy is in
+  if (e == cudaSuccess) e = cudaEventRecord(hp->ready[4], cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, hp->ready[4], 0);
   for (int g = 1; g < kEeGroups && e == cudaSuccess; ++g) {
     e = cudaEventRecord(hp->ready[g], gs[g]);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, hp->ready[g], 0);
@@ -1373,6 +1389,7 @@ specv_status specv_release_stream(void *stream) {
         if (hp->stage) dev_bufs.push_back(hp->stage);
         if (hp->h_alive) host_bufs.push_back(hp->h_alive);
         copy_streams.push_back(hp->copy);
+        copy_streams.push_back(hp->aux);
         events.push_back(hp->start);
         for (int c = 0; c < kHostMaxChunks; ++c) events.push_back(hp->ready[c]);
         delete hp;

@@ -317,17 +317,19 @@ __device__ __forceinline__ float sample_weight(int mode, int kind, const SampleP
 // sample_weight without branches on `kind`: every candidate is computed and
 // one is selected, for warps whose lanes serve sequences of different kinds
 // (a bonus sequence next to a residual one).  Same values as sample_weight;
-// the candidates not selected may be non-finite and are discarded.
+// the candidates not selected may be non-finite and are discarded.  For the
+// bonus kind the caller passes zq = zt (there is no draft row at K + 1): the
+// mixed logit is then zt itself (mix_logit(zt, zt, l) == zt in every case,
+// masked entries included), so pa is the bonus weight in both modes.
 __device__ __forceinline__ float sample_weight_sel(int mode, int kind, const SampleParams &p,
                                                    float zt, float zq) {
   const float a = (mode == kProbMix) ? zt : mix_logit(zt, zq, p.lam);
   const float pa = prob_from_offset(a, p.nA);
   const float pq = prob_from_offset(zq, p.nB);
-  const float bonus = (mode == kProbMix) ? pa : prob_from_offset(zt, p.nA);
   const float resid = fmaxf(0.0f, __fsub_rn(pa, pq));
   const float mixed =
       (mode == kProbMix) ? __fmaf_rn(p.lam, pq, __fmul_rn(__fsub_rn(1.0f, p.lam), pa)) : pa;
-  return kind == kWBonus ? bonus : (kind == kWResidual ? resid : mixed);
+  return kind == kWBonus ? pa : (kind == kWResidual ? resid : mixed);
 }
 
 }  // namespace specv

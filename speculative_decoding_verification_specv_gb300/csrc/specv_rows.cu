@@ -322,17 +322,15 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   // from now on; it waits for this whole grid to complete before it reads
   // anything this grid writes.
   if (a.defer_sampling) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // The inputs of this position's own acceptance test, loaded now so that
-  // their latency hides behind the stream (rank 0's thread 0 decides).
+  // The inputs of this position's own acceptance test (rank 0's thread 0
+  // decides): the drafted token and its uniform now, so that their latency
+  // hides behind the stream; the two logits at the token right after it.
   int x_own = -1;
   float u_own = 0.0f, zt_own = 0.0f, zq_own = 0.0f;
-  if (rank == 0 && threadIdx.x == 0 && pair && !skip) {
+  const bool decides = rank == 0 && threadIdx.x == 0 && pair && !skip;
+  if (decides) {
     x_own = a.tokens[b * K + i];
     u_own = a.u_accept[b * K + i];
-    if (x_own >= 0 && x_own < V) {
-      zt_own = Elem<T>::load(rowA + x_own);
-      zq_own = Elem<T>::load(rowB + x_own);
-    }
   }
 
   // ---------------------------------------------------------------- phase 1
@@ -350,6 +348,10 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
         rowA, rowB, pair, lam_seq, V, g_lo, g_hi, mA, sA, mB, sB,
         a.ws_reject != nullptr ? &a.ws_reject[b] : nullptr, i, K);
     skip = stopped;
+  }
+  if (decides && x_own >= 0 && x_own < V) {  // in flight during the merges below
+    zt_own = Elem<T>::load(rowA + x_own);
+    zq_own = Elem<T>::load(rowB + x_own);
   }
   if (a.ws_reject != nullptr) skip = __syncthreads_or(skip) != 0;  // CTA-wide: partial statistics
   block_merge_stats<kNT>(sh.bs, mA, sA, mB, sB);
