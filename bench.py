@@ -63,9 +63,10 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every step from the host instead of replaying a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-api", default="early-exit", choices=["early-exit", "chunked"],
-                    help="host-buffer call of the e2e leg: specv_verify_host_early_exit (copies "
-                         "the rows the step reaches) or specv_verify_host (copies every row)")
+    ap.add_argument("--e2e-api", default="direct", choices=["direct", "early-exit", "chunked"],
+                    help="host-buffer call of the e2e leg: specv_verify_host_direct (kernels read "
+                         "the pinned inputs in place), specv_verify_host_early_exit (copies the "
+                         "rows the step reaches) or specv_verify_host (copies every row)")
     ap.add_argument("--e2e-chunks", type=int, default=0,
                     help="chunks of the host-buffer call (0 = the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -684,7 +685,13 @@ def main():
 
         def e2e_step():
             # one C-ABI call on host buffers, then the results back to the host
-            if args.e2e_api == "early-exit":
+            if args.e2e_api == "direct":
+                # the kernels read the page-locked inputs over the host link in place
+                specv.verify_host_direct(
+                    host["target_logits"], host["draft_logits"], host["draft_tokens"],
+                    host["u_accept"], host["u_resample"], host["lam"], mode=mode,
+                    out_tokens=host_tok, out_n_accepted=host_n, stream=stream)
+            elif args.e2e_api == "early-exit":
                 # position by position, only the rows the verify step reaches
                 _, _, link["h2d"], link["d2h"] = specv.verify_host_early_exit(
                     host["target_logits"], host["draft_logits"], host["draft_tokens"],
@@ -712,14 +719,28 @@ def main():
         torch.cuda.synchronize(dev)
         barrier()
         e_ms = max_over_ranks(a.elapsed_time(b), ws, dev)
+        if args.e2e_api == "direct":
+            # what crosses the host link: the per-sequence arrays and the rows
+            # the outputs depend on (the token draws read their rows a second
+            # time from a device copy the stream fills); left out: the part of
+            # a position streamed before an earlier rejection of its sequence
+            # was published.  The outputs are written in place.
+            n_h = host_n.to(torch.int64)
+            link["h2d"] = (needed_bytes(n_h, w.K, w.V, w.elem_bytes) +
+                           sum(host[k].numel() * host[k].element_size()
+                               for k in ("draft_tokens", "u_accept", "u_resample", "lam")))
+            link["d2h"] = d2h
         e2e = {"value": job_throughput(rows_per_step, e_steps, ws, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": link["h2d"], "d2h_bytes_per_step": link["d2h"],
                "every_row_h2d_bytes": h2d, "steps": e_steps, "ms_per_step": e_ms / e_steps,
-               "api": ("specv_verify_host_early_exit (pinned host buffers; rows copied "
-                       "position by position up to each sequence's first rejection)"
-                       if args.e2e_api == "early-exit" else
-                       "specv_verify_host (pinned host buffers, chunks="
-                       f"{args.e2e_chunks or 'auto'})")}
+               "api": {"direct": "specv_verify_host_direct (pinned host buffers read and "
+                                 "written in place by the kernels over the host link; only "
+                                 "the rows the step reaches cross it)",
+                       "early-exit": "specv_verify_host_early_exit (pinned host buffers; rows "
+                                     "copied position by position up to each sequence's "
+                                     "first rejection)",
+                       "chunked": "specv_verify_host (pinned host buffers, chunks="
+                                  f"{args.e2e_chunks or 'auto'})"}[args.e2e_api]}
         del host
 
     if rank != 0:

@@ -149,6 +149,34 @@ specv_status specv_verify_host(const void *target_logits, const void *draft_logi
                                int32_t *out_n_accepted, int32_t chunks, void *stream);
 
 /*
+ * specv_verify_host_direct -- specv_verify on inputs and outputs in host
+ * memory that the device reads and writes in place: the kernels load the rows
+ * they reach straight over the host link, so only those rows cross it (the
+ * pages' loop stops at the first rejection -- RAPID explainer, "3) 候选验证机制
+ * （伪代码）" -- and on batches of several waves positions after a published
+ * rejection read nothing), with no staging copy to wait for.
+ *
+ *   Arguments, layouts and results as specv_verify_host, without `chunks`.
+ *   Every buffer must be device-accessible: page-locked and mapped
+ *   (cudaHostAlloc, cudaHostRegister, or PyTorch's pin_memory), or ordinary
+ *   host memory on a device that reads pageable memory
+ *   (cudaDevAttrPageableMemoryAccess); device memory is accepted as well.
+ *
+ * Asynchronous on `stream` like specv_verify: the outputs are complete once the
+ * stream has completed.  The kernels that stage rows with bulk copies are not
+ * planned here (the register-load kernels read host memory the same way as
+ * device memory); results equal specv_verify's on the same plan.  Errors as
+ * specv_verify, and SPECV_ERR_UNSUPPORTED when a buffer is not
+ * device-accessible (nothing is launched).
+ */
+specv_status specv_verify_host_direct(const void *target_logits, const void *draft_logits,
+                                      const int32_t *draft_tokens, const float *u_accept,
+                                      const float *u_resample, const float *lambda, int64_t B,
+                                      int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,
+                                      int32_t *out_tokens, int32_t *out_n_accepted,
+                                      void *stream);
+
+/*
  * specv_verify_host_early_exit -- specv_verify_host that copies only the rows
  * the verify step reaches.  The pages' loop stops at the first rejection
  * (RAPID explainer, "3) 候选验证机制（伪代码）"; SD explainer, "修改的拒绝采样":

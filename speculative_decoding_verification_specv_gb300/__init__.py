@@ -99,6 +99,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.specv_verify_tree.argtypes = [vp] * 8 + [i64, i32, i32, i32, ctypes.c_int,
                                                      ctypes.c_int, vp, vp, vp, vp]
         lib.specv_verify_tree.restype = ctypes.c_int
+        lib.specv_verify_host_direct.argtypes = common + [vp]
+        lib.specv_verify_host_direct.restype = ctypes.c_int
         lib.specv_verify_host_early_exit.argtypes = common + [ctypes.POINTER(i64),
                                                               ctypes.POINTER(i64), vp]
         lib.specv_verify_host_early_exit.restype = ctypes.c_int
@@ -229,6 +231,26 @@ def verify_host(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
         _dtype_code(target_logits), int(mode), out_tokens.data_ptr(), out_n.data_ptr(),
         int(chunks), _stream_ptr(stream, dev))
     _check(st, "specv_verify_host")
+    return out_tokens, out_n
+
+
+def verify_host_direct(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lam,
+                       mode: int = PROB_MIX, out_tokens=None, out_n_accepted=None, stream=None):
+    """verify() on host tensors that the GPU reads and writes in place (page-locked,
+    e.g. ``pin_memory()``): the kernels load only the rows they reach over the host
+    link.  Asynchronous on ``stream``; the outputs (page-locked ones allocated if
+    not given) are complete once it has completed."""
+    B, K, V, _, out_tokens, out_n = _args(target_logits, draft_logits, draft_tokens, u_accept,
+                                          u_resample, lam, mode, out_tokens, out_n_accepted,
+                                          host=True)
+    dev = stream.device if stream is not None else torch.device("cuda",
+                                                                torch.cuda.current_device())
+    st = load().specv_verify_host_direct(
+        target_logits.data_ptr(), draft_logits.data_ptr(), draft_tokens.data_ptr(),
+        u_accept.data_ptr(), u_resample.data_ptr(), lam.data_ptr(), B, K, V,
+        _dtype_code(target_logits), int(mode), out_tokens.data_ptr(), out_n.data_ptr(),
+        _stream_ptr(stream, dev))
+    _check(st, "specv_verify_host_direct")
     return out_tokens, out_n
 
 

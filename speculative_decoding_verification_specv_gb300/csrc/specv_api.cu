@@ -264,13 +264,14 @@ int variant_from_env() {
 //    per SM; otherwise the streaming row kernel runs.
 //  SPECV_CLUSTER_SIZE and SPECV_ROWS_VARIANT override the choices.
 specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int sms, int64_t l2,
-                       bool aligned, Plan *p) {
+                       bool aligned, Plan *p, bool allow_tma = true) {
   const int elem = dtype == SPECV_BF16 ? 2 : 4;
   std::memset(p, 0, sizeof(*p));
   const bool greedy = mode == SPECV_GREEDY;
   const int64_t seq_bytes = (int64_t)(2 * K + 1) * V * elem + (int64_t)(K + 1) * 16;
   const int64_t data_bytes0 = (int64_t)(2 * K + 1) * V * elem;
-  const bool tma0 = aligned && ((int64_t)V * elem) % 16 == 0 && data_bytes0 <= kTmaTileStageBytes;
+  const bool tma0 = allow_tma && aligned && ((int64_t)V * elem) % 16 == 0 &&
+                    data_bytes0 <= kTmaTileStageBytes;
   // greedy runs in the TMA tile kernel or the streaming row kernel only
   if (V <= kTileMaxV && seq_bytes * kTileMinSeqs + 64 <= kTileSmemBudget && (!greedy || tma0)) {
     const int64_t data_bytes = data_bytes0;
@@ -330,7 +331,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     }
     return SPECV_OK;
   }
-  const bool can_resident = aligned && (row_bytes % 16 == 0) && env_var != 1;
+  const bool can_resident = allow_tma && aligned && (row_bytes % 16 == 0) && env_var != 1;
   auto slice_smem = [&](int S) { return 2 * ((G + S - 1) / S) * 16; };
   int S = 0;
   int kernel = 1;
@@ -403,7 +404,8 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
 specv_status run(const void *target, const void *draft, const int32_t *tokens, const float *ua,
                  const float *ur, const float *lam, int64_t B, int32_t K, int32_t V,
                  specv_dtype dtype, specv_mode mode, int32_t *out_tokens, int32_t *out_n,
-                 float *dbg_ptilde, float *dbg_q, float *dbg_lse, void *stream_ptr) {
+                 float *dbg_ptilde, float *dbg_q, float *dbg_lse, void *stream_ptr,
+                 bool allow_tma = true, void *mirror_t = nullptr, void *mirror_d = nullptr) {
   if (!target || !draft || !tokens || !ua || !ur || !lam || !out_tokens || !out_n)
     return SPECV_ERR_INVALID_ARG;
   if (!sizes_ok(B, K, V, dtype, mode)) return SPECV_ERR_INVALID_ARG;
@@ -416,7 +418,7 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
   const bool aligned = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
                        ((int64_t)V * elem % 16 == 0);
   Plan p;
-  if ((s = make_plan(B, K, V, dtype, mode, sms, l2, aligned, &p)) != SPECV_OK) return s;
+  if ((s = make_plan(B, K, V, dtype, mode, sms, l2, aligned, &p, allow_tma)) != SPECV_OK) return s;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   cudaError_t e;
   if (p.kernel == 0 || p.kernel == 3) {
@@ -526,6 +528,10 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     if (p.early_exit && dbg_ptilde == nullptr && dbg_lse == nullptr) {
       a.ws_reject = cnt + B;
       a.pos_major = 1;
+    }
+    if (aligned && mirror_t != nullptr && mirror_d != nullptr && mode != SPECV_GREEDY) {
+      a.mirror_target = mirror_t;  // device copies of the rows streamed, for the token draws
+      a.mirror_draft = mirror_d;
     }
     a.stats_cluster = p.cluster;
     a.stats_groups_per_slice = p.groups_per_slice;
@@ -733,6 +739,95 @@ specv_status verify_host(const void *target, const void *draft, const int32_t *t
     return SPECV_ERR_CUDA;
   }
   return SPECV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Verify on host buffers that the device can read in place: the kernels load
+// the rows they reach straight from host memory over the host link, so only
+// those rows cross it (early exit skips the rest) and nothing waits for a
+// copy to finish.  The host link is about 30 times slower than HBM, so the
+// kernels spend most of the time waiting on it; the kernels that stage rows
+// with bulk copies (the resident and TMA tile kernels) are not planned, the
+// register-load kernels are.
+//
+// A host pointer qualifies when the runtime reports it page-locked and
+// mapped (cudaHostAlloc, cudaHostRegister: its device address is used), or
+// when it is ordinary host memory and the device reads pageable memory
+// (cudaDevAttrPageableMemoryAccess, e.g. over a coherent CPU-GPU link).
+bool device_address(const void *p, bool pageable_ok, const void **out) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return true;
+  }
+  if (at.type == cudaMemoryTypeHost && at.devicePointer != nullptr) {
+    // the same offset from the allocation's device address
+    *out = static_cast<const char *>(at.devicePointer) +
+           (static_cast<const char *>(p) - static_cast<const char *>(at.hostPointer));
+    return true;
+  }
+  if (at.type == cudaMemoryTypeUnregistered && pageable_ok) {
+    *out = p;
+    return true;
+  }
+  return false;
+}
+
+specv_status verify_host_direct(const void *target, const void *draft, const int32_t *tokens,
+                                const float *ua, const float *ur, const float *lam, int64_t B,
+                                int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,
+                                int32_t *out_tokens, int32_t *out_n, void *stream_ptr) {
+  if (!target || !draft || !tokens || !ua || !ur || !lam || !out_tokens || !out_n)
+    return SPECV_ERR_INVALID_ARG;
+  if (!sizes_ok(B, K, V, dtype, mode)) return SPECV_ERR_INVALID_ARG;
+  int sms = kDefaultSMs;
+  int64_t l2 = kDefaultL2;
+  specv_status s = ensure_device(&sms, &l2);
+  if (s != SPECV_OK) return s;
+  int dev = 0, pageable = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  const void *in[6] = {target, draft, tokens, ua, ur, lam};
+  const void *dv[6];
+  for (int k = 0; k < 6; ++k)
+    if (!device_address(in[k], pageable != 0, &dv[k])) return SPECV_ERR_UNSUPPORTED;
+  const void *dot = nullptr, *don = nullptr;
+  if (!device_address(out_tokens, pageable != 0, &dot) ||
+      !device_address(out_n, pageable != 0, &don))
+    return SPECV_ERR_UNSUPPORTED;
+  // Device copies of the rows as they stream (the streaming kernel's token
+  // draws read the rejected pair a second time, from HBM instead of across
+  // the link): the pipe's staging memory, laid out like the inputs.
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if ((e = cudaStreamIsCapturing(stream, &cap)) != cudaSuccess) {
+    note_cuda_error(e);
+    (void)cudaGetLastError();
+    return SPECV_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return SPECV_ERR_UNSUPPORTED;  // staging may grow
+  const size_t elem = dtype == SPECV_BF16 ? 2 : 4;
+  if ((uint64_t)B * (uint64_t)(2 * K + 1) > ((uint64_t)1 << 50) / elem / (uint64_t)V)
+    return SPECV_ERR_NO_MEMORY;
+  const size_t t_bytes = (size_t)B * (K + 1) * V * elem, d_bytes = (size_t)B * K * V * elem;
+  HostPipe *hp = nullptr;
+  if ((s = host_pipe(dev, stream, round256(t_bytes) + round256(d_bytes), &hp)) != SPECV_OK) return s;
+  char *mir = static_cast<char *>(hp->stage);
+  return run(dv[0], dv[1], static_cast<const int32_t *>(dv[2]), static_cast<const float *>(dv[3]),
+             static_cast<const float *>(dv[4]), static_cast<const float *>(dv[5]), B, K, V, dtype,
+             mode, static_cast<int32_t *>(const_cast<void *>(dot)),
+             static_cast<int32_t *>(const_cast<void *>(don)), nullptr, nullptr, nullptr,
+             stream_ptr, /*allow_tma=*/false, mir, mir + round256(t_bytes));
 }
 
 // ---------------------------------------------------------------------------
@@ -1088,6 +1183,17 @@ specv_status specv_verify_host(const void *target_logits, const void *draft_logi
   NvtxRange range("specv_verify_host");
   return verify_host(target_logits, draft_logits, draft_tokens, u_accept, u_resample, lambda, B,
                      K, V, dtype, mode, out_tokens, out_n_accepted, chunks, stream);
+}
+
+specv_status specv_verify_host_direct(const void *target_logits, const void *draft_logits,
+                                      const int32_t *draft_tokens, const float *u_accept,
+                                      const float *u_resample, const float *lambda, int64_t B,
+                                      int32_t K, int32_t V, specv_dtype dtype, specv_mode mode,
+                                      int32_t *out_tokens, int32_t *out_n_accepted,
+                                      void *stream) {
+  NvtxRange range("specv_verify_host_direct");
+  return verify_host_direct(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                            lambda, B, K, V, dtype, mode, out_tokens, out_n_accepted, stream);
 }
 
 specv_status specv_verify_host_early_exit(const void *target_logits, const void *draft_logits,

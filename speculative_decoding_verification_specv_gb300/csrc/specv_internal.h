@@ -98,6 +98,9 @@ struct RowArgs {
   unsigned *ws_reject = nullptr;  // optional scratch [B] (zero at entry, left zero): early exit.
                                   // K + 1 - j for the earliest position j whose own acceptance
                                   // test is known to reject; positions after it skip their rows
+  void *mirror_target = nullptr;  // optional device copies [B][K+1][V] / [B][K][V] (aligned
+  void *mirror_draft = nullptr;   // rows): the stream stores what it reads there, and the
+                                  // token draws read the rows back from them
   int pos_major = 0;         // 1: the grid runs position-major (all sequences' position 0, then
                              // position 1, ...), so that later positions of a sequence start
                              // after its earlier ones have published their decisions

@@ -73,6 +73,12 @@ struct __align__(16) RowsShared {
   float segi[kMaxSegs];   // running sums of segm in index order (inclusive)
 };
 
+// Row `r` of a device mirror (null when the launch has none).
+template <typename T>
+__device__ __forceinline__ T *mirror_row(void *mirror, int64_t r, int V) {
+  return mirror == nullptr ? nullptr : static_cast<T *>(mirror) + r * (int64_t)V;
+}
+
 // Phase 1 of the bonus row: (max, sum-exp) of every segment of this CTA's
 // slice, written to out[s] for s < nseg (an empty segment gives (-inf, 0)),
 // and merged into lane 0's running statistics (the other lanes keep theirs
@@ -80,7 +86,7 @@ struct __align__(16) RowsShared {
 // kSegLaneGroups coalesced 16-byte loads per lane.
 template <typename T, bool ALIGNED>
 __device__ void bonus_segment_stats(const T *row, int V, int g_lo, int g_hi, int seg_groups,
-                                    int nseg, float2 *out, float &mA, float &sA) {
+                                    int nseg, float2 *out, float &mA, float &sA, T *mir) {
   constexpr int VW = Elem<T>::kPerVec;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int s = warp; s < nseg; s += kNW) {
@@ -93,6 +99,8 @@ __device__ void bonus_segment_stats(const T *row, int V, int g_lo, int g_hi, int
       for (int u = 0; u < kSegLaneGroups; ++u) {
         const int g = g0 + u * 32 + lane;
         z[u] = g < sg_hi ? load_group<T, ALIGNED>(row, g, V) : neg_inf_group<T>();
+        if (ALIGNED && mir != nullptr && g < sg_hi)
+          __stcs(reinterpret_cast<uint4 *>(mir + (int64_t)g * Elem<T>::kPerVec), z[u]);
       }
       float bm = -INFINITY;
 #pragma unroll
@@ -283,7 +291,7 @@ __device__ __forceinline__ int residual_kind(float lam) {
   return !(lam < 1.0f) ? kWMixture : kWResidual;
 }
 
-template <typename T, int MODE, bool ALIGNED>
+template <typename T, int MODE, bool ALIGNED, bool MIRROR = false>
 __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   __shared__ RowsShared sh;
   cg::cluster_group cluster = cg::this_cluster();
@@ -340,13 +348,16 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   if (skip) {
     // nothing to read: a rejection before this position is already published
   } else if (!pair && a.ws_seg != nullptr) {
-    bonus_segment_stats<T, ALIGNED>(rowA, V, g_lo, g_hi, seg_groups, nseg,
-                                    a.ws_seg + (b * S + rank) * (int64_t)nseg, mA, sA);
+    bonus_segment_stats<T, ALIGNED>(
+        rowA, V, g_lo, g_hi, seg_groups, nseg, a.ws_seg + (b * S + rank) * (int64_t)nseg, mA, sA,
+        MIRROR ? mirror_row<T>(a.mirror_target, b * (K + 1) + i, V) : nullptr);
   } else {
     // with early exit the stream stops when an earlier rejection is published meanwhile
     const bool stopped = slice_stats<T, MODE, ALIGNED, kNT, kUnroll>(
         rowA, rowB, pair, lam_seq, V, g_lo, g_hi, mA, sA, mB, sB,
-        a.ws_reject != nullptr ? &a.ws_reject[b] : nullptr, i, K);
+        a.ws_reject != nullptr ? &a.ws_reject[b] : nullptr, i, K,
+        MIRROR ? mirror_row<T>(a.mirror_target, b * (K + 1) + i, V) : nullptr,
+        MIRROR ? mirror_row<T>(a.mirror_draft, b * K + (pair ? i : 0), V) : nullptr);
     skip = stopped;
   }
   if (decides && x_own >= 0 && x_own < V) {  // in flight during the merges below
@@ -438,8 +449,11 @@ __global__ void __launch_bounds__(kNT, 4) rows_kernel(RowArgs a) {
   cluster.sync();  // broadcast visible everywhere
   const Broadcast bc = sh.bc;
   if (bc.n < 0) return;
-  const T *sA_row = tgt + (b * (K + 1) + bc.n) * (int64_t)V;
-  const T *sB_row = dft + (b * K + (bc.n < K ? bc.n : 0)) * (int64_t)V;
+  // the second read of the rows: from the device mirror when there is one
+  const T *tsrc = MIRROR ? static_cast<const T *>(a.mirror_target) : tgt;
+  const T *dsrc = MIRROR ? static_cast<const T *>(a.mirror_draft) : dft;
+  const T *sA_row = tsrc + (b * (K + 1) + bc.n) * (int64_t)V;
+  const T *sB_row = dsrc + (b * K + (bc.n < K ? bc.n : 0)) * (int64_t)V;
   if (bc.kind == kWBonus && a.ws_seg != nullptr) {
     // every draft accepted: the bonus row's segment statistics are in the workspace
     if (rank != 0) return;
@@ -477,8 +491,10 @@ __global__ void __launch_bounds__(kNT, 4) rows_sample_kernel(RowArgs a) {
   const float u = a.u_resample[b];
   const T *tgt = static_cast<const T *>(a.target);
   const T *dft = static_cast<const T *>(a.draft);
-  const T *sA_row = tgt + (b * (K + 1) + n) * (int64_t)V;
-  const T *sB_row = dft + (b * K + (n < K ? n : 0)) * (int64_t)V;
+  const T *tsrc = a.mirror_target != nullptr ? static_cast<const T *>(a.mirror_target) : tgt;
+  const T *dsrc = a.mirror_draft != nullptr ? static_cast<const T *>(a.mirror_draft) : dft;
+  const T *sA_row = tsrc + (b * (K + 1) + n) * (int64_t)V;
+  const T *sB_row = dsrc + (b * K + (n < K ? n : 0)) * (int64_t)V;
   int32_t *out = a.out_tokens + b * (K + 1) + n;
   if (kind == kWBonus && a.ws_seg != nullptr) {
     if (rank != 0) return;
@@ -625,17 +641,21 @@ __global__ void __launch_bounds__(kNT, 4) rows_greedy_kernel(RowArgs a) {
   if (lane == 0) a.out_n[b] = valid ? n : -1;
 }
 
-template <typename T, int MODE, bool ALIGNED>
+template <typename T, int MODE, bool ALIGNED, bool MIRROR = false>
 constexpr void (*row_kernel_of())(RowArgs) {
   if constexpr (MODE == kGreedy)
     return rows_greedy_kernel<T, ALIGNED>;
   else
-    return rows_kernel<T, MODE, ALIGNED>;
+    return rows_kernel<T, MODE, ALIGNED, MIRROR>;
 }
 
 template <typename T, int MODE, bool ALIGNED>
 cudaError_t launch_one(const RowArgs &a, int S, int64_t grid, cudaStream_t stream) {
-  void (*kern)(RowArgs) = row_kernel_of<T, MODE, ALIGNED>();
+  // the mirrored variant (aligned sampling rows with device copies to fill)
+  constexpr bool kCanMirror = ALIGNED && MODE != kGreedy;
+  void (*kern)(RowArgs) = (kCanMirror && a.mirror_target != nullptr)
+                              ? row_kernel_of<T, MODE, ALIGNED, kCanMirror>()
+                              : row_kernel_of<T, MODE, ALIGNED>();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kNT, 1, 1);
@@ -676,6 +696,11 @@ template <typename T, int MODE, bool ALIGNED>
 cudaError_t prepare_one() {
   cudaError_t e = cudaFuncSetAttribute(row_kernel_of<T, MODE, ALIGNED>(),
                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if constexpr (ALIGNED && MODE != kGreedy) {
+    const cudaError_t e1 = cudaFuncSetAttribute(row_kernel_of<T, MODE, true, true>(),
+                                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) e = e1;
+  }
   if constexpr (MODE != kGreedy) {
     const cudaError_t e2 = cudaFuncSetAttribute(rows_sample_kernel<T, MODE, ALIGNED>,
                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);

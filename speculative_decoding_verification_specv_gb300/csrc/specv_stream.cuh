@@ -124,12 +124,15 @@ constexpr int kExitEvery = 1;
 
 // Returns true if the thread stopped early (its statistics are then partial:
 // the position lies after the sequence's first rejection and is never used).
+// With mirA / mirB set (aligned rows only), every group streamed is also
+// stored there, at the same index: a device copy of the rows for a second
+// read when the rows themselves sit across a slow link.
 template <typename T, int MODE, bool ALIGNED, int NT, int U>
 __device__ __forceinline__ bool slice_stats(const T *rowA, const T *rowB, bool pair, float lam,
                                             int V, int g_lo, int g_hi, float &mA, float &sA,
                                             float &mB, float &sB,
                                             const unsigned *exit_word = nullptr, int pos = 0,
-                                            int K = 0) {
+                                            int K = 0, T *mirA = nullptr, T *mirB = nullptr) {
   unsigned seen = 0u;
   int it = 0;
   for (int g0 = g_lo + (int)threadIdx.x; g0 < g_hi; g0 += NT * U, ++it) {
@@ -147,6 +150,16 @@ __device__ __forceinline__ bool slice_stats(const T *rowA, const T *rowB, bool p
         za[u] = load_group<T, ALIGNED>(rowA, g, V);
         if (pair) zb[u] = load_group<T, ALIGNED>(rowB, g, V);
       }
+    }
+    if (ALIGNED && mirA != nullptr) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (ok[u]) {
+          const int g = g0 + u * NT;
+          constexpr int VW = Elem<T>::kPerVec;
+          __stcs(reinterpret_cast<uint4 *>(mirA + (int64_t)g * VW), za[u]);
+          if (pair) __stcs(reinterpret_cast<uint4 *>(mirB + (int64_t)g * VW), zb[u]);
+        }
     }
     fold_batch<T, MODE, U>(za, zb, ok, pair, lam, mA, sA, mB, sB);
   }

@@ -246,3 +246,61 @@ def test_release_stream_frees_and_reallocates(specv):
     with torch.cuda.graph(g, stream=s2):
         st = specv.raw_call("specv_release_stream", s2.cuda_stream)
     assert st == 2
+
+
+DIRECT_SHAPES = [
+    (4, dict(B=24, K=8, V=128256), True),   # streaming kernel in both calls: bit-equal
+    (3, dict(B=8), True),
+    (1, dict(B=9, K=3, V=33), True),        # rows off 16-byte boundaries: generic tile kernel
+    (5, dict(B=3000), False),               # short rows: no TMA tile kernel on host memory
+    (2, dict(), False),                     # B = 1: no resident (TMA-staged) kernel either
+]
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["prob", "logit", "greedy"])
+@pytest.mark.parametrize("shape", DIRECT_SHAPES, ids=lambda s: f"w{s[0]}-" + "-".join(
+    f"{k}{v}" for k, v in s[1].items()))
+def test_direct_host_call(specv, shape, mode):
+    """specv_verify_host_direct: the kernels read the page-locked host inputs
+    and write the host outputs in place.  Where the device call plans the same
+    kernel the outputs are equal bit for bit; elsewhere (the kernels that stage
+    rows by bulk copy are not planned on host memory) they agree with the
+    oracle outside the decision band."""
+    cfg, kw, same_plan = shape
+    w = workloads.WORKLOADS[cfg].scaled(**kw)
+    x = workloads.make_inputs(w, DEV)
+    h = _host(x)
+    tok, n = specv.verify_host_direct(*(h[k] for k in KEYS), mode=mode)
+    torch.cuda.synchronize()
+    tok, n = tok.numpy().copy(), n.numpy().copy()
+    if same_plan:
+        ref_tok, ref_n = _device_ref(specv, x, mode)
+        np.testing.assert_array_equal(n, ref_n)
+        np.testing.assert_array_equal(tok, ref_tok)
+    xh = _parity.to_host(x)
+    if mode == 2:
+        import oracle
+        orc = oracle.verify_greedy(xh["target_logits"], xh["draft_logits"], xh["draft_tokens"],
+                                   xh["lam"])
+        _parity.compare_greedy(xh, tok, n, orc)
+    else:
+        _parity.compare(xh, mode, tok, n, _parity.run_oracle(xh, mode))
+
+
+def test_direct_host_call_pageable_or_refused(specv):
+    """Pageable host tensors: read in place where the device reads pageable
+    memory, refused with SPECV_ERR_UNSUPPORTED (nothing launched) elsewhere."""
+    w = workloads.WORKLOADS[3].scaled(B=4)
+    x = workloads.make_inputs(w, DEV)
+    h = _host(x, pinned=False)
+    ref_tok, ref_n = _device_ref(specv, x, 0)
+    out_t = torch.empty((w.B, w.K + 1), dtype=torch.int32)
+    out_n = torch.empty((w.B,), dtype=torch.int32)
+    try:
+        specv.verify_host_direct(*(h[k] for k in KEYS), out_tokens=out_t, out_n_accepted=out_n)
+    except specv.SpecvError as e:
+        assert e.status == 2
+        return
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out_n.numpy(), ref_n)
+    np.testing.assert_array_equal(out_t.numpy(), ref_tok)
