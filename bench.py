@@ -138,7 +138,8 @@ def job_throughput(rows_per_step, steps, ws, slowest_ms):
 
 # kernel function timed for the roofline, by the planner's kernel name
 PLAN_KERNEL_FUNCTION = {"tile": "tile_kernel", "rows-stream": "rows_kernel",
-                        "rows-resident": "resident_kernel", "tile-tma": "tile_tma_kernel"}
+                        "rows-resident": "resident_kernel", "tile-tma": "tile_tma_kernel",
+                        "rows-seq": "rows_seq_kernel"}
 
 
 def measured_peak():

@@ -283,10 +283,14 @@ specv_status specv_verify_debug(const void *target_logits, const void *draft_log
  *            memory by TMA; chosen when rows start on 16-byte boundaries and
  *            a slice fits shared memory, and the grid is a single wave),
  *            3 = small-vocabulary tile kernel with TMA-staged, double-buffered
- *            tiles (16-byte aligned rows).
+ *            tiles (16-byte aligned rows), 4 = sequence-cluster row kernel (one
+ *            cluster of 16 CTAs per sequence streams every position, decides
+ *            it and draws its token in one launch with no workspace; sampling
+ *            rules, device memory, grids of one wave of 2 to 4 CTAs per SM).
  *            For tests, the environment variable SPECV_ROWS_VARIANT=stream or
  *            =resident forces kernel 1 or 2, and SPECV_CLUSTER_SIZE=1..16
- *            forces the cluster size of the row kernels.
+ *            forces the cluster size of the row kernels (either one, or
+ *            SPECV_SAMPLE_SPLIT, rules out kernel 4).
  *   cluster: CTAs per thread-block cluster splitting each row (1 for kernel 0)
  *   ctas:    CTAs launched by a row kernel; tiles of sequences for kernels 0, 3
  *   workspace_bytes: scratch bytes of the row kernels' workspace (kept per

@@ -438,7 +438,7 @@ class AdaptiveK:
 
 
 # specv_plan's kernel codes
-KERNEL_NAMES = {0: "tile", 1: "rows-stream", 2: "rows-resident", 3: "tile-tma"}
+KERNEL_NAMES = {0: "tile", 1: "rows-stream", 2: "rows-resident", 3: "tile-tma", 4: "rows-seq"}
 
 
 def plan(B: int, K: int, V: int, dtype: int = F32, mode: int = PROB_MIX) -> dict:

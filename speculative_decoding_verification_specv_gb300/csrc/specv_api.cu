@@ -189,7 +189,8 @@ specv_status ensure_device(int *sms_out, int64_t *l2_out) {
 }
 
 struct Plan {
-  int kernel;            // 0 tile, 1 streaming row kernel, 2 resident row kernel, 3 TMA tile
+  int kernel;            // 0 tile, 1 streaming row kernel, 2 resident row kernel, 3 TMA tile,
+                         // 4 sequence-cluster row kernel
   int cluster;           // CTAs per cluster (row kernels)
   int64_t ctas;          // CTAs of the row kernels (tile kernel: tiles)
   int64_t ws_bytes;      // scratch bytes
@@ -379,6 +380,30 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
     // waves keep the draws in the statistics launch, overlapped with streaming.
     const int env_split = split_from_env();
     const bool one_wave = P * S <= waves_slots;
+    // About one wave of few sequences: one cluster of 16 CTAs per sequence
+    // streams all its positions, decides it and draws its token in a single
+    // launch (no scratch, no second launch), when 16 CTAs per sequence fit
+    // one wave of 4 CTAs per SM and the clusters fill at least two CTAs per
+    // SM (measured on GB300 against the two-launch plan: 39.6 against 43.7 us
+    // at B = 32, K = 5, V = 152064 bf16; 41.6 against 49.8 us at B = 24,
+    // K = 6, V = 40001; but with more sequences on smaller clusters the
+    // two-launch plan wins: 33.4 against 27.3 us at B = 40, K = 3, V = 32000
+    // on clusters of 15).  Device memory only: a forced variant, cluster size
+    // or draw split keeps the streaming kernel.
+    if (one_wave && allow_tma && env_split < 0 && env_var == 0 && env_S == 0) {
+      const int64_t sq = specv::kMaxCluster;
+      if (B * sq <= 4LL * sms && B * sq >= 2LL * sms && K + 1 <= specv::kSeqMaxPositions &&
+          row_bytes / sq >= 4096) {
+        p->kernel = 4;
+        p->cluster = (int)sq;
+        p->ctas = B * sq;
+        p->groups_per_slice = (int)((G + sq - 1) / sq);
+        specv::rows_segments(p->groups_per_slice, &p->seg_tiles, &p->segs_per_slice);
+        p->counters = 0;
+        p->ws_bytes = 0;
+        return SPECV_OK;
+      }
+    }
     p->split = env_split >= 0 ? env_split : (one_wave ? 1 : 0);
     if (p->split) {
       int64_t s2 = (2 * row_bytes + 48 * 1024 - 1) / (48 * 1024);
@@ -449,6 +474,37 @@ specv_status run(const void *target, const void *draft, const int32_t *tokens, c
     if (grid > p.ctas) grid = p.ctas;
     e = p.kernel == 3 ? specv::tile_tma_launch(a, bf16, mode, grid, p.smem_total, stream)
                       : specv::tile_launch(a, bf16, mode, grid, p.smem_total, stream);
+    if (e != cudaSuccess) {
+      note_cuda_error(e);
+      return SPECV_ERR_CUDA;
+    }
+    return SPECV_OK;
+  }
+  if (p.kernel == 4) {  // the sequence-cluster kernel: no scratch
+    specv::RowArgs a;
+    a.target = target;
+    a.draft = draft;
+    a.tokens = tokens;
+    a.u_accept = ua;
+    a.u_resample = ur;
+    a.lam = lam;
+    a.B = B;
+    a.K = K;
+    a.V = V;
+    a.out_tokens = out_tokens;
+    a.out_n = out_n;
+    a.ws_stats = nullptr;
+    a.ws_count = nullptr;
+    a.dbg_ptilde = dbg_ptilde;
+    a.dbg_q = dbg_q;
+    a.dbg_lse = dbg_lse;
+    a.groups_per_slice = p.groups_per_slice;
+    a.num_groups = p.num_groups;
+    a.seg_tiles = p.seg_tiles;
+    a.segs_per_slice = p.segs_per_slice;
+    a.ws_seg = nullptr;
+    a.defer_sampling = 0;
+    e = specv::rows_seq_launch(a, bf16, mode, aligned, p.cluster, stream);
     if (e != cudaSuccess) {
       note_cuda_error(e);
       return SPECV_ERR_CUDA;

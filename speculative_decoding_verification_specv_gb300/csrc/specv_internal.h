@@ -209,6 +209,13 @@ cudaError_t tree_launch(const TreeArgs &a, int dtype_bf16, int mode, bool aligne
 cudaError_t rows_prepare();
 cudaError_t rows_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
                         int64_t grid, cudaStream_t stream);
+// The sequence-cluster kernel: one cluster of S CTAs per sequence (grid B * S)
+// streams every position of its sequence, decides it and draws its token in
+// one launch (grids of about one wave); K + 1 <= kSeqMaxPositions, device
+// memory only (aligned rows are staged with asynchronous copies).
+constexpr int kSeqMaxPositions = 64;
+cudaError_t rows_seq_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
+                            cudaStream_t stream);
 // The deferred token draws: one cluster of S CTAs per sequence (grid B * S),
 // after a rows_launch with defer_sampling = 1 on the same stream.
 cudaError_t rows_sample_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,

@@ -512,6 +512,211 @@ __global__ void __launch_bounds__(kNT, 4) rows_sample_kernel(RowArgs a) {
                                a.seg_tiles * kSegGroups, a.segs_per_slice, kind, sp, u, out);
 }
 
+// One cluster per SEQUENCE (grid B * S; plan for grids of about one wave):
+// the CTAs of the cluster stream the sequence's rows (the target and draft
+// rows of positions 0..K-1, then target row K) in S contiguous parts and
+// push their partial statistics of every position into rank 0's shared
+// memory.  After one cluster barrier rank 0's first warp merges them (lane =
+// position), takes the acceptance tests (their inputs were loaded while the
+// rows streamed), finds the first rejection n and writes the outputs; the
+// token at n is then drawn by the whole cluster from its slices of row pair
+// n (or of target row K) -- the rows were streamed moments ago, so the second
+// read hits L2 -- with no second launch, no scratch memory and no arrival
+// counter.  Dynamic shared memory: the partials [K+1][S] of every rank (used
+// in rank 0), then the drafted tokens, acceptance uniforms and the resample
+// uniform of the sequence (copied in by rank 0's first warp).
+extern __shared__ float4 g_seq_smem[];
+
+// Work units of one group of a pair position against one group of the bonus
+// row: the bytes (2 : 1) in the probability rule; the logit rule's mixed row
+// costs about 1.6 times as much per byte (Qwen-shaped batch, B = 32, K = 5,
+// V = 152064 bf16, with 2 : 1: CTAs on pair positions streamed for 26.8 us
+// median, those on the bonus row 16.7 us, for equal bytes), hence 3 : 1.
+template <int MODE>
+constexpr int kSeqPairUnits = MODE == kLogitMix ? 3 : 2;
+
+__host__ __device__ constexpr int64_t seq_smem_bytes(int K, int S) {
+  return (int64_t)(K + 1) * S * 16 + (2 * kSeqMaxPositions + 4) * 4;
+}
+
+template <typename T, int MODE, bool ALIGNED>
+__global__ void __launch_bounds__(kNT, 4) rows_seq_kernel(RowArgs a) {
+  __shared__ RowsShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int S = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int64_t b = (int64_t)blockIdx.x / S;
+  const int K = a.K, V = a.V;
+  const T *tgt = static_cast<const T *>(a.target) + b * (K + 1) * (int64_t)V;
+  const T *dft = static_cast<const T *>(a.draft) + b * K * (int64_t)V;
+  const int g_lo = rank * a.groups_per_slice;
+  const int g_hi = min(a.num_groups, g_lo + a.groups_per_slice);
+  const float lam = a.lam[b];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool decider = rank == 0 && warp == 0;
+  float4 *part = g_seq_smem;                             // [K+1][S]
+  int *pre_x = reinterpret_cast<int *>(part + (K + 1) * S);  // [kSeqMaxPositions]
+  float *pre_u = reinterpret_cast<float *>(pre_x + kSeqMaxPositions);  // [kSeqMaxPositions]
+  float *pre_ur = pre_u + kSeqMaxPositions;
+  // the decision inputs, copied into shared memory while the rows stream
+  if (decider) {
+    for (int j = lane; j < K; j += 32) {
+      cp_async4(pre_x + j, a.tokens + b * K + j);
+      cp_async4(pre_u + j, a.u_accept + b * K + j);
+    }
+    if (lane == 0) cp_async4(pre_ur, a.u_resample + b);
+  }
+
+  // ------------------------------------------------- statistics of every position
+  // The sequence's rows as one range of work units (a pair position's group
+  // is kSeqPairUnits units, a bonus-row group 1), cut into S equal contiguous parts: CTA
+  // `rank` streams its part -- long runs of at most a few positions, like a
+  // one-position cluster's slice -- and contributes a partial to every
+  // position its part touches (the identity to the others).
+  float4 *part0 = cluster.map_shared_rank(part, 0);
+  {
+    // this part: from group g_first of position i_first to group g_last
+    // (exclusive) of position i_last
+    const int G = a.num_groups;
+    int i_first, g_first, i_last, g_last;
+    {
+      const int64_t total = ((int64_t)kSeqPairUnits<MODE> * K + 1) * G;
+      const int64_t per = (total + S - 1) / S;
+      const int64_t u_lo = min(total, (int64_t)rank * per), u_hi = min(total, u_lo + per);
+      auto locate = [&](int64_t u, int &i, int &g) {  // the first group at or after unit u
+        const int64_t ip = u / ((int64_t)kSeqPairUnits<MODE> * G);
+        i = ip < K ? (int)ip : K;
+        const int upg = i < K ? kSeqPairUnits<MODE> : 1;
+        g = (int)((u - (int64_t)kSeqPairUnits<MODE> * i * G + upg - 1) / upg);
+      };
+      locate(u_lo, i_first, g_first);
+      locate(u_hi, i_last, g_last);
+      if (g_last == 0 && i_last > i_first) {  // the part ends at a position boundary
+        --i_last;
+        g_last = G;
+      }
+    }
+    for (int i = (int)threadIdx.x; i <= K; i += kNT)  // positions this part does not touch
+      if (i < i_first || i > i_last) part0[i * S + rank] = make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+    for (int i = i_first; i <= i_last; ++i) {
+      const int gl = i == i_first ? g_first : 0, gh = i == i_last ? g_last : G;
+      // The bonus row alone streams its two halves as the two rows of a
+      // plain pair (as many loads in flight as a pair position; lambda 0
+      // makes the logit rule's fold the plain one), then the groups left
+      // over -- an odd one, and the row's partial last group, whose bounds
+      // check needs its own index -- as a single row; the statistics of the
+      // pieces are merged.
+      const bool bonus = i == K;
+      const int gp = (bonus && gh == G && V % Elem<T>::kPerVec != 0) ? gh - 1 : gh;
+      const int h = bonus ? (gp > gl ? (gp - gl) / 2 : 0) : gh - gl;
+      const T *rowA = tgt + (int64_t)i * V;
+      float mA = -INFINITY, sA = 0.0f, mB = -INFINITY, sB = 0.0f;
+      for (int c = 0; c < (bonus ? 2 : 1); ++c) {
+        const bool pr = c == 0;
+        const T *rowB = bonus ? rowA + (int64_t)h * Elem<T>::kPerVec : dft + (int64_t)i * V;
+        float a0 = -INFINITY, a1 = 0.0f, b0 = -INFINITY, b1 = 0.0f;
+        slice_stats<T, MODE, ALIGNED, kNT, kUnroll>(rowA, rowB, pr, bonus ? 0.0f : lam, V,
+                                                    pr ? gl : gl + 2 * h, pr ? gl + h : gh, a0, a1,
+                                                    b0, b1);
+        if (bonus) {
+          merge_stats(mA, sA, a0, a1);
+          merge_stats(mA, sA, b0, b1);
+        } else {
+          mA = a0;
+          sA = a1;
+          mB = b0;
+          sB = b1;
+        }
+      }
+      block_merge_stats<kNT>(sh.bs, mA, sA, mB, sB);
+      if (threadIdx.x == 0) part0[i * S + rank] = make_float4(mA, sA, mB, sB);
+    }
+  }
+  // the logits at the first 32 drafted tokens, in flight during the barrier
+  float zt_pre = 0.0f, zq_pre = 0.0f;
+  if (decider) {
+    cp_async_wait_all();
+    __syncwarp();
+    const int x = lane < K ? pre_x[lane] : -1;
+    if (x >= 0 && x < V) {
+      zt_pre = Elem<T>::load(tgt + (int64_t)lane * V + x);
+      zq_pre = Elem<T>::load(dft + (int64_t)lane * V + x);
+    }
+  }
+  cluster.sync();  // every rank's partials of every position are in rank 0's shared memory
+
+  // ------------------------------------------------- decisions (rank 0, warp 0)
+  if (decider) {
+    const bool lam_ok = lambda_valid(lam);
+    bool lane_ok = true;
+    int n = K;
+    float4 st0 = make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);  // position `lane`'s statistics
+    for (int i0 = 0; i0 < K; i0 += 32) {
+      const int j = i0 + lane;
+      bool rejected = false;
+      if (j < K) {
+        const int x = pre_x[j];
+        const bool tok_ok = x >= 0 && x < V;
+        lane_ok = lane_ok && tok_ok;
+        PosStats st;
+        merge_stats2_n(S, [&](int r) { return part[j * S + r]; }, st.mA, st.sA, st.mB, st.sB);
+        if (i0 == 0) st0 = make_float4(st.mA, st.sA, st.mB, st.sB);
+        if (tok_ok && lam_ok) {
+          const float zt_x = i0 == 0 ? zt_pre : Elem<T>::load(tgt + (int64_t)j * V + x);
+          const float zq_x = i0 == 0 ? zq_pre : Elem<T>::load(dft + (int64_t)j * V + x);
+          float px = 0.0f, qx = 0.0f;
+          const float ratio =
+              accept_ratio(MODE, st, zt_x, zq_x, lam, a.dbg_ptilde ? &px : nullptr, &qx);
+          rejected = !accept_test(pre_u[j], ratio);
+          if (a.dbg_ptilde) a.dbg_ptilde[b * K + j] = px;
+          if (a.dbg_q) a.dbg_q[b * K + j] = qx;
+        }
+      }
+      const unsigned rej = __ballot_sync(0xffffffffu, rejected);
+      if (rej != 0u && n == K) n = i0 + __ffs(rej) - 1;
+    }
+    const bool valid = lam_ok && __all_sync(0xffffffffu, lane_ok);  // every lane votes
+    if (a.dbg_lse) {
+      for (int j = lane; j <= K; j += 32) {
+        float m0, s0, m1, s1;
+        merge_stats2_n(S, [&](int r) { return part[j * S + r]; }, m0, s0, m1, s1);
+        a.dbg_lse[(b * (K + 1) + j) * 2 + 0] = m0 + lg2(s0) * kLn2;
+        a.dbg_lse[(b * (K + 1) + j) * 2 + 1] = j < K ? m1 + lg2(s1) * kLn2 : 0.0f;
+      }
+    }
+    for (int j = lane; j <= K; j += 32) {
+      int out = -1;
+      if (valid && j < n) out = pre_x[j];
+      if (!valid || j != n) a.out_tokens[b * (K + 1) + j] = out;
+    }
+    // the statistics of the drawn row: lane n's (a rejected position < 32),
+    // else merged again (the bonus row, or a rejection past the first 32)
+    const int nd = valid ? n : 0;
+    float4 sn;
+    sn.x = __shfl_sync(0xffffffffu, st0.x, nd & 31);
+    sn.y = __shfl_sync(0xffffffffu, st0.y, nd & 31);
+    sn.z = __shfl_sync(0xffffffffu, st0.z, nd & 31);
+    sn.w = __shfl_sync(0xffffffffu, st0.w, nd & 31);
+    if (nd >= 32 || nd == K)
+      merge_stats2_n(S, [&](int r) { return part[nd * S + r]; }, sn.x, sn.y, sn.z, sn.w);
+    Broadcast bc;
+    bc.n = valid ? n : -1;
+    bc.u = *pre_ur;
+    bc.sp = make_sample_params_rn(sn.x, sn.y, sn.z, sn.w, lam);
+    bc.kind = n == K ? kWBonus : residual_kind<MODE>(lam);
+    if (lane == 0) a.out_n[b] = bc.n;
+    if (lane < S) *cluster.map_shared_rank(&sh.bc, lane) = bc;
+  }
+  cluster.sync();  // the decision is in every rank
+  const Broadcast bc = sh.bc;
+  if (bc.n < 0) return;  // invalid input: every output is -1 already
+  const T *sA_row = tgt + (int64_t)bc.n * V;
+  const T *sB_row = dft + (int64_t)(bc.n < K ? bc.n : 0) * V;
+  draw_token<T, MODE, ALIGNED>(sh, cluster, S, rank, sA_row, sB_row, V, g_lo, g_hi,
+                               a.seg_tiles * kSegGroups, a.segs_per_slice, bc.kind, bc.sp, bc.u,
+                               a.out_tokens + b * (K + 1) + bc.n);
+}
+
 // Greedy verification with the same decomposition (one cluster per position,
 // rank r streams slice r): each rank finds the argmax of the mixed logits
 // w = z_t + lambda (z_q - z_t) over its slice (target row K alone at the bonus
@@ -693,6 +898,23 @@ cudaError_t launch_sample_one(const RowArgs &a, int S, int64_t grid, cudaStream_
 }
 
 template <typename T, int MODE, bool ALIGNED>
+cudaError_t launch_seq_one(const RowArgs &a, int S, int64_t grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kNT, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)seq_smem_bytes(a.K, S);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rows_seq_kernel<T, MODE, ALIGNED>, a);
+}
+
+template <typename T, int MODE, bool ALIGNED>
 cudaError_t prepare_one() {
   cudaError_t e = cudaFuncSetAttribute(row_kernel_of<T, MODE, ALIGNED>(),
                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -705,6 +927,13 @@ cudaError_t prepare_one() {
     const cudaError_t e2 = cudaFuncSetAttribute(rows_sample_kernel<T, MODE, ALIGNED>,
                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess) e = e2;
+    const cudaError_t e3 = cudaFuncSetAttribute(rows_seq_kernel<T, MODE, ALIGNED>,
+                                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) e = e3;
+    const cudaError_t e4 = cudaFuncSetAttribute(rows_seq_kernel<T, MODE, ALIGNED>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)seq_smem_bytes(kSeqMaxPositions - 1, kMaxCluster));
+    if (e == cudaSuccess) e = e4;
   }
   return e;
 }
@@ -773,6 +1002,23 @@ cudaError_t rows_sample_launch(const RowArgs &a, int dtype_bf16, int mode, bool 
                    : launch_sample_one<float, kProbMix, false>(a, S, grid, stream);
   return aligned ? launch_sample_one<float, kLogitMix, true>(a, S, grid, stream)
                  : launch_sample_one<float, kLogitMix, false>(a, S, grid, stream);
+}
+
+cudaError_t rows_seq_launch(const RowArgs &a, int dtype_bf16, int mode, bool aligned, int S,
+                            cudaStream_t stream) {
+  const int64_t grid = a.B * (int64_t)S;
+  if (dtype_bf16) {
+    if (mode == kProbMix)
+      return aligned ? launch_seq_one<uint16_t, kProbMix, true>(a, S, grid, stream)
+                     : launch_seq_one<uint16_t, kProbMix, false>(a, S, grid, stream);
+    return aligned ? launch_seq_one<uint16_t, kLogitMix, true>(a, S, grid, stream)
+                   : launch_seq_one<uint16_t, kLogitMix, false>(a, S, grid, stream);
+  }
+  if (mode == kProbMix)
+    return aligned ? launch_seq_one<float, kProbMix, true>(a, S, grid, stream)
+                   : launch_seq_one<float, kProbMix, false>(a, S, grid, stream);
+  return aligned ? launch_seq_one<float, kLogitMix, true>(a, S, grid, stream)
+                 : launch_seq_one<float, kLogitMix, false>(a, S, grid, stream);
 }
 
 }  // namespace specv

@@ -166,6 +166,15 @@ __device__ __forceinline__ bool slice_stats(const T *rowA, const T *rowB, bool p
   return false;
 }
 
+// Asynchronous 4-byte copy from global into shared memory (no register
+// holds the value while it is in flight); cp_async_wait_all waits for every
+// copy this thread issued.
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+  const unsigned dst = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Greedy: folds one 16-byte group (elements idx0, idx0 + 1, ...) into this
 // thread's candidate (best, bidx).  A thread visits its groups in increasing
 // index order, so the first maximum in index order is kept by taking a group

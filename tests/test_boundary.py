@@ -115,12 +115,33 @@ def test_plan_cluster_size_model(lib):
     positions: S = 3 fills one wave where S = 4 needs two)."""
     assert specv.plan(256, 8, 128256, specv.F32)["cluster"] == 2
     assert specv.plan(256, 8, 128256, specv.F32, specv.GREEDY)["cluster"] == 2
-    p3 = specv.plan(32, 5, 152064, specv.BF16)
+    p3 = specv.plan(32, 5, 152064, specv.BF16, specv.GREEDY)
     assert p3["kernel"] == "rows-stream" and p3["cluster"] == 3 and p3["ctas"] == 192 * 3
-    assert specv.plan(32, 5, 152064, specv.BF16, specv.GREEDY)["cluster"] == 3
     for B, K, V, dt in [(16, 8, 128256, 0), (64, 4, 32000, 1), (8, 4, 128256, 1), (3, 2, 9000, 0)]:
         S = specv.plan(B, K, V, dt)["cluster"]
         assert 1 <= S <= 16
+
+
+def test_plan_sequence_clusters(lib, monkeypatch):
+    """Sampling grids of about one wave with 19 to 38 sequences (on 152 SMs)
+    run one cluster of 16 CTAs per sequence (at least 4 KiB of each row per
+    CTA) and need no scratch; SPECV_SAMPLE_SPLIT forces the two-launch
+    streaming plan, and greedy verification never uses it."""
+    monkeypatch.delenv("SPECV_SAMPLE_SPLIT", raising=False)
+    for mode in (specv.PROB_MIX, specv.LOGIT_MIX):
+        p3 = specv.plan(32, 5, 152064, specv.BF16, mode)
+        assert p3 == {"kernel": "rows-seq", "cluster": 16, "ctas": 512, "workspace_bytes": 0,
+                      "early_exit": False, "split_draws": False}
+    assert specv.plan(24, 6, 40001, specv.F32)["kernel"] == "rows-seq"     # unaligned rows
+    assert specv.plan(38, 3, 65536, specv.BF16)["kernel"] == "rows-seq"    # 16 x 38 CTAs: one wave
+    assert specv.plan(40, 3, 65536, specv.BF16)["kernel"] == "rows-stream"  # clusters under 16
+    assert specv.plan(150, 2, 16384, specv.BF16)["kernel"] == "rows-stream"
+    assert specv.plan(8, 4, 128256, specv.BF16)["kernel"] != "rows-seq"     # too few sequences
+    assert specv.plan(256, 8, 128256, specv.F32)["kernel"] == "rows-stream"  # many waves
+    assert specv.plan(40, 3, 4096, specv.F32)["kernel"] != "rows-seq"       # short rows
+    monkeypatch.setenv("SPECV_SAMPLE_SPLIT", "1")
+    p = specv.plan(32, 5, 152064, specv.BF16)
+    assert p["kernel"] == "rows-stream" and p["cluster"] == 3 and p["split_draws"]
 
 
 def test_plan_early_exit(lib, monkeypatch):
@@ -132,8 +153,8 @@ def test_plan_early_exit(lib, monkeypatch):
     for mode in (specv.PROB_MIX, specv.LOGIT_MIX, specv.GREEDY):
         p4 = specv.plan(256, 8, 128256, specv.F32, mode)
         assert p4["early_exit"] and not p4["split_draws"]
-    p3 = specv.plan(32, 5, 152064, specv.BF16)
-    assert not p3["early_exit"] and p3["split_draws"]
+    p3 = specv.plan(32, 5, 152064, specv.BF16, specv.GREEDY)
+    assert not p3["early_exit"] and not p3["split_draws"]
     assert not specv.plan(1, 8, 128256, specv.BF16)["early_exit"]       # resident
     assert not specv.plan(1_000_000, 4, 32, specv.F32)["early_exit"]    # TMA tile
     ws_on = specv.plan(256, 8, 128256, specv.F32)["workspace_bytes"]

@@ -402,3 +402,49 @@ def test_streams_and_graph_capture_share_nothing_wrongly(specv):
             g.replay()
             torch.cuda.synchronize()
             assert torch.equal(tok, ref[0][0]) and torch.equal(nn, ref[0][1])
+
+
+SEQ_SHAPES = [
+    # (B, K, V, dtype, structure): grids of about one wave with one cluster per sequence
+    (32, 5, 152064, "bf16", "rho:3.0:0.5:0.95"),        # the Qwen-shaped workload
+    (38, 3, 65536, "bf16", "half_equal:3.0:0.85:1.0"),  # half the sequences draw the bonus
+    (20, 12, 65536, "f32", "corr:3.0:0.85:1.0"),
+    (19, 32, 32768, "bf16", "half_equal:3.0:0.9:0.5"),  # 33 positions: more than a warp's lanes
+    (24, 6, 40001, "bf16", "corr:2.0:0.8:1.0"),         # rows off 16-byte boundaries
+    (30, 4, 40001, "f32", "half_equal:3.0:0.85:1.0"),
+    (32, 2, 4099 * 8, "f32", "corr:2.0:0.8:1.0"),       # parts ending inside the bonus row
+]
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+@pytest.mark.parametrize("shape", SEQ_SHAPES, ids=lambda s: f"B{s[0]}K{s[1]}V{s[2]}{s[3]}")
+def test_sequence_cluster_kernel(specv, cluster_env, shape, mode):
+    """One cluster per sequence: every position streamed, decided and the token
+    drawn in one launch; decisions and probabilities against the oracle."""
+    B, K, V, dt, st = shape
+    plan = specv.plan(B, K, V, 1 if dt == "bf16" else 0, mode)
+    assert plan["kernel"] == "rows-seq" and plan["workspace_bytes"] == 0, plan
+    w = workloads.Workload("seq", B, K, V, dt, st, ("uniform", 0.0, 0.6), 43)
+    x = workloads.make_inputs(w, DEV)
+    rep, tok, n = _check(specv, x, mode)
+    if st.startswith("half_equal"):
+        assert (n[B // 2:] == K).all()
+    print(f"{shape} mode={mode} plan={plan}: {rep}")
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["prob", "logit"])
+def test_sequence_cluster_kernel_whole_rows_and_invalid_inputs(specv, mode):
+    w = workloads.Workload("seq", 38, 3, 65536, "bf16", "corr:3.0:0.85:1.0", (0.3,), 44)
+    x = workloads.make_inputs(w, DEV)
+    x["draft_tokens"][1, 2] = w.V
+    x["lam"][3] = float("nan")
+    args = (x["target_logits"], x["draft_logits"], x["draft_tokens"], x["u_accept"],
+            x["u_resample"], x["lam"])
+    dbg = specv.verify_debug(*args, mode=mode)
+    torch.cuda.synchronize()
+    n = dbg["n_accepted"].cpu().numpy()
+    tok = dbg["tokens"].cpu().numpy()
+    assert n[1] == -1 and n[3] == -1 and (tok[[1, 3]] == -1).all()
+    xh = _parity.to_host(x)
+    _parity.compare(xh, mode, tok, n, _parity.run_oracle(xh, mode))
+    _parity.check_rows(xh, mode, dbg, seqs=[0, 37])
