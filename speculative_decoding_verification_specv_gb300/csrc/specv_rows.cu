@@ -535,8 +535,21 @@ extern __shared__ float4 g_seq_smem[];
 template <int MODE>
 constexpr int kSeqPairUnits = MODE == kLogitMix ? 3 : 2;
 
-__host__ __device__ constexpr int64_t seq_smem_bytes(int K, int S) {
-  return (int64_t)(K + 1) * S * 16 + (2 * kSeqMaxPositions + 4) * 4;
+// The logit rule's parts of aligned rows stream through a ring of per-thread
+// asynchronous copies (slice_stats_staged, kSeqDepth groups per row in
+// flight), the others with batches of register loads: measured at B = 32,
+// K = 5, V = 152064 bf16 (GB300, one launch per step after an L2 flush), the
+// ring gave 47.6 against 51.2 us in the logit rule but 41.5 against 41.1 us
+// in the probability rule, whose lighter arithmetic the one-group folds of
+// the ring outweigh.
+constexpr int kSeqDepth = 4;
+constexpr int kSeqRing = (kSeqDepth + 1) * 2 * kNT;  // 16-byte slots of the copy ring
+template <int MODE, bool ALIGNED>
+__host__ __device__ constexpr bool seq_staged() { return ALIGNED && MODE == kLogitMix; }
+
+__host__ __device__ constexpr int64_t seq_smem_bytes(int K, int S, bool staged) {
+  return (staged ? (int64_t)kSeqRing * 16 : 0) + (int64_t)(K + 1) * S * 16 +
+         (2 * kSeqMaxPositions + 4) * 4;
 }
 
 template <typename T, int MODE, bool ALIGNED>
@@ -554,7 +567,8 @@ __global__ void __launch_bounds__(kNT, 4) rows_seq_kernel(RowArgs a) {
   const float lam = a.lam[b];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool decider = rank == 0 && warp == 0;
-  float4 *part = g_seq_smem;                             // [K+1][S]
+  uint4 *ring = reinterpret_cast<uint4 *>(g_seq_smem);  // [kSeqDepth + 1][2][kNT] when staged
+  float4 *part = g_seq_smem + (seq_staged<MODE, ALIGNED>() ? kSeqRing : 0);  // [K+1][S]
   int *pre_x = reinterpret_cast<int *>(part + (K + 1) * S);  // [kSeqMaxPositions]
   float *pre_u = reinterpret_cast<float *>(pre_x + kSeqMaxPositions);  // [kSeqMaxPositions]
   float *pre_ur = pre_u + kSeqMaxPositions;
@@ -615,7 +629,12 @@ __global__ void __launch_bounds__(kNT, 4) rows_seq_kernel(RowArgs a) {
         const bool pr = c == 0;
         const T *rowB = bonus ? rowA + (int64_t)h * Elem<T>::kPerVec : dft + (int64_t)i * V;
         float a0 = -INFINITY, a1 = 0.0f, b0 = -INFINITY, b1 = 0.0f;
-        slice_stats<T, MODE, ALIGNED, kNT, kUnroll>(rowA, rowB, pr, bonus ? 0.0f : lam, V,
+        if constexpr (seq_staged<MODE, ALIGNED>())
+          slice_stats_staged<T, MODE, kNT, kSeqDepth>(rowA, rowB, pr, bonus ? 0.0f : lam,
+                                                      pr ? gl : gl + 2 * h, pr ? gl + h : gh, ring,
+                                                      a0, a1, b0, b1);
+        else
+          slice_stats<T, MODE, ALIGNED, kNT, kUnroll>(rowA, rowB, pr, bonus ? 0.0f : lam, V,
                                                     pr ? gl : gl + 2 * h, pr ? gl + h : gh, a0, a1,
                                                     b0, b1);
         if (bonus) {
@@ -902,7 +921,7 @@ cudaError_t launch_seq_one(const RowArgs &a, int S, int64_t grid, cudaStream_t s
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kNT, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)seq_smem_bytes(a.K, S);
+  cfg.dynamicSmemBytes = (size_t)seq_smem_bytes(a.K, S, seq_staged<MODE, ALIGNED>());
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -932,7 +951,7 @@ cudaError_t prepare_one() {
     if (e == cudaSuccess) e = e3;
     const cudaError_t e4 = cudaFuncSetAttribute(rows_seq_kernel<T, MODE, ALIGNED>,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)seq_smem_bytes(kSeqMaxPositions - 1, kMaxCluster));
+                                                (int)seq_smem_bytes(kSeqMaxPositions - 1, kMaxCluster, true));
     if (e == cudaSuccess) e = e4;
   }
   return e;

@@ -166,6 +166,57 @@ __device__ __forceinline__ bool slice_stats(const T *rowA, const T *rowB, bool p
   return false;
 }
 
+// Asynchronous 16-byte copy from global into shared memory, cached in L2
+// only; copies are committed and waited on in groups.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const unsigned dst = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// slice_stats over groups [g_lo, g_hi) of 16-byte aligned rows with the loads
+// decoupled from the arithmetic: each thread keeps its next D groups of each
+// row in flight as asynchronous copies into its own slots of a ring in
+// shared memory (ring: [D + 1][2][NT] 16-byte slots; a slot is refilled only
+// after the fold of the group it held, so no copy lands on a value still
+// being read), instead of a batch of register loads that drains before the
+// next is issued.  No thread reads another thread's slots: no barrier.
+template <typename T, int MODE, int NT, int D>
+__device__ __forceinline__ void slice_stats_staged(const T *rowA, const T *rowB, bool pair,
+                                                   float lam, int g_lo, int g_hi, uint4 *ring,
+                                                   float &mA, float &sA, float &mB, float &sB) {
+  constexpr int VW = Elem<T>::kPerVec;
+  const int tid = (int)threadIdx.x;
+  int gi = g_lo + tid;  // the next group to copy
+  auto issue = [&](int slot) {
+    if (gi < g_hi) {
+      cp_async16(&ring[(slot * 2) * NT + tid], rowA + (int64_t)gi * VW);
+      if (pair) cp_async16(&ring[(slot * 2 + 1) * NT + tid], rowB + (int64_t)gi * VW);
+      gi += NT;
+    }
+    cp_async_commit();  // an empty group past the last copy keeps the count uniform
+  };
+#pragma unroll
+  for (int d = 0; d < D; ++d) issue(d);
+  int slot = 0, fill = D;
+  const bool ok[1] = {true};
+  for (int g = g_lo + tid; g < g_hi; g += NT) {
+    cp_async_wait<D - 1>();  // the oldest copy group (this group's) has landed
+    uint4 za[1], zb[1];
+    za[0] = ring[(slot * 2) * NT + tid];
+    if (pair) zb[0] = ring[(slot * 2 + 1) * NT + tid];
+    issue(fill);  // the slot folded in the previous step
+    fold_batch<T, MODE, 1>(za, zb, ok, pair, lam, mA, sA, mB, sB);
+    slot = slot == D ? 0 : slot + 1;
+    fill = fill == D ? 0 : fill + 1;
+  }
+  cp_async_wait<0>();
+}
+
 // Asynchronous 4-byte copy from global into shared memory (no register
 // holds the value while it is in flight); cp_async_wait_all waits for every
 // copy this thread issued.
