@@ -404,6 +404,7 @@ def run_per_config(specv, dev, args, l2_bytes):
                     "rows_per_s": w.B * w.K / (ms / 1e3), "algorithmic_bytes": alg,
                     "hbm_gbs": gbs, "frac": gbs / peak, "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
                     "every_row_frac": w.roofline_bytes / (ms / 1e3) / 1e9 / peak,
+                    "traffic": profiled_traffic(w.name, mname) if not env else None,
                     "mean_accepted": mean_n, "plan": plan, "steps": steps,
                     "gpu_launches": steps * launches_per_step(plan),
                     "l2": "flushed before every step" if flushed else "inputs > L2"})
