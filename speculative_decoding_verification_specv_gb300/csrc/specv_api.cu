@@ -283,7 +283,7 @@ specv_status make_plan(int64_t B, int32_t K, int32_t V, int dtype, int mode, int
       // row tasks (2K+1 per sequence) for the CTA's threads; at most one
       // stage-B lane group per sequence
       ts = (int)(kTmaTileTargetBytes / data_bytes);
-      const int by_rows = specv::kTileThreads / (2 * K + 1);
+      const int by_rows = specv::kTmaTileThreads / (2 * K + 1);
       if (ts > by_rows && by_rows >= 1) ts = by_rows;
       if (ts > specv::kTmaTileMaxSeqs) ts = specv::kTmaTileMaxSeqs;
       if (ts < 1) ts = 1;
@@ -1097,8 +1097,8 @@ specv_status verify_host_early_exit(const void *target, const void *draft, const
   while (S > 1 && Bg * S > INT32_MAX) S /= 2;
   if (Bg * S > INT32_MAX) return SPECV_ERR_UNSUPPORTED;
   const bool aligned = row % 16 == 0;
-  int level[kEeGroups];
-  bool active[kEeGroups];
+  int level[kEeGroups] = {};
+  bool active[kEeGroups] = {};
 
   // level lv of group g: the live members' rows, then (below K) the decision
   // pass and the read-back of the group's flags, all on the group's stream

@@ -13,8 +13,9 @@ void note_cuda_error(cudaError_t e);
 constexpr int kRowThreads = 256;   // threads per CTA of the cluster row kernel
 constexpr int kMaxCluster = 16;    // largest cluster (non-portable size, opt-in)
 constexpr int kTileThreads = 256;  // threads per CTA of the small-vocabulary kernel
-constexpr int kTmaTileLanes = 8;           // stage-B lanes per sequence of the TMA tile kernel
-constexpr int kTmaTileMaxSeqs = kTileThreads / kTmaTileLanes;  // sequences per TMA tile (32)
+constexpr int kTmaTileThreads = 256;  // threads per CTA of the TMA tile kernel
+constexpr int kTmaTileLanes = 4;      // stage-B lanes per sequence of the TMA tile kernel
+constexpr int kTmaTileMaxSeqs = kTmaTileThreads / kTmaTileLanes;  // sequences per TMA tile
 constexpr int kResidentChunkGroups = 1024;  // 16-byte groups per TMA chunk (16 KiB per row)
 constexpr int kResidentMaxChunks = 8;       // chunks per row slice (128 KiB per row at most)
 

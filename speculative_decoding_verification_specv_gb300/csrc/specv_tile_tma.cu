@@ -11,11 +11,16 @@
 //            per-position offset (the same for the target and draft row of a
 //            position, so identical rows give identical statistics) that
 //            spreads simultaneous reads over the banks;
-//   stage B: a group of kLanes lanes per sequence (kLanes = 8; four
+//   stage B: a group of kLanes lanes per sequence (kLanes = 4; eight
 //            sequences per warp in lockstep): lanes 0..K-1 of the group test
-//            positions 0..K-1, a ballot gives the first rejection, and the
-//            inverse CDF is a segmented scan across the group, each lane
-//            owning a contiguous run of 16-byte groups of the row.
+//            positions 0..K-1 (in rounds of kLanes), a ballot gives the first
+//            rejection, and the inverse CDF is a segmented scan across the
+//            group, each lane owning a contiguous run of 16-byte groups of
+//            the row.  Measured at B = 10^6, K = 4, V = 32 fp32 against 8
+//            lanes per sequence: probability 239.2 vs 252.3 us, logit 281.7
+//            vs 297.5 us, greedy 228.7 vs 231.0 us (the per-lane fixed work
+//            of a sequence -- sampler parameters, scan, ballots -- is done by
+//            half as many lanes).
 // The per-sequence scalars (tokens, uniforms, lambda) are loaded into
 // registers before stage A so their latency overlaps it.  No scratch memory.
 #include <climits>
@@ -28,7 +33,7 @@ namespace specv {
 
 namespace {
 
-constexpr int kNT = kTileThreads;
+constexpr int kNT = kTmaTileThreads;
 constexpr int kLanes = kTmaTileLanes;          // lanes per sequence in stage B
 
 template <typename T>
@@ -114,7 +119,9 @@ template <typename T, int MODE>
 __global__ void __launch_bounds__(kNT) tile_tma_kernel(TileArgs a) {
   constexpr bool GREEDY = MODE == kGreedy;  // argmax per row; no draft-row tasks, no sampling
   constexpr int VW = Elem<T>::kPerVec;
-  constexpr int kCacheC = 1;  // stage-B groups per lane whose weights are kept
+  // stage-B groups per lane whose weights are kept in registers (two fp32
+  // groups fit the 64 registers of four CTAs per SM; two bf16 groups do not)
+  constexpr int kCacheC = sizeof(T) == 4 ? 2 : 1;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
   const int K = a.K, V = a.V, TS = a.tile_seqs;
