@@ -182,10 +182,16 @@ def capture_graph(launch, dev):
 
 
 def kernel_source_hash():
+    """Hash of the row kernels' code: comments and whitespace are left out, so
+    that a profile's traffic stays attached to the code it was measured on."""
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)  # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -522,9 +522,10 @@ __global__ void __launch_bounds__(kNT, 4) rows_sample_kernel(RowArgs a) {
 // token at n is then drawn by the whole cluster from its slices of row pair
 // n (or of target row K) -- the rows were streamed moments ago, so the second
 // read hits L2 -- with no second launch, no scratch memory and no arrival
-// counter.  Dynamic shared memory: the partials [K+1][S] of every rank (used
-// in rank 0), then the drafted tokens, acceptance uniforms and the resample
-// uniform of the sequence (copied in by rank 0's first warp).
+// counter.  Dynamic shared memory: the copy ring (logit rule, aligned rows;
+// see seq_staged), the partials [K+1][S] of every rank (used in rank 0), then
+// the drafted tokens, acceptance uniforms and the resample uniform of the
+// sequence (copied in by rank 0's first warp).
 extern __shared__ float4 g_seq_smem[];
 
 // Work units of one group of a pair position against one group of the bonus
