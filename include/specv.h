@@ -27,8 +27,11 @@
  * Conventions for every entry point:
  *   - All array pointers are DEVICE pointers to contiguous row-major memory
  *     owned by the caller; the library never frees or retains them.  The
- *     only memory the library allocates is a small scratch workspace for the
- *     row kernels (16*B*(K+1) + 4*B bytes at most), one per (device, stream):
+ *     device memory the library allocates is a scratch workspace for the
+ *     row kernels (the streaming kernel's: 16*B*(K+1) bytes of position
+ *     statistics, at most 8*B*16*512 bytes of bonus-row segment statistics,
+ *     8*B bytes of counters; the other kernels need less or none), plus the
+ *     host-buffer calls' staging (see specv_verify_host), one per (device, stream):
  *     created on the first call on that stream that needs it, reused by
  *     every later call on the stream (calls on one stream are ordered, so
  *     they never overlap), kept until the process exits.  A call made while
@@ -43,7 +46,10 @@
  *   - Device-side input errors (a draft token outside [0, V), or lambda
  *     outside [0, 1] or NaN) set out_n_accepted[b] = -1 and fill
  *     out_tokens[b][0..K] with -1.  No trap, no assert.
- *   - NaN or +-inf logits: behaviour unspecified (no fault).
+ *   - A -inf logit masks its entry (probability 0; in the logit mixture a
+ *     -inf term of positive weight masks the mixed entry, a term of weight 0
+ *     drops out; a drafted token masked in the draft row is accepted iff
+ *     p~(x) > 0).  NaN or +inf logits: behaviour unspecified (no fault).
  *   - Uniforms are taken as given; values in [0, 1) give the documented
  *     distribution.
  */
@@ -96,12 +102,16 @@ typedef enum {
  *                                      or bonus (n = K) token at index n, then -1
  *   out_n_accepted [B]          int32  n = number of accepted drafts (0..K), -1 if invalid
  *
- * Each logit is read from HBM once.  With the resident row kernel the
- * replacement or bonus token is drawn from the copy of the row held in
- * shared memory; with the streaming row kernel (misaligned rows, or slices
- * too large for shared memory) the rejected row pair or the bonus row is
- * read a second time, usually from L2.  out_n_accepted[b] = -2 reports an
- * internal copy timeout (a bounded wait that expired; not expected).
+ * Each logit is read from HBM at most once for the statistics; on batches of
+ * several waves of CTAs the rows after a sequence's first rejection are not
+ * read at all (early exit, specv_plan_flags).  With the resident row kernel
+ * and the tile kernels the replacement or bonus token is drawn from the copy
+ * of the row held in shared memory; with the sequence-cluster kernel the
+ * rejected row pair is read a second time from L2 right after it streamed;
+ * with the streaming row kernel the rejected pair is read a second time
+ * (from HBM on batches of many waves) and the bonus row only for the one
+ * segment its draw lands in.  out_n_accepted[b] = -2 reports an internal
+ * copy timeout (a bounded wait that expired; not expected).
  */
 specv_status specv_verify(const void *target_logits, const void *draft_logits,
                           const int32_t *draft_tokens, const float *u_accept,
