@@ -142,6 +142,14 @@ def test_plan_sequence_clusters(lib, monkeypatch):
     monkeypatch.setenv("SPECV_SAMPLE_SPLIT", "1")
     p = specv.plan(32, 5, 152064, specv.BF16)
     assert p["kernel"] == "rows-stream" and p["cluster"] == 3 and p["split_draws"]
+    monkeypatch.delenv("SPECV_SAMPLE_SPLIT")
+    # the edges of the rule on 152 SMs: 2 to 4 CTAs per SM, K + 1 <= 64, >= 4 KiB of a row per CTA
+    seq = lambda B, K, V, dt: specv.plan(B, K, V, dt)["kernel"] == "rows-seq"
+    assert not seq(18, 5, 152064, specv.BF16) and seq(19, 5, 152064, specv.BF16)
+    assert seq(38, 5, 152064, specv.BF16) and not seq(39, 5, 152064, specv.BF16)
+    assert seq(19, 63, 32768, specv.BF16) and not seq(19, 64, 32768, specv.BF16)
+    assert seq(32, 5, 32768, specv.BF16) and not seq(32, 5, 32760, specv.BF16)
+    assert seq(32, 5, 16384, specv.F32) and not seq(32, 5, 16376, specv.F32)
 
 
 def test_plan_early_exit(lib, monkeypatch):
