@@ -211,3 +211,21 @@ def test_host_binding_checks_tensors():
         specv.verify_host(*bad.values(), **outs)
     with pytest.raises(ValueError):  # CUDA-side entry point on host tensors
         specv.verify(*x.values())
+
+
+def test_random_shape_families_reach_their_plans(lib):
+    """The families of the random-shape GPU parity cases are what they say:
+    every family is planned as named at least once (greedy shapes of the
+    sampling-only plans go to the streaming kernel)."""
+    from tests.test_gpu_random_shapes import FAMILIES, N_CASES, _draw_case
+    seen = set()
+    for seed in range(N_CASES):
+        fam, w, mode = _draw_case(seed)
+        p = specv.plan(w.B, w.K, w.V, specv.BF16 if w.dtype == "bf16" else specv.F32, mode)
+        name = p["kernel"]
+        if name == "rows-stream":
+            name = ("rows-stream-split" if p["split_draws"] else
+                    "rows-stream-exit" if p["early_exit"] else "rows-stream")
+        if name == fam:
+            seen.add(fam)
+    assert seen == set(FAMILIES), sorted(set(FAMILIES) - seen)
