@@ -117,15 +117,21 @@ __device__ __forceinline__ void chunk_stats(const uint4 *cA, const uint4 *cB, in
 }
 
 // The last cluster of sequence b: first rejection over the position records,
-// then the outputs.  Run by one warp.
+// then the outputs.  Run by one warp.  The records of the first 32 positions
+// and their drafted tokens are loaded together, so that the token at n and
+// the accepted prefix need no second round trip.
 __device__ void finalize_sequence(const ResArgs &a, int64_t b) {
   const int K = a.K;
   const int lane = threadIdx.x & 31;
+  int2 r0 = make_int2(kRecAccepted, -1);
+  int x0 = -1;
+  if (lane <= K) r0 = __ldcg(&a.rec[b * (K + 1) + lane]);
+  if (lane < K) x0 = a.tokens[b * K + lane];
   int n = K, bad = 0;
   for (int j0 = 0; j0 <= K; j0 += 32) {
     const int j = j0 + lane;
     int st = kRecAccepted;
-    if (j <= K) st = __ldcg(&a.rec[b * (K + 1) + j]).x;
+    if (j <= K) st = j0 == 0 ? r0.x : __ldcg(&a.rec[b * (K + 1) + j]).x;
     const unsigned rej = __ballot_sync(0xffffffffu, j < K && st == kRecRejected);
     if (rej != 0u && n == K) n = j0 + __ffs(rej) - 1;
     const bool any_err = __any_sync(0xffffffffu, st == kRecError);  // every lane votes
@@ -138,9 +144,11 @@ __device__ void finalize_sequence(const ResArgs &a, int64_t b) {
     if (lane == 0) a.out_n[b] = bad;
     return;
   }
-  const int tok_n = __ldcg(&a.rec[b * (K + 1) + n]).y;
+  const int tok_lo = __shfl_sync(0xffffffffu, r0.y, n & 31);
+  const int tok_n = n < 32 ? tok_lo : __ldcg(&a.rec[b * (K + 1) + n]).y;
   for (int j = lane; j <= K; j += 32)
-    a.out_tokens[b * (K + 1) + j] = j < n ? a.tokens[b * K + j] : (j == n ? tok_n : -1);
+    a.out_tokens[b * (K + 1) + j] =
+        j < n ? (j < 32 ? x0 : a.tokens[b * K + j]) : (j == n ? tok_n : -1);
   if (lane == 0) a.out_n[b] = n;
 }
 
@@ -312,10 +320,12 @@ __global__ void __launch_bounds__(kNT) resident_kernel(ResArgs a) {
   // -------------------------------------------------------------- publish
   if (threadIdx.x == 0) {
     a.rec[p] = make_int2(status, token);
-    __threadfence();
-    const unsigned prev = atomicAdd(&a.count[b], 1u);
+    // one acquire-release atomic: the record before the count, and for the
+    // last arrival every other position's record after it
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(prev) : "l"(&a.count[b]) : "memory");
     if (prev == (unsigned)K) {
-      __threadfence();
       a.count[b] = 0;  // every position has arrived: leave the counter zero for the next call
       sh.last = 1;
     }
