@@ -260,11 +260,14 @@ __device__ void draw_token(RowsShared &sh, cg::cluster_group &cluster, int S, in
 // (and its own draw, if any) are written: returns 1 for the last of the K + 1
 // positions, which resets the counter and the early-exit word for the next call.
 __device__ __forceinline__ int arrive(const RowArgs &a, int64_t b, int K) {
-  __threadfence();
-  const unsigned prev = atomicAdd(&a.ws_count[b], 1u);
+  // one acquire-release atomic: this position's results (and, through the
+  // cluster barrier before it, its ranks' fenced writes) before the count, and
+  // for the last arrival every other position's results after it
+  unsigned prev;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+               : "=r"(prev) : "l"(&a.ws_count[b]) : "memory");
   const int last = prev == (unsigned)K;
   if (last) {
-    __threadfence();
     a.ws_count[b] = 0;  // every position has arrived: leave the counter zero for the next call
     if (a.ws_reject != nullptr) a.ws_reject[b] = 0;  // and the early-exit word
   }
